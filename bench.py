@@ -1,0 +1,392 @@
+"""Benchmark of the forecast-driven block-sparse decode step on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (one "step" = one decode token for every sequence through the whole stack): 32
+layers, batch 16, context 131072 tokens, 32 query heads / 2 KV heads / head_dim 128, forecast
+projection 4096 -> 256 per layer (layer 0 also has its same-layer head), compression window
+32/16, 64-token blocks, top-32 blocks plus block 0 and the tail block, KV resident in HBM
+(64 GiB), 16 planted high-score blocks per (layer, sequence, group). Inputs are seeded
+synthetic bf16 N(0,1) (weights N(0, 0.02^2)). The K timed steps are consecutive decode
+positions ending at context 131072. Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_LAYERS, BATCH, CTX, G, H, D, HIDDEN, TOPK, PLANTED = 32, 16, 131072, 2, 16, 128, 4096, 32, 16
+METRIC = "decode tok/s @128K ctx (B=16 resident, B=64 offload); select+attn HBM GB/s"
+WORKLOAD = "32-layer forecast-driven block-sparse decode step, batch 16, context 131072, KV resident"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def source_sha(name):
+    path = os.path.join(ROOT, "block_sparse_attention_forecast_gb300", "csrc", name)
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source still
+    matches the one profiled (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            t = json.load(fh)
+    except OSError:
+        return None
+    e = t.get(kernel_file)
+    if not e or e.get("source_sha") != source_sha(kernel_file):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % device_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------- workload
+def build_workload(device, seed, steps_total):
+    import torch
+    import synth
+    import block_sparse_attention_forecast_gb300.binding as sb
+    from block_sparse_attention_forecast_gb300.step import DecodeStack
+
+    shape = sb.Shape(n_groups=G, topk=TOPK, max_ctx=CTX, max_batch=BATCH)
+    T0 = CTX - steps_total + 1          # the last step runs at context CTX
+    nb = CTX // 64
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    W_self0 = synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 1, device, std=0.02)
+    W_next = [synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 2 + L, device, std=0.02)
+              for L in range(N_LAYERS - 1)]
+    h = synth.normal_bf16_device((N_LAYERS, BATCH, HIDDEN), seed * 1000 + 40, device)
+    layers = []
+    import numpy as np
+    for L in range(N_LAYERS):
+        layer = sb.LayerKV.empty(shape, device=device)
+        layer.k.copy_(synth.normal_bf16_device(layer.k.shape, seed * 1000 + 100 + L, device))
+        layer.v.copy_(synth.normal_bf16_device(layer.v.shape, seed * 1000 + 200 + L, device))
+        # planted blocks, shifted along the forecast that selects this layer's blocks
+        Wsel, hsel = (W_self0, h[0]) if L == 0 else (W_next[L - 1], h[L - 1])
+        direction = (hsel.float() @ Wsel.float().T).view(BATCH, G, D)
+        blocks = np.stack([[synth.planted_blocks(seed, (T0 - 1) // 64 + 1, PLANTED, L, b, gg)
+                            for gg in range(G)] for b in range(BATCH)])
+        synth.plant_batched(layer.k, blocks, direction)
+        sb.sparda_compress_keys(shape, layer, torch.full((BATCH,), T0 - 1, dtype=torch.int32, device=device), BATCH)
+        layers.append(layer)
+    stack = DecodeStack(shape, layers, W_self0, W_next, BATCH, device=device, advance=True)
+    stack.h.copy_(h)
+    stack.q.copy_(synth.normal_bf16_device(stack.q.shape, seed * 1000 + 41, device))
+    stack.k_new.copy_(synth.normal_bf16_device(stack.k_new.shape, seed * 1000 + 42, device))
+    stack.v_new.copy_(synth.normal_bf16_device(stack.v_new.shape, seed * 1000 + 43, device))
+    stack.seq_len.fill_(T0)
+    torch.cuda.synchronize()
+    return shape, stack, T0
+
+
+def kernel_times(stack, reps=10):
+    """Average device time of one forecast_select launch and one sparse_decode_attn launch,
+    timed with CUDA events on the launching stream over back-to-back launches of the step's
+    own calls (same buffers), after the timed region."""
+    import torch
+    import block_sparse_attention_forecast_gb300.binding as sb
+    sh, B, n = stack.shape, stack.batch, stack.n_layers
+    s = torch.cuda.current_stream()
+
+    def sel_loop():
+        for L in range(1, n):
+            sb.sparda_forecast_select(sh, stack.layers[L].ck, stack.f[L], stack.seq_len, B, stack.idx[L],
+                                      stack.cnt[L], stack.ws_sel, stream=s)
+
+    def attn_loop():
+        for L in range(n):
+            sb.sparda_sparse_decode_attn(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L],
+                                         stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
+
+    out = {}
+    for name, fn, per in (("select", sel_loop, n - 1), ("attn", attn_loop, n)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) * 1e-3 / (reps * per)
+    return out
+
+
+def select_bytes(T):
+    from block_sparse_attention_forecast_gb300.binding import num_windows
+    return BATCH * G * (num_windows(T - 1) * D * 2 + D * 2)
+
+
+def attn_bytes():
+    return BATCH * G * ((TOPK + 2) * 64 * D * 2 * 2 + 2 * H * D * 2)
+
+
+# ---------------------------------------------------------------------- CPU oracle sample
+CPU_SAMPLE_SCRIPT = r"""
+import sys, time, json
+sys.path.insert(0, %(root)r)
+import numpy as np
+import synth
+from oracle import sparda_oracle as O
+units, T = %(units)d, %(T)d
+t_total = 0.0
+for u in range(units):
+    K = synth.normal_bf16((T, 128), 900, u, 1).double().numpy()
+    V = synth.normal_bf16((T, 128), 900, u, 2).double().numpy()
+    q = synth.normal_bf16((16, 128), 900, u, 3).double().numpy()
+    W = synth.normal_bf16((128, 4096), 900, u, 4, std=0.02).double().numpy()
+    h = synth.normal_bf16((4096,), 900, u, 5).double().numpy()
+    t0 = time.perf_counter()
+    f = O.forecast_project(W, h)
+    sel = O.forecast_select_one(K, f, T, 32)
+    o = O.block_sparse_attention(q, K, V, sel, T)
+    t_total += time.perf_counter() - t0
+print(json.dumps({"seconds": t_total, "units": units}))
+"""
+
+
+def cpu_oracle_sample(units):
+    """Times the oracle on `units` (layer, sequence, group) pieces of the 128K step in a
+    single-threaded subprocess; returns (seconds per full step, cores, description)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = CPU_SAMPLE_SCRIPT % {"root": ROOT, "units": units, "T": CTX}
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    per_unit = res["seconds"] / res["units"]
+    per_step = per_unit * N_LAYERS * BATCH * G
+    desc = ("%d (layer, sequence, group) units of the 128K step (forecast projection + compressed "
+            "keys + select + 16-head attention each), %.2f s per unit, x%d units per step" %
+            (units, per_unit, N_LAYERS * BATCH * G))
+    return per_step, 1, desc
+
+
+def run_reference(args):
+    """The oracle arm: each step is one (layer, sequence, group) unit of the 128K workload
+    (the oracle is far too slow for a whole step); the per-step figure is extrapolated to
+    the 1024 units of a full step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    units = max(1, min(args.steps, 40))
+    per_step, cores, desc = cpu_oracle_sample(units)
+    value = BATCH / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": units, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": BATCH, "context": CTX, "layers": N_LAYERS, "topk": TOPK},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- main arm
+def run_ours(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = "cuda:%d" % local
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(24)          # before any heavy GPU setup; ~15 s of CPU work
+
+    steps_total = 1 + args.warmup + args.steps
+    shape, stack, T0 = build_workload(device, args.seed + rank, steps_total)
+    import block_sparse_attention_forecast_gb300.binding as sb
+    stack.capture()                          # one eager step, then the captured graph
+    for _ in range(args.warmup):
+        stack.run()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        stack.run()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    dev_err = sb.sparda_device_error(clear=True)
+    elapsed = e0.elapsed_time(e1) * 1e-3
+    T_last = int(stack.seq_len[0].item()) - 1
+
+    # end to end through the public API: per step, H2D of the step's inputs from pinned host
+    # memory, the step, D2H of the attention outputs
+    import synth
+    host_in = [torch.empty_like(t, device="cpu").pin_memory() for t in (stack.h, stack.q, stack.k_new, stack.v_new)]
+    for hb, t in zip(host_in, (stack.h, stack.q, stack.k_new, stack.v_new)):
+        hb.copy_(t.cpu())
+    host_out = torch.empty_like(stack.out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = min(args.steps, 200)
+    stack.seq_len.fill_(CTX - e2e_steps)
+    stack.run()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for hb, t in zip(host_in, (stack.h, stack.q, stack.k_new, stack.v_new)):
+            t.copy_(hb, non_blocking=True)
+        stack.run()
+        host_out.copy_(stack.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_elapsed = time.perf_counter() - t0
+
+    kt = kernel_times(stack)
+    if dist:
+        tt = torch.tensor([elapsed, e2e_elapsed], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed, e2e_elapsed = tt.tolist()
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    sel_b, att_b = select_bytes(CTX), attn_bytes()
+    sel_gbs = sel_b / kt["select"] / 1e9
+    att_gbs = att_b / kt["attn"] / 1e9
+    traffic = ncu_traffic("select.cu")
+    ms = elapsed / args.steps * 1e3
+    value = world * BATCH * args.steps / elapsed
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch_per_gpu": BATCH, "context": CTX, "layers": N_LAYERS,
+                   "kv_heads": G, "q_heads": G * H, "head_dim": D, "topk": TOPK, "block": 64,
+                   "window": "32/16", "hidden": HIDDEN, "parallelism": "replicas" if world > 1 else "single",
+                   "positions": "%d consecutive decode steps ending at context %d" % (args.steps, T_last + 1),
+                   "l2": "inputs larger than L2 (a step reads ~3.4 GB of compressed keys and KV)",
+                   "timing": "CUDA graph replay, CUDA events on the launching stream, max over ranks"},
+        "roofline": {"bound": "hbm", "kernel": "forecast_select_kernel", "achieved": sel_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": sel_gbs / hbm, "peak_source": peak_src + " hbm_gbs (burst)",
+                     "traffic": traffic, "alg_bytes_per_launch": sel_b, "launch_us": kt["select"] * 1e6},
+        "kernels": {
+            "forecast_select": {"us": kt["select"] * 1e6, "alg_bytes": sel_b, "gbs": sel_gbs, "frac": sel_gbs / hbm},
+            "sparse_decode_attn": {"us": kt["attn"] * 1e6, "alg_bytes": att_b, "gbs": att_gbs, "frac": att_gbs / hbm},
+            "select_attn_gbs": (sel_b + att_b) / (kt["select"] + kt["attn"]) / 1e9,
+        },
+        "e2e": {"value": world * BATCH * e2e_steps / e2e_elapsed, "unit": "tok/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * stack.kernel_launches_per_step(),
+        "device_error_flags": dev_err,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        per_step, cores, desc = cpu
+        line["cpu_baseline"] = {"value": BATCH / per_step, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,327 @@
+// The C ABI of libsparda (declared in include/sparda.h): argument checks, workspace layout,
+// TMA tensor-map encoding and kernel launches. Nothing here allocates device or host memory.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace sparda;
+
+// The device error word (bits SPARDA_DEV_*). Kernels receive its device address.
+__device__ int g_sparda_dev_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* dev_error_ptr() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sparda_dev_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int32_t shape_status(const sparda_shape* s) {
+  if (!s) return SPARDA_ERR_INVALID_ARG;
+  if (s->head_dim != kHeadDim || s->heads_per_group != kHeads || s->block != kBlock ||
+      s->win_kernel != kWinKernel || s->win_stride != kWinStride)
+    return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  if (s->n_groups < 1 || s->max_batch < 1 || s->topk < 1 || s->topk > kMaxTopk ||
+      s->max_ctx < kBlock || s->max_ctx % kBlock != 0 || s->max_ctx > kMaxCtx)
+    return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  // every row index of a cache must fit a signed 32-bit TMA coordinate
+  if ((int64_t)s->max_batch * s->n_groups * s->max_ctx >= (int64_t)1 << 31)
+    return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  return SPARDA_OK;
+}
+
+int32_t batch_status(const sparda_shape* s, int32_t batch) {
+  return (batch < 1 || batch > s->max_batch) ? SPARDA_ERR_INVALID_ARG : SPARDA_OK;
+}
+
+int w_cap(const sparda_shape* s) { return num_windows(s->max_ctx); }
+int nb_cap(const sparda_shape* s) { return s->max_ctx / kBlock; }
+int kslots(const sparda_shape* s) { return s->topk + 2; }
+int attn_splits(const sparda_shape* s) {
+  return (kslots(s) + attn_blocks_per_cta() - 1) / attn_blocks_per_cta();
+}
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspaces are laid out for max_batch sequences so that their counters sit at the same
+// place whatever batch a call uses: [counters: max_batch*G u32][data].
+size_t counters_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * sizeof(unsigned));
+}
+size_t select_data_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * nb_cap(s) * sizeof(float));
+}
+size_t attn_o_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * attn_splits(s) * kHeads * kHeadDim * sizeof(float));
+}
+size_t attn_ml_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * attn_splits(s) * 2 * kHeads * sizeof(float));
+}
+
+int32_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SPARDA_OK;
+  std::fprintf(stderr, "sparda: CUDA error %s\n", cudaGetErrorString(e));
+  return SPARDA_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ TMA tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A [rows, 128] bf16 matrix read in boxes of 64 rows x 64 columns, 128-byte swizzle.
+int32_t make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return SPARDA_ERR_CUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPARDA_OK : SPARDA_ERR_CUDA;
+}
+
+// Pinned host memory mapped into the device's address space.
+int32_t host_mapped_status(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SPARDA_ERR_NOT_MAPPED_HOST;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return SPARDA_ERR_NOT_MAPPED_HOST;
+  return SPARDA_OK;
+}
+
+int32_t layer_status(const sparda_layer_kv* L, bool need_kv) {
+  if (!L || !L->ck) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(L->ck, 16)) return SPARDA_ERR_MISALIGNED;
+  if (!need_kv) return SPARDA_OK;
+  if (!L->k || !L->v) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(L->k, 16) || !aligned(L->v, 16)) return SPARDA_ERR_MISALIGNED;
+  if (L->on_host) {
+    if (!L->hot_k || !L->hot_v) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(L->hot_k, 16) || !aligned(L->hot_v, 16)) return SPARDA_ERR_MISALIGNED;
+    int32_t st = host_mapped_status(L->k);
+    if (st == SPARDA_OK) st = host_mapped_status(L->v);
+    if (st != SPARDA_OK) return st;
+  }
+  return SPARDA_OK;
+}
+
+#define SPARDA_TRY(x)                     \
+  do {                                    \
+    const int32_t st_ = (x);              \
+    if (st_ != SPARDA_OK) return st_;     \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int32_t sparda_abi_version(void) { return 1; }
+
+const char* sparda_status_string(int32_t status) {
+  switch (status) {
+    case SPARDA_OK: return "ok";
+    case SPARDA_ERR_INVALID_ARG: return "invalid argument";
+    case SPARDA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case SPARDA_ERR_MISALIGNED: return "misaligned pointer";
+    case SPARDA_ERR_NOT_MAPPED_HOST: return "host memory not pinned and mapped for the device";
+    case SPARDA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SPARDA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int32_t sparda_check_shape(const sparda_shape* shape) { return shape_status(shape); }
+
+size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind) {
+  if (shape_status(s) != SPARDA_OK || batch < 1 || batch > s->max_batch) return 0;
+  switch (kind) {
+    case SPARDA_WS_SELECT: return counters_bytes(s) + select_data_bytes(s);
+    case SPARDA_WS_ATTN: return counters_bytes(s) + attn_o_bytes(s) + attn_ml_bytes(s);
+    default: return 0;
+  }
+}
+
+int32_t sparda_device_error(int32_t* flags, int32_t clear) {
+  if (!flags) return SPARDA_ERR_INVALID_ARG;
+  int* p = dev_error_ptr();
+  if (!p) return SPARDA_ERR_CUDA;
+  SPARDA_TRY(cuda_status(cudaDeviceSynchronize()));
+  SPARDA_TRY(cuda_status(cudaMemcpy(flags, p, sizeof(int), cudaMemcpyDeviceToHost)));
+  if (clear) SPARDA_TRY(cuda_status(cudaMemset(p, 0, sizeof(int))));
+  return SPARDA_OK;
+}
+
+int32_t sparda_prefetch_default_ctas(int32_t batch) { return batch < 32 ? 16 : 32; }
+
+int32_t sparda_append_kv(const sparda_shape* s, const sparda_layer_kv* L, const void* k_new,
+                         const void* v_new, const int32_t* seq_len, int32_t batch, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  SPARDA_TRY(layer_status(L, true));
+  if (!k_new || !v_new || !seq_len) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(seq_len, 4)) return SPARDA_ERR_MISALIGNED;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  AppendArgs a{static_cast<__nv_bfloat16*>(L->k), static_cast<__nv_bfloat16*>(L->v),
+               static_cast<__nv_bfloat16*>(L->ck), static_cast<__nv_bfloat16*>(L->hot_k),
+               static_cast<__nv_bfloat16*>(L->hot_v), static_cast<const __nv_bfloat16*>(k_new),
+               static_cast<const __nv_bfloat16*>(v_new), seq_len, err, s->n_groups, s->max_ctx,
+               w_cap(s), L->on_host ? 1 : 0};
+  launch_append_kv(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_compress_keys(const sparda_shape* s, const sparda_layer_kv* L, const int32_t* seq_len,
+                             int32_t batch, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  SPARDA_TRY(layer_status(L, true));
+  if (!seq_len) return SPARDA_ERR_INVALID_ARG;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  CompressArgs a{static_cast<const __nv_bfloat16*>(L->k), static_cast<const __nv_bfloat16*>(L->hot_k),
+                 static_cast<__nv_bfloat16*>(L->ck), seq_len, err, s->n_groups, s->max_ctx, w_cap(s),
+                 L->on_host ? 1 : 0};
+  launch_compress_keys(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int32_t hidden,
+                                int32_t batch, void* f, void* stream) {
+  if (!W || !h || !f) return SPARDA_ERR_INVALID_ARG;
+  if (rows < 8 || rows % 8 != 0 || hidden < 32 || hidden % 32 != 0 || batch < 1)
+    return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W, 16) || !aligned(h, 16) || !aligned(f, 16)) return SPARDA_ERR_MISALIGNED;
+  ProjectArgs a{static_cast<const __nv_bfloat16*>(W), static_cast<const __nv_bfloat16*>(h),
+                static_cast<__nv_bfloat16*>(f), rows, hidden, batch};
+  launch_forecast_project(a, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void* forecast,
+                               const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
+                               void* ws, size_t ws_bytes, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!ck || !forecast || !seq_len || !idx || !cnt || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(ck, 16) || !aligned(forecast, 16) || !aligned(ws, 16) || !aligned(idx, 4) ||
+      !aligned(cnt, 4) || !aligned(seq_len, 4))
+    return SPARDA_ERR_MISALIGNED;
+  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_SELECT)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const int bgc = batch * s->n_groups;
+  SelectArgs a{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
+               seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
+               reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
+               s->topk, select_chunk_blocks(nb_cap(s), bgc)};
+  launch_forecast_select(a, bgc, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_sparse_decode_attn(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
+                                  const void* staging_v, const void* q, const int32_t* idx,
+                                  const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* out,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!L || !q || !idx || !cnt || !seq_len || !out || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16) || !aligned(idx, 4) || !aligned(cnt, 4))
+    return SPARDA_ERR_MISALIGNED;
+  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_ATTN)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap mk, mv, hk, hv;
+  const uint64_t bgcap = (uint64_t)s->max_batch * s->n_groups;
+  if (L->on_host) {
+    if (!staging_k || !staging_v || !L->hot_k || !L->hot_v) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(staging_k, 16) || !aligned(staging_v, 16) || !aligned(L->hot_k, 16) || !aligned(L->hot_v, 16))
+      return SPARDA_ERR_MISALIGNED;
+    SPARDA_TRY(make_kv_map(&mk, staging_k, bgcap * kslots(s) * kBlock));
+    SPARDA_TRY(make_kv_map(&mv, staging_v, bgcap * kslots(s) * kBlock));
+    SPARDA_TRY(make_kv_map(&hk, L->hot_k, bgcap * kHotSlots * kBlock));
+    SPARDA_TRY(make_kv_map(&hv, L->hot_v, bgcap * kHotSlots * kBlock));
+  } else {
+    if (!L->k || !L->v) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(L->k, 16) || !aligned(L->v, 16)) return SPARDA_ERR_MISALIGNED;
+    SPARDA_TRY(make_kv_map(&mk, L->k, bgcap * s->max_ctx));
+    SPARDA_TRY(make_kv_map(&mv, L->v, bgcap * s->max_ctx));
+    hk = mk;
+    hv = mv;
+  }
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  AttnArgs a{static_cast<const __nv_bfloat16*>(q), idx, cnt, seq_len, static_cast<__nv_bfloat16*>(out),
+             reinterpret_cast<float*>(w + counters_bytes(s)),
+             reinterpret_cast<float*>(w + counters_bytes(s) + attn_o_bytes(s)),
+             reinterpret_cast<unsigned*>(w), err, s->n_groups, s->max_ctx, kslots(s), attn_splits(s),
+             L->on_host ? 1 : 0};
+  launch_sparse_attn(a, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_prefetch_blocks(const sparda_shape* s, const sparda_layer_kv* L, const int32_t* idx,
+                               const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* staging_k,
+                               void* staging_v, int32_t n_ctas, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!L || !L->on_host) return SPARDA_ERR_INVALID_ARG;
+  SPARDA_TRY(layer_status(L, true));
+  if (!idx || !cnt || !seq_len || !staging_k || !staging_v || n_ctas < 0 || n_ctas > 4096)
+    return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(staging_k, 16) || !aligned(staging_v, 16)) return SPARDA_ERR_MISALIGNED;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  PrefetchArgs a{static_cast<const __nv_bfloat16*>(L->k), static_cast<const __nv_bfloat16*>(L->v), idx, cnt,
+                 seq_len, static_cast<__nv_bfloat16*>(staging_k), static_cast<__nv_bfloat16*>(staging_v), err,
+                 batch, s->n_groups, s->max_ctx, kslots(s)};
+  launch_prefetch(a, n_ctas ? n_ctas : sparda_prefetch_default_ctas(batch), static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_multihead_select(const sparda_shape* s, const void* ck, const void* q, const int32_t* seq_len,
+                                int32_t batch, int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes,
+                                void* stream) {
+  (void)ck; (void)q; (void)seq_len; (void)idx; (void)cnt; (void)ws; (void)ws_bytes; (void)stream;
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  return SPARDA_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel translation units.
+// Every struct is passed to its kernel by value; pointers are device (or UVA) addresses.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sparda {
+
+struct AppendArgs {
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  __nv_bfloat16* ck;
+  __nv_bfloat16* hot_k;
+  __nv_bfloat16* hot_v;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int32_t* seq_len;
+  int* err;
+  int G, max_ctx, W_cap, on_host;
+};
+
+struct CompressArgs {
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* hot_k;
+  __nv_bfloat16* ck;
+  const int32_t* seq_len;
+  int* err;
+  int G, max_ctx, W_cap, on_host;
+};
+
+struct ProjectArgs {
+  const __nv_bfloat16* W;
+  const __nv_bfloat16* h;
+  __nv_bfloat16* f;
+  int rows, hidden, batch;
+};
+
+struct SelectArgs {
+  const __nv_bfloat16* ck;
+  const __nv_bfloat16* f;        // forecast [B, G, d]
+  const int32_t* seq_len;
+  int32_t* idx;                  // [B, G, topk+2]
+  int32_t* cnt;                  // [B, G]
+  float* block_scores;           // workspace [B*G, nb_cap]
+  unsigned* counters;            // workspace [B*G], zero between calls
+  int* err;
+  int G, W_cap, max_ctx, nb_cap, topk, chunk_blocks;
+};
+
+struct AttnArgs {
+  const __nv_bfloat16* q;        // [B, G*H, d]
+  const int32_t* idx;
+  const int32_t* cnt;
+  const int32_t* seq_len;
+  __nv_bfloat16* out;            // [B, G*H, d]
+  float* part_o;                 // workspace [B*G, n_split, H, d]
+  float* part_ml;                // workspace [B*G, n_split, 2, H]
+  unsigned* counters;            // workspace [B*G]
+  int* err;
+  int G, max_ctx, kslots, n_split, offload;
+};
+
+struct PrefetchArgs {
+  const __nv_bfloat16* hk;       // host cache (UVA) [B, G, max_ctx, d]
+  const __nv_bfloat16* hv;
+  const int32_t* idx;
+  const int32_t* cnt;
+  const int32_t* seq_len;
+  __nv_bfloat16* sk;             // staging [B, G, kslots, 64, d]
+  __nv_bfloat16* sv;
+  int* err;
+  int B, G, max_ctx, kslots;
+};
+
+void launch_append_kv(const AppendArgs& a, int bg_count, cudaStream_t s);
+void launch_compress_keys(const CompressArgs& a, int bg_count, cudaStream_t s);
+void launch_forecast_project(const ProjectArgs& a, cudaStream_t s);
+void launch_forecast_select(const SelectArgs& a, int bg_count, cudaStream_t s);
+// maps: K and V of the resident cache or of the staging buffer, then hot K and V (offload).
+void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const CUtensorMap& hk, const CUtensorMap& hv, int bg_count,
+                        cudaStream_t s);
+void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s);
+
+// Sizes the C ABI needs to lay out workspaces.
+int select_chunk_blocks(int nb_cap, int bg_count);
+int attn_blocks_per_cta();
+size_t smem_select_bytes(int chunk_blocks);
+
+}  // namespace sparda

@@ -1,0 +1,156 @@
+"""The decode step of a forecast-driven block-sparse layer stack, on CUDA streams and graphs.
+
+Per layer L (bittide thread: layer L's forecast predicts layer L+1's blocks, which layer L+1
+then attends with its own queries; techwalker section 三: layer 0 has no earlier forecast
+and selects its own blocks with a same-layer forecast):
+
+    main stream   append_kv(L) ............................ sparse_decode_attn(L, idx[L])
+    side stream        forecast_project(W_next[L], h[L]) -> forecast_select(ck[L+1]) -> idx[L+1]
+    (join before layer L+1)
+
+The forecast branch of layer L only needs layer L's hidden state, so its selection for
+layer L+1 runs concurrently with layer L's attention. Offloaded layers add a third stream
+that gathers layer L+1's selected blocks from pinned host memory as soon as they are known,
+into one of two staging buffers; layer L+1's attention waits for that gather.
+
+Everything here is host-side orchestration of libsparda calls (no arithmetic); the whole step
+can be captured once into a CUDA graph and replayed.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as sb
+
+
+class DecodeStack:
+    """Buffers and streams of an n_layers decode stack with forecast lookahead.
+
+    layers: list of sb.LayerKV (resident or offloaded; layer 0 must be resident).
+    W_self0: bf16 [G*d, hidden] (layer 0's same-layer forecast head); W_next[L]: bf16
+    [G*d, hidden] for L < n_layers - 1 (layer L's head that forecasts layer L+1).
+    Per-step inputs live in static device buffers h, q, k_new, v_new, seq_len; outputs in
+    out. idx[L] / cnt[L] hold the blocks layer L attends at the current step.
+    """
+
+    def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
+                 overlap=True, advance=False):
+        self.shape = shape
+        self.layers = layers
+        self.n_layers = len(layers)
+        self.W_self0 = W_self0
+        self.W_next = W_next
+        self.batch = batch
+        self.device = device
+        self.gather_ctas = gather_ctas
+        self.overlap = overlap
+        self.advance = advance          # move every sequence one token on after each step
+        assert not layers[0].on_host, "layer 0 stays resident"
+        G, H, d = shape.n_groups, shape.heads_per_group, shape.head_dim
+        hidden = W_self0.shape[1]
+        n, B = self.n_layers, batch
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.h = torch.zeros((n, B, hidden), **bf)
+        self.q = torch.zeros((n, B, G * H, d), **bf)
+        self.k_new = torch.zeros((n, B, G, d), **bf)
+        self.v_new = torch.zeros((n, B, G, d), **bf)
+        self.out = torch.zeros((n, B, G * H, d), **bf)
+        self.f = torch.zeros((n + 1, B, G, d), **bf)        # f[L]: forecast for layer L
+        self.idx = torch.full((n, B, G, shape.kslots), -1, dtype=torch.int32, device=device)
+        self.cnt = torch.zeros((n, B, G), dtype=torch.int32, device=device)
+        self.seq_len = torch.ones(B, dtype=torch.int32, device=device)
+        self.ws_sel = sb.workspace(shape, B, sb.WS_SELECT, device)
+        self.ws_attn = sb.workspace(shape, B, sb.WS_ATTN, device)
+        self.any_offload = any(l.on_host for l in layers)
+        if self.any_offload:
+            st = (shape.max_batch, G, shape.kslots, shape.block, d)
+            self.stage_k = [torch.zeros(st, **bf) for _ in range(2)]
+            self.stage_v = [torch.zeros(st, **bf) for _ in range(2)]
+        self.side = torch.cuda.Stream(device=device)
+        self.gather = torch.cuda.Stream(device=device) if self.any_offload else None
+        self.graph = None
+
+    # ------------------------------------------------------------------ one step
+    def enqueue(self):
+        """Enqueue one decode step on the current stream (plus the side streams)."""
+        sh, B = self.shape, self.batch
+        main = torch.cuda.current_stream()
+        side = self.side
+        ev = lambda: torch.cuda.Event()
+        attn_done = [None] * self.n_layers
+        gather_done = [None] * self.n_layers
+
+        # layer 0 selects its own blocks from a same-layer forecast
+        sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
+        sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
+                                  self.idx[0], self.cnt[0], self.ws_sel, stream=main)
+        for L in range(self.n_layers):
+            layer = self.layers[L]
+            fork = ev()
+            fork.record(main)
+            if L + 1 < self.n_layers:
+                side.wait_event(fork)
+                nxt = self.layers[L + 1]
+                sb.sparda_forecast_project(self.W_next[L], self.h[L], self.f[L + 1].view(B, -1), stream=side)
+                sb.sparda_forecast_select(sh, nxt.ck, self.f[L + 1], self.seq_len, B, self.idx[L + 1],
+                                          self.cnt[L + 1], self.ws_sel, stream=side)
+                sel_done = ev()
+                sel_done.record(side)
+                if nxt.on_host:
+                    slot = (L + 1) % 2
+                    self.gather.wait_event(sel_done)
+                    if L - 1 >= 0 and attn_done[L - 1] is not None:
+                        self.gather.wait_event(attn_done[L - 1])   # staging slot reuse
+                    sb.sparda_prefetch_blocks(sh, nxt, self.idx[L + 1], self.cnt[L + 1], self.seq_len, B,
+                                              self.stage_k[slot], self.stage_v[slot], self.gather_ctas,
+                                              stream=self.gather)
+                    gather_done[L + 1] = ev()
+                    gather_done[L + 1].record(self.gather)
+                    if not self.overlap:
+                        main.wait_event(gather_done[L + 1])
+            sb.sparda_append_kv(sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B, stream=main)
+            if layer.on_host:
+                main.wait_event(gather_done[L])
+                slot = L % 2
+                sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
+                                             self.out[L], self.ws_attn, staging_k=self.stage_k[slot],
+                                             staging_v=self.stage_v[slot], stream=main)
+            else:
+                sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
+                                             self.out[L], self.ws_attn, stream=main)
+            attn_done[L] = ev()
+            attn_done[L].record(main)
+            if L + 1 < self.n_layers:
+                main.wait_event(sel_done)
+        if self.any_offload:
+            main.wait_stream(self.gather)
+        if self.advance:
+            self.seq_len.add_(1)
+
+    def capture(self):
+        """Capture one step into a CUDA graph (after one eager warm-up step)."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.enqueue()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.enqueue()
+        torch.cuda.synchronize()
+        return self.graph
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.enqueue()
+
+    def kernel_launches_per_step(self):
+        """Kernels one step launches: per layer append, forecast projection, select (all
+        but the last layer), attention, plus layer 0's own projection and select and one
+        gather per offloaded layer."""
+        n = self.n_layers
+        gathers = sum(1 for l in self.layers[1:] if l.on_host)
+        return 2 + n * 2 + (n - 1) * 2 + gathers

@@ -1,0 +1,249 @@
+/*
+ * sparda.h -- C ABI of the forecast-driven block-sparse decode step (libsparda.so).
+ *
+ * SparDA ("SparDA: Sparse Decoupled Attention for Efficient Long-Context LLM Inference", as
+ * described by three web pages: a bittide.aicompass.dev thread with the translated
+ * abstract, the techwalker.com article "NVIDIA与MIT联手：让超长文本AI助手的'记忆搜索'快了5倍多"
+ * and the 10100.com piece "不是我硬件不好 是你软件架构有硬伤") adds a fourth projection, the
+ * Forecast, to every attention layer. Layer L's forecast picks the KV blocks that layer L+1
+ * will attend, so those blocks can be fetched from host memory while layer L still runs.
+ * This library implements one layer's decode-step pieces as CUDA kernels for sm_103a:
+ *
+ *   sparda_append_kv           store the new token's K/V, maintain the compressed keys
+ *   sparda_compress_keys       build every compressed key of a cache at once (prefill)
+ *   sparda_forecast_project    the forecast projection (one 128-wide head per KV group)
+ *   sparda_forecast_select     forecast scoring + max-pool onto blocks + top-k
+ *   sparda_sparse_decode_attn  block-sparse GQA decode attention over the selection
+ *   sparda_prefetch_blocks     gather of selected blocks from pinned host memory (UVA)
+ *   sparda_multihead_select    the baseline query-driven selector, for comparison
+ *
+ * Conventions shared by every call
+ *   - All tensors are caller-owned. The library never allocates, frees or synchronises on
+ *     these calls; kernels are enqueued on the stream given (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) and the call returns at once.
+ *   - bf16 means IEEE bfloat16 stored as 16-bit words. All layouts are dense, row-major,
+ *     innermost dimension last.
+ *   - B = batch (sequences), G = KV groups (KV heads), H = query heads per group,
+ *     d = head dimension. Query head h belongs to group h / H.
+ *   - seq_len is a DEVICE int32 array [B]: seq_len[b] = T, the number of tokens of
+ *     sequence b's context INCLUDING the current decode token, which sits at position T-1.
+ *     1 <= T <= shape->max_ctx is required; a sequence outside that range produces no
+ *     output (cnt = 0, idx = -1, zero attention output) and sets SPARDA_DEV_BAD_SEQ_LEN in
+ *     the device error word.
+ *   - Pointers must be 16-byte aligned (KV caches, staging and hot buffers 1024-byte
+ *     aligned); a violation returns SPARDA_ERR_MISALIGNED before anything is launched.
+ *   - Every argument check is synchronous and happens before any launch. Errors inside a
+ *     kernel (a bounded wait that ran out, an out-of-range seq_len or block index) never
+ *     trap: the kernel skips the bad access, ORs a bit into a device-side error word and
+ *     returns. sparda_device_error() reads that word.
+ *   - Workspaces: calls that take a workspace need sparda_workspace_bytes() bytes of
+ *     device memory, zero-filled before their first use (cudaMemset). Every call leaves
+ *     the workspace's counters at zero again, so it can be reused without clearing.
+ *     Two calls that may run at the same time must not share a workspace.
+ */
+#ifndef SPARDA_H_
+#define SPARDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+#define SPARDA_OK                        0
+#define SPARDA_ERR_INVALID_ARG          -1  /* null pointer, negative or zero size        */
+#define SPARDA_ERR_UNSUPPORTED_SHAPE    -2  /* a shape this build does not support         */
+#define SPARDA_ERR_MISALIGNED           -3  /* pointer alignment rule broken               */
+#define SPARDA_ERR_NOT_MAPPED_HOST      -4  /* host KV not reachable by the device (UVA)   */
+#define SPARDA_ERR_WORKSPACE_TOO_SMALL  -5
+#define SPARDA_ERR_CUDA                 -6  /* a CUDA runtime/driver call failed           */
+
+/* bits of the device error word (sparda_device_error) */
+#define SPARDA_DEV_WAIT_TIMEOUT   1   /* a bounded wait on a copy's completion ran out      */
+#define SPARDA_DEV_BAD_SEQ_LEN    2   /* seq_len[b] outside [1, max_ctx]                    */
+#define SPARDA_DEV_BAD_INDEX      4   /* a block index outside the sequence's blocks        */
+
+/* workspace kinds for sparda_workspace_bytes */
+#define SPARDA_WS_SELECT      1
+#define SPARDA_WS_ATTN        2
+#define SPARDA_WS_MULTIHEAD   3
+
+/* ---------------------------------------------------------------- shapes */
+/*
+ * The decode-step geometry. This build supports head_dim 128, heads_per_group 16, block 64,
+ * win_kernel 32, win_stride 16 (the compression window the techwalker article, section 四,
+ * gives for inference), 1 <= topk <= 62, max_ctx a multiple of 64 up to 262144, any
+ * n_groups >= 1 and max_batch >= 1. max_batch sizes the caches (their outer dimension);
+ * a call may use any batch <= max_batch.
+ */
+typedef struct sparda_shape {
+  int32_t n_groups;         /* G: KV groups (KV heads) of the layer                          */
+  int32_t heads_per_group;  /* H: query heads sharing one KV head                            */
+  int32_t head_dim;         /* d                                                             */
+  int32_t block;            /* tokens per KV block                                           */
+  int32_t win_kernel;       /* tokens per compression window                                 */
+  int32_t win_stride;       /* stride between compression windows                            */
+  int32_t topk;             /* scored blocks kept on top of block 0 and the tail block       */
+  int32_t max_ctx;          /* token capacity per sequence                                   */
+  int32_t max_batch;        /* sequence capacity of the caches                               */
+} sparda_shape;
+
+/*
+ * One layer's KV state. W_cap = (max_ctx - win_kernel) / win_stride + 1 compressed-key
+ * slots per sequence and group.
+ *
+ *   k, v   bf16 [max_batch, G, max_ctx, d]. Resident layer (on_host = 0): device memory.
+ *          Offloaded layer (on_host = 1): pinned host memory allocated or registered with
+ *          the mapped flag; pass the DEVICE pointer of that memory (cudaHostGetDevicePointer,
+ *          equal to the host pointer under UVA). It holds every complete block.
+ *   ck     bf16 [max_batch, G, W_cap, d], device memory (always resident): ck[.., i, :] is the
+ *          mean of keys 16i .. 16i+31 rounded to bf16.
+ *   hot_k, hot_v
+ *          offloaded layers only (NULL otherwise): bf16 [max_batch, G, 3, block, d] device
+ *          memory. Slot 0 holds block 0; the block j >= 1 that holds the newest token lives
+ *          in slot 1 + (j & 1), and the block before it in the other of slots 1 and 2. The
+ *          attention reads block 0 and the tail block from here, never from host memory.
+ */
+typedef struct sparda_layer_kv {
+  void* k;
+  void* v;
+  void* ck;
+  void* hot_k;
+  void* hot_v;
+  int32_t on_host;
+  int32_t reserved;
+} sparda_layer_kv;
+
+/* ---------------------------------------------------------------- utilities */
+int32_t sparda_abi_version(void);
+const char* sparda_status_string(int32_t status);
+
+/* SPARDA_OK if this build supports the shape, else SPARDA_ERR_UNSUPPORTED_SHAPE. */
+int32_t sparda_check_shape(const sparda_shape* shape);
+
+/* Bytes of workspace the call of the given kind (SPARDA_WS_*) needs for `batch`
+ * sequences; 0 for an unsupported shape. */
+size_t sparda_workspace_bytes(const sparda_shape* shape, int32_t batch, int32_t kind);
+
+/* Reads the device error word (bits SPARDA_DEV_*) of the current device into *flags and,
+ * if clear != 0, resets it. Synchronous: waits for all work on the device. */
+int32_t sparda_device_error(int32_t* flags, int32_t clear);
+
+/* Copy-CTA count the gather uses by default for a batch: 16 below batch 32, 32 from 32 on
+ * (the batch-adaptive rule of the techwalker article, section 三). */
+int32_t sparda_prefetch_default_ctas(int32_t batch);
+
+/* ---------------------------------------------------------------- the decode step */
+
+/*
+ * sparda_append_kv -- store the current token's key and value and keep the compressed keys
+ * up to date as tokens arrive (compression window kernel 32 / stride 16, techwalker §四).
+ *
+ * k_new, v_new: device bf16 [B, G, d]. For every sequence b (T = seq_len[b]) the token is
+ * written at position T-1. When T >= 32 and (T - 32) % 16 == 0 a window completes and
+ * ck[b, g, (T-32)/16, :] = bf16(mean of keys T-32 .. T-1) is written; the mean is formed in
+ * float64 (exact for bf16 keys of ordinary range) and rounded to nearest even.
+ * Offloaded layers: the token goes to the hot tail slot; when it fills its block (T % 64
+ * == 0) that block is also written to the host cache, so that a later gather finds it.
+ */
+int32_t sparda_append_kv(const sparda_shape* shape, const sparda_layer_kv* layer,
+                         const void* k_new, const void* v_new, const int32_t* seq_len,
+                         int32_t batch, void* stream);
+
+/*
+ * sparda_compress_keys -- write every compressed key that is complete within the first
+ * seq_len[b] tokens of the cache (windows i < (T - 32) / 16 + 1), as sparda_append_kv would
+ * have written them one by one. Used after a prefill. Offloaded layers read the keys from
+ * the host cache over the host link (slow; a set-up step).
+ */
+int32_t sparda_compress_keys(const sparda_shape* shape, const sparda_layer_kv* layer,
+                             const int32_t* seq_len, int32_t batch, void* stream);
+
+/*
+ * sparda_forecast_project -- the Forecast projection, the fourth per-layer projection
+ * (bittide thread; techwalker §二): f[b, r] = bf16(sum_c W[r, c] * h[b, c]).
+ *
+ * W: device bf16 [rows, hidden] (rows = G * d: row g*d + c is component c of group g's
+ * forecast head); h: device bf16 [batch, hidden]; f: device bf16 [batch, rows], i.e.
+ * [batch, G, d]. Products and sums in float32 (tensor cores), output rounded to nearest
+ * even. rows must be a multiple of 8 and hidden a multiple of 32.
+ */
+int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int32_t hidden,
+                                int32_t batch, void* f, void* stream);
+
+/*
+ * sparda_forecast_select -- the Forecast selector (bittide thread: one forecast head per
+ * GQA group and no softmax; techwalker §二; 10100 "SparDA 的解法"), for the target layer
+ * whose compressed keys are `ck` (layer L+1 under lookahead, layer 0 for its same-layer
+ * forecast, techwalker §三).
+ *
+ * For each (b, g), with T = seq_len[b], tb = (T-1)/64 and W = the windows complete within
+ * the first T-1 tokens (the current token's window does not exist yet in the target layer):
+ *   s[i] = sum_c f[b,g,c] * ck[b,g,i,c]          (float32, i < W; no softmax, no scale)
+ *   S[j] = max { s[i] : window i overlaps block j }   (windows 4j-1 .. 4j+3)
+ *   chosen = the topk highest S[j] over 1 <= j < tb (ties -> lower j)
+ * Output idx: int32 [B, G, topk+2], the blocks {0, tb} U chosen sorted ascending, then -1
+ * padding; cnt: int32 [B, G], the number of valid entries (min(topk, tb-1) + 2, or 1 when
+ * tb = 0). forecast: device bf16 [B, G, d]. workspace: SPARDA_WS_SELECT.
+ */
+int32_t sparda_forecast_select(const sparda_shape* shape, const void* ck, const void* forecast,
+                               const int32_t* seq_len, int32_t batch, int32_t* idx,
+                               int32_t* cnt, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * sparda_sparse_decode_attn -- block-sparse GQA decode attention (bittide thread: the next
+ * layer's own queries attend the selected blocks; techwalker §六: the sparse attention
+ * itself is unchanged by SparDA). For every query head h of group g:
+ *   o[b, g*H + h, :] = sum_t softmax_t(q . k_t / sqrt(d)) v_t
+ * over the tokens t < T of the blocks idx[b, g, 0 .. cnt[b,g]-1].
+ *
+ * q: device bf16 [B, G*H, d]; out: device bf16 [B, G*H, d]; idx/cnt as produced by
+ * sparda_forecast_select. Resident layer: K/V are read from the layer's cache. Offloaded
+ * layer: staging_k / staging_v (device bf16 [max_batch, G, topk+2, 64, d], filled by
+ * sparda_prefetch_blocks for the same idx) supply every selected block except block 0 and
+ * the tail block, which come from the layer's hot buffers. QK^T and PV run on tensor cores
+ * (bf16 operands, float32 accumulation); the softmax is float32. workspace: SPARDA_WS_ATTN.
+ */
+int32_t sparda_sparse_decode_attn(const sparda_shape* shape, const sparda_layer_kv* layer,
+                                  const void* staging_k, const void* staging_v, const void* q,
+                                  const int32_t* idx, const int32_t* cnt,
+                                  const int32_t* seq_len, int32_t batch, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sparda_prefetch_blocks -- the gather that hides the host-offload copy (bittide thread:
+ * the next layer's blocks are fetched on a separate CUDA stream while the current layer
+ * computes; techwalker §三: a persistent kernel with a few copy CTAs reads host memory
+ * directly over unified virtual addressing, 16 CTAs below batch 32 and 32 from 32 on).
+ *
+ * For every (b, g) and slot s < cnt[b,g] whose block j = idx[b,g,s] is neither block 0 nor
+ * the tail block, copies block j of the offloaded layer's host k and v into slot s of
+ * staging_k / staging_v (device bf16 [max_batch, G, topk+2, 64, d]). n_ctas = 0 picks
+ * sparda_prefetch_default_ctas(batch). Enqueue it on a side stream after an event recorded
+ * behind the select call, and make the attention wait on an event recorded behind it.
+ */
+int32_t sparda_prefetch_blocks(const sparda_shape* shape, const sparda_layer_kv* layer,
+                               const int32_t* idx, const int32_t* cnt, const int32_t* seq_len,
+                               int32_t batch, void* staging_k, void* staging_v,
+                               int32_t n_ctas, void* stream);
+
+/*
+ * sparda_multihead_select -- the baseline query-driven selector the pages compare against
+ * (bittide thread; 10100 "先把痛点讲透"): every query head of the group scores every
+ * compressed key (scale 1/sqrt(d)), a softmax per head over the windows, a sum over the
+ * group's heads, then the same max-pool and top-k as sparda_forecast_select.
+ * q: device bf16 [B, G*H, d]. Outputs as sparda_forecast_select. workspace:
+ * SPARDA_WS_MULTIHEAD.
+ */
+int32_t sparda_multihead_select(const sparda_shape* shape, const void* ck, const void* q,
+                                const int32_t* seq_len, int32_t batch, int32_t* idx,
+                                int32_t* cnt, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARDA_H_ */

@@ -1,0 +1,263 @@
+"""Parity of each libsparda kernel with the fp64 oracle, on small seeded inputs that span
+several tiles and ragged tails. Every call goes through the C ABI (the ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import sparda_oracle as O
+from tests.parity import check_attention, check_selection, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sb(cuda_ok):
+    from block_sparse_attention_forecast_gb300 import build
+    build.build()
+    import block_sparse_attention_forecast_gb300.binding as b
+    b.sparda_device_error(clear=True)
+    return b
+
+
+def _no_device_error(sb):
+    assert sb.sparda_device_error(clear=True) == 0
+
+
+# ------------------------------------------------------------------ compressed keys
+@pytest.mark.parametrize("T_list", [[1000, 33, 64], [31, 32, 47, 48], [1024, 1023, 999, 512]])
+def test_compress_keys_bit_exact(sb, T_list):
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=1024, max_batch=B, topk=8)
+    layer = sb.LayerKV.empty(shape)
+    K = synth.normal_bf16((B, 2, 1024, 128), 11, B)
+    layer.k.copy_(K.cuda())
+    layer.v.zero_()
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    sb.sparda_compress_keys(shape, layer, seq, B)
+    torch.cuda.synchronize()
+    ck = to64(layer.ck)
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            W = O.num_windows(T)
+            want = O.compress_keys(to64(K[b, g]), W)
+            assert np.array_equal(ck[b, g, :W], want), (b, g, T)
+    _no_device_error(sb)
+
+
+def test_append_tokens_and_windows(sb):
+    B, steps, T0 = 3, 70, [100, 37, 500]
+    shape = sb.Shape(max_ctx=1024, max_batch=B, topk=8)
+    layer = sb.LayerKV.empty(shape)
+    K = synth.normal_bf16((B, 2, 1024, 128), 12, 1)
+    V = synth.normal_bf16((B, 2, 1024, 128), 12, 2)
+    layer.k.copy_(K.cuda())
+    layer.v.copy_(V.cuda())
+    seq = torch.tensor(T0, dtype=torch.int32, device="cuda")
+    sb.sparda_compress_keys(shape, layer, seq, B)
+    Kref, Vref = to64(K), to64(V)
+    for s in range(steps):
+        T = [t + s + 1 for t in T0]                      # the new token sits at T - 1
+        kn = synth.normal_bf16((B, 2, 128), 13, s, 1)
+        vn = synth.normal_bf16((B, 2, 128), 13, s, 2)
+        seq.copy_(torch.tensor(T, dtype=torch.int32))
+        sb.sparda_append_kv(shape, layer, kn.cuda(), vn.cuda(), seq, B)
+        for b in range(B):
+            Kref[b, :, T[b] - 1] = to64(kn[b])
+            Vref[b, :, T[b] - 1] = to64(vn[b])
+    torch.cuda.synchronize()
+    k_gpu, v_gpu, ck = to64(layer.k), to64(layer.v), to64(layer.ck)
+    for b in range(B):
+        T = T0[b] + steps
+        assert np.array_equal(k_gpu[b, :, :T], Kref[b, :, :T])
+        assert np.array_equal(v_gpu[b, :, :T], Vref[b, :, :T])
+        for g in range(2):
+            W = O.num_windows(T)
+            assert np.array_equal(ck[b, g, :W], O.compress_keys(Kref[b, g], W)), (b, g)
+    _no_device_error(sb)
+
+
+# ------------------------------------------------------------------ forecast projection
+@pytest.mark.parametrize("B,rows,hidden", [(1, 256, 4096), (5, 256, 4096), (16, 256, 4096),
+                                           (20, 64, 96), (64, 256, 4096)])
+def test_forecast_project(sb, B, rows, hidden):
+    W = synth.normal_bf16((rows, hidden), 21, B, std=0.02)
+    h = synth.normal_bf16((B, hidden), 22, B)
+    f = torch.empty((B, rows), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_forecast_project(W.cuda(), h.cuda(), f)
+    torch.cuda.synchronize()
+    got = to64(f)
+    Wd, hd = to64(W), to64(h)
+    exact = hd @ Wd.T                                    # unrounded float64 products
+    want = O.bf16_round(exact)
+    diff = got != want
+    # A float32 sum may round to the other bf16 neighbour only when the exact value sits
+    # within float32 accumulation error of the midpoint between the two (and then the two
+    # values are neighbours, since the exact value lies between them).
+    if diff.any():
+        lo, hi = np.minimum(got, want)[diff], np.maximum(got, want)[diff]
+        mid = (lo + hi) / 2
+        e = exact[diff]
+        assert np.all(np.abs(e - mid) <= 2e-4 * np.abs(e) + 1e-6), "non-midpoint rounding difference"
+    assert diff.mean() < 0.01
+
+
+# ------------------------------------------------------------------ forecast selector
+def _select_case(sb, K, f, T_list, k, max_ctx):
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    ck = torch.zeros((B, 2, shape.w_cap, 128), dtype=torch.bfloat16)
+    Sref = {}
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            W = O.num_windows(T - 1)
+            c = O.compress_keys(to64(K[b, g]), W)
+            ck[b, g, :W] = torch.from_numpy(c).to(torch.bfloat16)
+            s = O.forecast_scores(c, to64(f[b, g]))
+            Sref[b, g] = O.pool_to_blocks(s, (T - 1) // 64 + 1)
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    idx = torch.full((B, 2, k + 2), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, 2), -7, dtype=torch.int32, device="cuda")
+    ws = sb.workspace(shape, B, sb.WS_SELECT)
+    for rep in range(2):                                 # the workspace is reusable as left
+        sb.sparda_forecast_select(shape, ck.cuda(), f.cuda(), seq, B, idx, cnt, ws)
+        torch.cuda.synchronize()
+        unique = 0
+        for b, T in enumerate(T_list):
+            for g in range(2):
+                unique += check_selection(idx[b, g].cpu().numpy(), cnt[b, g].item(), Sref[b, g], T, k)
+    _no_device_error(sb)
+    return unique
+
+
+def test_select_tiny_planted(sb):
+    # batch 1, context 4096, k = 8, 8 planted blocks per group shifted along the forecast
+    for seed in range(3):
+        case = synth.tiny_case(seed)
+        unique = _select_case(sb, case["K"], case["f"], [4096], 8, 4096)
+        assert unique >= 1
+
+
+@pytest.mark.parametrize("T_list,k,max_ctx", [
+    ([1, 2, 64, 65], 8, 1024),                # no candidates: forced blocks only
+    ([129, 200, 256, 257], 8, 1024),          # fewer candidates than k
+    ([4096, 4000, 1000, 3333], 8, 4096),
+    ([8192, 7777, 5000, 6401], 32, 8192),     # k = 32, ragged tails
+    ([16384, 9999], 62, 16384),               # the largest k
+])
+def test_select_ragged(sb, T_list, k, max_ctx):
+    B = len(T_list)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 31, B, k)
+    f = synth.normal_bf16((B, 2, 128), 32, B, k)
+    _select_case(sb, K, f, T_list, k, max_ctx)
+
+
+def test_select_ties_break_to_lower_block(sb):
+    # Every window identical -> every candidate block scores the same; the selection must be
+    # the k lowest candidate indices.
+    T, k = 2048, 8
+    K = torch.ones((1, 2, T, 128), dtype=torch.bfloat16) * 0.5
+    f = torch.ones((1, 2, 128), dtype=torch.bfloat16)
+    shape = sb.Shape(max_ctx=T, max_batch=1, topk=k)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    seq = torch.tensor([T], dtype=torch.int32, device="cuda")
+    sb.sparda_compress_keys(shape, layer, torch.tensor([T - 1], dtype=torch.int32, device="cuda"), 1)
+    idx = torch.zeros((1, 2, k + 2), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    ws = sb.workspace(shape, 1, sb.WS_SELECT)
+    sb.sparda_forecast_select(shape, layer.ck, f.cuda(), seq, 1, idx, cnt, ws)
+    torch.cuda.synchronize()
+    for g in range(2):
+        assert idx[0, g].tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 8, 31]
+    _no_device_error(sb)
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("T_list,k,max_ctx", [
+    ([4096], 8, 4096),
+    ([1, 63, 64, 65], 8, 1024),
+    ([3000, 1500, 4095], 8, 4096),
+    ([8192, 7000], 32, 8192),
+    ([16384], 62, 16384),
+])
+def test_sparse_attention(sb, T_list, k, max_ctx):
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 41, B, k)
+    V = synth.normal_bf16((B, 2, max_ctx, 128), 42, B, k)
+    q = synth.normal_bf16((B, 32, 128), 43, B, k)
+    f = synth.normal_bf16((B, 2, 128), 44, B, k)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    layer.v.copy_(V.cuda())
+    idx = torch.full((B, 2, k + 2), -1, dtype=torch.int32)
+    cnt = torch.zeros((B, 2), dtype=torch.int32)
+    sels = {}
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            sel = O.forecast_select_one(to64(K[b, g]), to64(f[b, g]), T, k)
+            sels[b, g] = sel
+            idx[b, g, :len(sel)] = torch.tensor(sel, dtype=torch.int32)
+            cnt[b, g] = len(sel)
+    out = torch.full((B, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sb.workspace(shape, B, sb.WS_ATTN)
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    for rep in range(2):
+        sb.sparda_sparse_decode_attn(shape, layer, q.cuda(), idx.cuda(), cnt.cuda(), seq, B, out, ws)
+        torch.cuda.synchronize()
+        o = to64(out)
+        for b, T in enumerate(T_list):
+            for g in range(2):
+                ref = O.block_sparse_attention(to64(q[b, 16 * g:16 * g + 16]), to64(K[b, g]),
+                                               to64(V[b, g]), sels[b, g], T)
+                check_attention(o[b, 16 * g:16 * g + 16], ref)
+    _no_device_error(sb)
+
+
+def test_attention_all_blocks_equals_dense(sb):
+    T, max_ctx = 1000, 1024
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=1, topk=62)
+    K = synth.normal_bf16((1, 2, max_ctx, 128), 51, 0)
+    V = synth.normal_bf16((1, 2, max_ctx, 128), 52, 0)
+    q = synth.normal_bf16((1, 32, 128), 53, 0)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    layer.v.copy_(V.cuda())
+    nb = (T - 1) // 64 + 1
+    idx = torch.full((1, 2, 64), -1, dtype=torch.int32)
+    idx[:, :, :nb] = torch.arange(nb, dtype=torch.int32)
+    cnt = torch.full((1, 2), nb, dtype=torch.int32)
+    out = torch.empty((1, 32, 128), dtype=torch.bfloat16, device="cuda")
+    ws = sb.workspace(shape, 1, sb.WS_ATTN)
+    sb.sparda_sparse_decode_attn(shape, layer, q.cuda(), idx.cuda(), cnt.cuda(),
+                                 torch.tensor([T], dtype=torch.int32, device="cuda"), 1, out, ws)
+    torch.cuda.synchronize()
+    for g in range(2):
+        ref = O.dense_causal_attention(to64(q[0, 16 * g:16 * g + 16]), to64(K[0, g]), to64(V[0, g]), T)
+        check_attention(to64(out[0, 16 * g:16 * g + 16]), ref)
+    _no_device_error(sb)
+
+
+def test_bad_seq_len_and_index_set_device_error(sb):
+    shape = sb.Shape(max_ctx=1024, max_batch=2, topk=8)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.zero_()
+    layer.v.zero_()
+    seq = torch.tensor([0, 5000], dtype=torch.int32, device="cuda")
+    idx = torch.zeros((2, 2, 10), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((2, 2), dtype=torch.int32, device="cuda")
+    ws = sb.workspace(shape, 2, sb.WS_SELECT)
+    f = torch.zeros((2, 2, 128), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_forecast_select(shape, layer.ck, f, seq, 2, idx, cnt, ws)
+    assert sb.sparda_device_error(clear=True) & sb.DEV_BAD_SEQ_LEN
+    assert cnt.abs().sum().item() == 0 and (idx == -1).all()
+    # a block index beyond the sequence is skipped and reported, never dereferenced
+    seq = torch.tensor([100, 100], dtype=torch.int32, device="cuda")
+    idx = torch.tensor([[[0, 5] + [-1] * 8] * 2] * 2, dtype=torch.int32, device="cuda")
+    cnt = torch.full((2, 2), 2, dtype=torch.int32, device="cuda")
+    out = torch.empty((2, 32, 128), dtype=torch.bfloat16, device="cuda")
+    wa = sb.workspace(shape, 2, sb.WS_ATTN)
+    q = torch.zeros((2, 32, 128), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_sparse_decode_attn(shape, layer, q, idx, cnt, seq, 2, out, wa)
+    assert sb.sparda_device_error(clear=True) & sb.DEV_BAD_INDEX

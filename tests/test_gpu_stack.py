@@ -1,0 +1,119 @@
+"""A whole decode step of a small layer stack (forecast lookahead, layer 0 same-layer
+forecast) through DecodeStack, eager and replayed from a CUDA graph, against the oracle's
+decode_step on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import sparda_oracle as O
+from tests.parity import check_attention, check_selection, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sb(cuda_ok):
+    from block_sparse_attention_forecast_gb300 import build
+    build.build()
+    import block_sparse_attention_forecast_gb300.binding as b
+    b.sparda_device_error(clear=True)
+    return b
+
+
+def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted):
+    """Seeded caches holding tokens 0..T-2, the step's inputs, and forecast heads; planted
+    blocks of each layer are shifted along the forecast (computed by the oracle) that selects
+    that layer's blocks."""
+    from block_sparse_attention_forecast_gb300.step import DecodeStack
+    G, d = 2, 128
+    shape = sb.Shape(n_groups=G, topk=topk, max_ctx=max_ctx, max_batch=B)
+    W_self0 = synth.normal_bf16((G * d, hidden), seed, 100, std=0.02)
+    W_next = [synth.normal_bf16((G * d, hidden), seed, 101, L, std=0.02) for L in range(n_layers - 1)]
+    h = synth.normal_bf16((n_layers, B, hidden), seed, 102)
+    q = synth.normal_bf16((n_layers, B, G * 16, d), seed, 103)
+    kn = synth.normal_bf16((n_layers, B, G, d), seed, 104)
+    vn = synth.normal_bf16((n_layers, B, G, d), seed, 105)
+    nb = (T - 1) // 64 + 1
+    Ks, Vs, layers = [], [], []
+    for L in range(n_layers):
+        K = synth.normal_bf16((B, G, max_ctx, d), seed, 200, L)
+        V = synth.normal_bf16((B, G, max_ctx, d), seed, 201, L)
+        Wsel, hsel = (W_self0, h[0]) if L == 0 else (W_next[L - 1], h[L - 1])
+        for b in range(B):
+            f = O.forecast_project(to64(Wsel), to64(hsel[b])).reshape(G, d)
+            for g in range(G):
+                synth.plant(K[b, g], synth.planted_blocks(seed, nb, n_planted, L, b, g), f[g])
+        layer = sb.LayerKV.empty(shape)
+        layer.k.copy_(K.cuda())
+        layer.v.copy_(V.cuda())
+        sb.sparda_compress_keys(shape, layer, torch.full((B,), T - 1, dtype=torch.int32, device="cuda"), B)
+        Ks.append(K)
+        Vs.append(V)
+        layers.append(layer)
+    stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B)
+    stack.h.copy_(h.cuda())
+    stack.q.copy_(q.cuda())
+    stack.k_new.copy_(kn.cuda())
+    stack.v_new.copy_(vn.cuda())
+    stack.seq_len.fill_(T)
+    inputs = dict(W_self0=W_self0, W_next=W_next, h=h, q=q, kn=kn, vn=vn, K=Ks, V=Vs)
+    return shape, stack, inputs
+
+
+def oracle_step(inputs, n_layers, B, T, topk):
+    layers = [(to64(inputs["K"][L]), to64(inputs["V"][L])) for L in range(n_layers)]
+    p = T - 1
+    sel, out = O.decode_step(layers, to64(inputs["W_self0"]), [to64(w) for w in inputs["W_next"]],
+                             [to64(inputs["h"][L]) for L in range(n_layers)],
+                             [to64(inputs["q"][L]) for L in range(n_layers)],
+                             [to64(inputs["kn"][L]) for L in range(n_layers)],
+                             [to64(inputs["vn"][L]) for L in range(n_layers)], p, topk, 16)
+    # block scores of every selection, for the near-tie rule
+    S = {}
+    for L in range(n_layers):
+        Wsel, hsel = (inputs["W_self0"], inputs["h"][0]) if L == 0 else (inputs["W_next"][L - 1], inputs["h"][L - 1])
+        for b in range(B):
+            f = O.forecast_project(to64(Wsel), to64(hsel[b])).reshape(2, 128)
+            for g in range(2):
+                _, S[L, b, g] = O.forecast_select_one(layers[L][0][b, g], f[g], T, topk, return_scores=True)
+    return sel, out, S
+
+
+def compare(stack, sel, out, S, n_layers, B, T, topk):
+    idx, cnt, o = stack.idx.cpu().numpy(), stack.cnt.cpu().numpy(), to64(stack.out)
+    same = 0
+    for L in range(n_layers):
+        for b in range(B):
+            for g in range(2):
+                check_selection(idx[L, b, g], cnt[L, b, g], S[L, b, g], T, topk)
+                if list(idx[L, b, g, :cnt[L, b, g]]) == sel[L][b][g]:
+                    same += 1
+                    check_attention(o[L, b, 16 * g:16 * g + 16], out[L][b, 16 * g:16 * g + 16])
+    return same
+
+
+@pytest.mark.parametrize("n_layers,B,T,topk,max_ctx,hidden", [
+    (3, 2, 1500, 8, 2048, 256),
+    (4, 3, 4097, 32, 8192, 4096),
+])
+def test_stack_step_eager_and_graph(sb, n_layers, B, T, topk, max_ctx, hidden):
+    shape, stack, inputs = make_stack_case(sb, 7, n_layers, B, T, topk, max_ctx, hidden, 8)
+    sel, out, S = oracle_step(inputs, n_layers, B, T, topk)
+    # eager
+    stack.enqueue()
+    torch.cuda.synchronize()
+    same = compare(stack, sel, out, S, n_layers, B, T, topk)
+    assert same >= n_layers * B * 2 * 3 // 4
+    eager_out = stack.out.clone()
+    eager_idx = stack.idx.clone()
+    # the same step replayed from a CUDA graph: the step rewrites token T-1, so the result
+    # is identical
+    stack.out.zero_()
+    stack.capture()
+    stack.out.zero_()
+    stack.run()
+    torch.cuda.synchronize()
+    assert torch.equal(stack.idx, eager_idx)
+    assert torch.equal(stack.out, eager_out)
+    assert sb.sparda_device_error(clear=True) == 0
