@@ -251,7 +251,7 @@ int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void
   SelectArgs a{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
                seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
                reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
-               s->topk, select_chunk_blocks(nb_cap(s), bgc)};
+               s->topk, select_chunk_blocks(nb_cap(s), bgc), 0};
   launch_forecast_select(a, bgc, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
@@ -291,7 +291,7 @@ int32_t sparda_sparse_decode_attn(const sparda_shape* s, const sparda_layer_kv* 
              reinterpret_cast<float*>(w + counters_bytes(s)),
              reinterpret_cast<float*>(w + counters_bytes(s) + attn_o_bytes(s)),
              reinterpret_cast<unsigned*>(w), err, s->n_groups, s->max_ctx, kslots(s), attn_splits(s),
-             L->on_host ? 1 : 0};
+             L->on_host ? 1 : 0, 0};
   launch_sparse_attn(a, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }

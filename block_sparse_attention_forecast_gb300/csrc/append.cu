@@ -50,11 +50,15 @@ __global__ void __launch_bounds__(64) append_kv_kernel(AppendArgs a) {
   }
   if (T >= kWinKernel && (T - kWinKernel) % kWinStride == 0) {
     const int i = (T - kWinKernel) / kWinStride;
+    uint32_t xs[kWinKernel - 1];           // all loads in flight before the sums
+#pragma unroll
+    for (int u = 0; u < kWinKernel - 1; ++u)
+      xs[u] = load_key2(a.k, a.hot_k, a.on_host, bg, a.max_ctx, tb, T - kWinKernel + u, t);
     double s0 = bf16_lo(kn), s1 = bf16_hi(kn);
-    for (int tok = T - kWinKernel; tok < p; ++tok) {
-      const uint32_t x = load_key2(a.k, a.hot_k, a.on_host, bg, a.max_ctx, tb, tok, t);
-      s0 += bf16_lo(x);
-      s1 += bf16_hi(x);
+#pragma unroll
+    for (int u = 0; u < kWinKernel - 1; ++u) {
+      s0 += bf16_lo(xs[u]);
+      s1 += bf16_hi(xs[u]);
     }
     __nv_bfloat16* dst = a.ck + ((size_t)bg * a.W_cap + i) * kHeadDim + 2 * t;
     dst[0] = f64_to_bf16_rn(s0 / kWinKernel);

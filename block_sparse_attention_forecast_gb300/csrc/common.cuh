@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/sparda.h"
+#include "sparda.h"
 
 namespace sparda {
 

@@ -49,6 +49,7 @@ struct SelectArgs {
   unsigned* counters;            // workspace [B*G], zero between calls
   int* err;
   int G, W_cap, max_ctx, nb_cap, topk, chunk_blocks;
+  int n_units;                   // B*G*nb_cap, set by the launcher
 };
 
 struct AttnArgs {
@@ -62,6 +63,7 @@ struct AttnArgs {
   unsigned* counters;            // workspace [B*G]
   int* err;
   int G, max_ctx, kslots, n_split, offload;
+  int n_units;                   // B*G*kslots, set by the launcher
 };
 
 struct PrefetchArgs {

@@ -1,42 +1,54 @@
 // The Forecast selector (bittide thread: one forecast head per GQA group, no softmax;
 // techwalker section 二; 10100 "SparDA 的解法"): score every compressed key of the target
-// layer with the group's forecast vector, max-pool the window scores onto 64-token blocks and
-// keep the top-k blocks plus block 0 and the tail block.
+// layer with the group's forecast vector, max-pool the window scores onto 64-token blocks
+// (windows 4j-1 .. 4j+3 overlap block j) and keep the top-k blocks plus block 0 and the tail
+// block.
 //
-// One kernel. A CTA owns `chunk_blocks` consecutive blocks of one (sequence, group): it
-// stages the contiguous run of compressed keys those blocks need with one bulk TMA copy,
-// scores them (8 lanes per window, float32), max-pools them and writes the block scores to
-// the workspace. The last CTA of the (sequence, group) to finish -- found with a counter in
-// the workspace, which it resets -- selects the top-k by a 4-pass radix select on
-// order-preserving 32-bit keys and writes the sorted block list.
-#include <climits>
-
+// Persistent kernel, one CTA per SM. The work is the list of (sequence-group, block) units,
+// B*G*nb_cap of them; CTA c owns the contiguous range [U*c/grid, U*(c+1)/grid), cut into
+// sub-chunks of up to 16 blocks that never cross a group boundary. Warp 8 is the producer:
+// one lane streams the compressed keys each sub-chunk needs (64 windows, 16 KiB, one bulk
+// TMA copy) into an 8-stage shared-memory ring guarded by full/empty mbarriers. Warps 0-7
+// consume: 4 lanes per window, 16-byte shared loads, float32 FMAs against the group's
+// forecast held in registers, a 2-step shuffle reduction, then the max-pool of each block
+// from its five windows (the window left of a sub-chunk is carried over from the previous
+// sub-chunk, or loaded with the first sub-chunk of a range) and a store of the block scores.
+//
+// When a CTA finishes its part of a (sequence, group), it bumps that group's counter in the
+// workspace; the last of the covering CTAs selects the top-k by a 4-pass radix select on
+// order-preserving 32-bit keys (ties to the lower block index) and writes the sorted list.
+// Because ranges are contiguous, that selection overlaps the producer's loads for the next
+// group; only the last group of the last CTA is a tail.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sparda {
 
-constexpr int kSelThreads = 256;
-constexpr int kMaxBlocksPerSeq = kMaxCtx / kBlock;                 // 4096
-constexpr int kKeysPerThread = kMaxBlocksPerSeq / kSelThreads;     // 16
-constexpr int kSmemHeader = 128;                                   // mbarrier + padding
+constexpr int kSelConsumerWarps = 8;
+constexpr int kSelConsumers = kSelConsumerWarps * 32;     // 256
+constexpr int kSelThreads = kSelConsumers + 32;
+constexpr int kSubBlocks = 16;                            // blocks per sub-chunk
+constexpr int kSubWindows = kWinPerBlock * kSubBlocks;    // 64 windows per sub-chunk
+constexpr int kSelStages = 8;
+constexpr int kSelStageBytes = (kSubWindows + 1) * kRowBytes;   // + the left window
+constexpr int kMaxBlocksPerSeq = kMaxCtx / kBlock;        // 4096
+constexpr int kKeysPerThread = kMaxBlocksPerSeq / kSelConsumers;  // 16
+constexpr int kSelSmem = 128 /*align slack*/ + 128 /*barriers*/ + kSelStages * kSelStageBytes;
 
-size_t smem_select_bytes(int chunk_blocks) {
-  const int nw = kWinPerBlock * chunk_blocks + 1;
-  return kSmemHeader + (size_t)nw * kRowBytes + (size_t)nw * sizeof(float);
+size_t smem_select_bytes(int) { return kSelSmem; }
+int select_chunk_blocks(int, int) { return kSubBlocks; }
+
+__device__ __forceinline__ void sel_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kSelConsumers) : "memory");
 }
 
-int select_chunk_blocks(int nb_cap, int bg_count) {
-  // Aim at about four resident CTAs per SM over 152 SMs; chunks of 16 .. 64 blocks.
-  const long total = (long)nb_cap * bg_count;
-  int ch = 16;
-  while (ch < 64 && total / ch > 152L * 4) ch *= 2;
-  return ch;
+__device__ __forceinline__ void sel_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Inclusive prefix sum over the 256 threads of the CTA; `warp_tot` is 8 words of shared
-// memory. Returns the inclusive sum; *total gets the CTA-wide sum.
-__device__ __forceinline__ int cta_inclusive_scan(int v, int* warp_tot, int* total) {
+// Inclusive prefix sum over the 256 consumer threads; `warp_tot` is 8 words of shared
+// memory. *total gets the sum over all consumers.
+__device__ __forceinline__ int sel_scan(int v, int* warp_tot, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -44,32 +56,37 @@ __device__ __forceinline__ int cta_inclusive_scan(int v, int* warp_tot, int* tot
     if (lane >= o) v += n;
   }
   if (lane == 31) warp_tot[warp] = v;
-  __syncthreads();
+  sel_sync();
   int before = 0, all = 0;
 #pragma unroll
-  for (int w = 0; w < kSelThreads / 32; ++w) {
+  for (int w = 0; w < kSelConsumerWarps; ++w) {
     const int x = warp_tot[w];
     if (w < warp) before += x;
     all += x;
   }
-  __syncthreads();  // warp_tot may be reused right after
+  sel_sync();
   *total = all;
   return v + before;
 }
 
-__device__ void select_topk(const SelectArgs& a, int bg, int T) {
-  __shared__ unsigned hist[256];
-  __shared__ int warp_tot[kSelThreads / 32];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_krem;
+struct TopkShared {
+  unsigned hist[256];
+  int warp_tot[kSelConsumerWarps];
+  uint32_t prefix;
+  int krem;
+  int last;
+};
 
+// Top-k of one (sequence, group) by the 256 consumer threads, from the block scores the
+// covering CTAs stored in the workspace.
+__device__ void select_topk(const SelectArgs& a, int bg, int T, TopkShared& sh) {
   const int t = threadIdx.x;
   const int kslots = a.topk + 2;
   int32_t* idx = a.idx + (size_t)bg * kslots;
   const bool valid = (T >= 1 && T <= a.max_ctx);
   const int tb = valid ? (T - 1) / kBlock : -1;
   const int nb = tb + 1;
-  const int per = (nb + kSelThreads - 1) / kSelThreads;
+  const int per = (nb + kSelConsumers - 1) / kSelConsumers;
   const int jb = t * per;
   const float* S = a.block_scores + (size_t)bg * a.nb_cap;
 
@@ -82,8 +99,8 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T) {
   const int n_cand = max(0, tb - 1);
   const int k_eff = min(a.topk, n_cand);
 
-  // Threshold: a candidate is kept when key > thr, or key == thr and fewer than take_eq
-  // equal keys sit at lower block indices.
+  // A candidate is kept when key > thr, or key == thr and fewer than take_eq equal keys
+  // sit at lower block indices.
   uint32_t thr;
   int take_eq;
   if (k_eff == n_cand) {
@@ -96,23 +113,29 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T) {
     uint32_t prefix = 0u, mask = 0u;
     int krem = k_eff;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[t] = 0u;
-      __syncthreads();
+      sh.hist[t] = 0u;
+      sel_sync();
+      // Scores cluster in a few exponents, so most keys share a digit in the first passes:
+      // lanes with equal digits add their count with one atomic (warp-aggregated).
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e)
-        if (key[e] != 0u && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & 255u], 1u);
-      __syncthreads();
-      const int v = (int)hist[255 - t];      // thread t looks at digit 255 - t
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        const bool in = key[e] != 0u && (key[e] & mask) == prefix;
+        const unsigned d = in ? (key[e] >> shift) & 255u : 256u;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
+      }
+      sel_sync();
+      const int v = (int)sh.hist[255 - t];      // thread t looks at digit 255 - t
       int tot;
-      const int incl = cta_inclusive_scan(v, warp_tot, &tot);
+      const int incl = sel_scan(v, sh.warp_tot, &tot);
       const int excl = incl - v;
       if (excl < krem && incl >= krem) {
-        s_prefix = prefix | ((uint32_t)(255 - t) << shift);
-        s_krem = krem - excl;
+        sh.prefix = prefix | ((uint32_t)(255 - t) << shift);
+        sh.krem = krem - excl;
       }
-      __syncthreads();
-      prefix = s_prefix;
-      krem = s_krem;
+      sel_sync();
+      prefix = sh.prefix;
+      krem = sh.krem;
       mask |= 255u << shift;
     }
     thr = prefix;
@@ -123,7 +146,7 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T) {
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) my_eq += (key[e] != 0u && key[e] == thr);
   int dummy;
-  int rank = cta_inclusive_scan(my_eq, warp_tot, &dummy) - my_eq;
+  int rank = sel_scan(my_eq, sh.warp_tot, &dummy) - my_eq;
 
   bool sel[kKeysPerThread];
   int my_sel = 0;
@@ -147,118 +170,207 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T) {
     my_sel += s;
   }
   int total;
-  int pos = cta_inclusive_scan(my_sel, warp_tot, &total) - my_sel;
+  int pos = sel_scan(my_sel, sh.warp_tot, &total) - my_sel;
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e)
     if (sel[e] && pos < kslots) idx[pos++] = jb + e;
-  for (int s = total + t; s < kslots; s += kSelThreads) idx[s] = -1;
+  for (int s = total + t; s < kslots; s += kSelConsumers) idx[s] = -1;
   if (t == 0) a.cnt[bg] = min(total, kslots);
 }
 
-__global__ void __launch_bounds__(kSelThreads) forecast_select_kernel(const SelectArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* tile = smem + kSmemHeader;
-  const int CH = a.chunk_blocks;
-  const int nw_max = kWinPerBlock * CH + 1;
-  float* s_sc = reinterpret_cast<float*>(tile + (size_t)nw_max * kRowBytes);
-  __shared__ bool s_last;
+__device__ __forceinline__ int sel_cta_of_unit(long long u, int grid, long long U) {
+  return (int)(((u + 1) * grid - 1) / U);
+}
 
-  const int bg = blockIdx.y;
-  const int b = bg / a.G;
-  const int t = threadIdx.x;
-  const int T = a.seq_len[b];
-  const bool valid = (T >= 1 && T <= a.max_ctx);
-  if (!valid && t == 0 && blockIdx.x == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+// Per (sequence, group) constants.
+struct SelGroup {
+  int T, nb, W;
+  bool valid;
+};
 
-  const int nb = valid ? (T - 1) / kBlock + 1 : 0;
-  const int W = valid ? num_windows(T - 1) : 0;
-  const int j0 = blockIdx.x * CH;
-  const int j1 = min(j0 + CH, nb);
-  if (j0 < j1) {
-    const int w0 = max(0, kWinPerBlock * j0 - 1);
-    const int w1 = min(W, kWinPerBlock * j1);
-    const int nw = w1 - w0;
-    bool ok = true;
-    if (nw > 0) {
-      if (t == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        const uint32_t bytes = (uint32_t)nw * kRowBytes;
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(tile, a.ck + ((size_t)bg * a.W_cap + w0) * kHeadDim, bytes, bar);
+__device__ __forceinline__ SelGroup sel_group(const SelectArgs& a, int bg) {
+  SelGroup gr;
+  gr.T = a.seq_len[bg / a.G];
+  gr.valid = gr.T >= 1 && gr.T <= a.max_ctx;
+  gr.nb = gr.valid ? (gr.T - 1) / kBlock + 1 : 0;
+  gr.W = gr.valid ? num_windows(gr.T - 1) : 0;
+  return gr;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const SelectArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kSelStages;
+  uint8_t* ring = smem + 128;
+  __shared__ float s_win[kSubWindows + 1];
+  __shared__ TopkShared sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long U = (long long)a.n_units;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const long long J0 = U * cta / grid, J1 = U * (cta + 1) / grid;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSelStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kSelConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kSelConsumerWarps) {
+    // -------------------------------------------------------------- producer
+    if (lane != 0) return;
+    int it = 0;
+    for (long long u = J0; u < J1;) {
+      const int bg = (int)(u / a.nb_cap);
+      const long long seg_end = min(J1, (long long)(bg + 1) * a.nb_cap);
+      const SelGroup gr = sel_group(a, bg);
+      const int jseg0 = (int)(u - (long long)bg * a.nb_cap);
+      const int jseg1 = (int)(seg_end - (long long)bg * a.nb_cap);
+      u = seg_end;
+      for (int j0 = jseg0; j0 < min(jseg1, gr.nb); j0 += kSubBlocks) {
+        const int j1 = min(min(j0 + kSubBlocks, jseg1), gr.nb);
+        const int w0 = (j0 == jseg0) ? max(0, kWinPerBlock * j0 - 1) : kWinPerBlock * j0;
+        const int w1 = min(gr.W, kWinPerBlock * j1);
+        const int stage = it % kSelStages;
+        if (it >= kSelStages && !mbar_wait(&empty[stage], ((it / kSelStages) & 1) ^ 1, a.err)) return;
+        if (w1 > w0) {
+          const uint32_t bytes = (uint32_t)(w1 - w0) * kRowBytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          bulk_load(ring + stage * kSelStageBytes, a.ck + ((size_t)bg * a.W_cap + w0) * kHeadDim, bytes,
+                    &full[stage]);
+        } else {
+          sel_arrive(&full[stage]);             // nothing to load: complete the phase
+        }
+        ++it;
       }
-      // forecast slice of this thread: dims 8c..8c+7 and 64+8c..64+8c+7
-      const int c = t & 7;
-      float fr[16];
-      {
-        const uint4* fp = reinterpret_cast<const uint4*>(a.f + (size_t)bg * kHeadDim);
-        const uint4 u0 = fp[c], u1 = fp[8 + c];
-        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int t = tid;
+  const int c = t & 3;                 // lane within a window: dims 8c + 32k, k = 0..3
+  const int wl = t >> 2;               // window of this thread within a 64-window pass
+  int it = 0;
+  bool ok = true;                      // false after a wait ran out: skip compute, keep pace
+  for (long long u = J0; u < J1;) {
+    const int bg = (int)(u / a.nb_cap);
+    const long long seg_end = min(J1, (long long)(bg + 1) * a.nb_cap);
+    const SelGroup gr = sel_group(a, bg);
+    if (!gr.valid && t == 0 && u == (long long)bg * a.nb_cap) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    const int jseg0 = (int)(u - (long long)bg * a.nb_cap);
+    const int jseg1 = (int)(seg_end - (long long)bg * a.nb_cap);
+    u = seg_end;
+    // forecast slice of this thread
+    float fr[32];
+    {
+      const uint4* fp = reinterpret_cast<const uint4*>(a.f + (size_t)bg * kHeadDim);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          fr[2 * e] = bf16_lo(w[e]);
-          fr[2 * e + 1] = bf16_hi(w[e]);
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = fp[c + 4 * k];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          fr[8 * k + 2 * e] = bf16_lo(w[e]);
+          fr[8 * k + 2 * e + 1] = bf16_hi(w[e]);
         }
       }
-      __syncthreads();                       // mbarrier initialised before anyone waits
-      ok = __syncthreads_and(mbar_wait(bar, 0, a.err));   // uniform across the CTA
-      if (ok) {
-        const int wl = t >> 3;               // 32 windows per pass, 8 lanes each
-        for (int base = 0; base < nw; base += kSelThreads / 8) {
-          const int i = base + wl;
-          float acc = 0.f;
-          if (i < nw) {
-            const uint8_t* row = tile + (size_t)i * kRowBytes;
-            const uint4 x0 = *reinterpret_cast<const uint4*>(row + 16 * c);
-            const uint4 x1 = *reinterpret_cast<const uint4*>(row + 128 + 16 * c);
-            const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              acc = fmaf(fr[2 * e], bf16_lo(w[e]), acc);
-              acc = fmaf(fr[2 * e + 1], bf16_hi(w[e]), acc);
-            }
-          }
-          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          if (c == 0 && i < nw) s_sc[i] = acc;
-        }
-      }
-      __syncthreads();
     }
     float* S = a.block_scores + (size_t)bg * a.nb_cap;
-    for (int jj = t; jj < j1 - j0; jj += kSelThreads) {
-      const int j = j0 + jj;
-      const int lo = max(kWinPerBlock * j - 1, 0);
-      const int hi = min(kWinPerBlock * j + 3, W - 1);
-      float m = -INFINITY;
-      if (ok)
-        for (int i = lo; i <= hi; ++i) m = fmaxf(m, s_sc[i - w0]);
-      S[j] = m;
+    float carry = -INFINITY;              // score of the window left of the sub-chunk
+    for (int j0 = jseg0; j0 < min(jseg1, gr.nb); j0 += kSubBlocks) {
+      const int j1 = min(min(j0 + kSubBlocks, jseg1), gr.nb);
+      const int w0 = (j0 == jseg0) ? max(0, kWinPerBlock * j0 - 1) : kWinPerBlock * j0;
+      const int w1 = min(gr.W, kWinPerBlock * j1);
+      const int nw = max(0, w1 - w0);
+      const int stage = it % kSelStages;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kSelStages) & 1, a.err));
+      ++it;
+      const uint8_t* tile = ring + stage * kSelStageBytes;
+      for (int base = 0; base < nw; base += kSubWindows) {
+        const int i = base + wl;
+        float acc = 0.f;
+        if (ok && i < nw) {
+          const uint8_t* row = tile + (size_t)i * kRowBytes + 16 * c;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 x = *reinterpret_cast<const uint4*>(row + 64 * k);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc = fmaf(fr[8 * k + 2 * e], bf16_lo(w[e]), acc);
+              acc = fmaf(fr[8 * k + 2 * e + 1], bf16_hi(w[e]), acc);
+            }
+          }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (c == 0 && i < nw) s_win[i] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) sel_arrive(&empty[stage]);
+      sel_sync();                                   // s_win complete
+      if (t < j1 - j0) {                            // block j uses windows 4j-1 .. 4j+3 below W
+        const int j = j0 + t;
+        float m = -INFINITY;
+        if (ok) {
+#pragma unroll
+          for (int d = -1; d <= 3; ++d) {
+            const int w = kWinPerBlock * j + d;
+            if (w < 0 || w >= gr.W) continue;
+            const int li = w - w0;
+            m = fmaxf(m, li < 0 ? carry : s_win[li]);
+          }
+        }
+        S[j] = m;
+      }
+      const float next_carry = (nw > 0) ? s_win[nw - 1] : -INFINITY;
+      sel_sync();                                   // s_win free again
+      carry = next_carry;
     }
-  }
 
-  // The last CTA of this (sequence, group) selects.
-  __threadfence();
-  __syncthreads();
-  if (t == 0) {
-    const unsigned prev = atomicAdd(a.counters + bg, 1u);
-    s_last = (prev == gridDim.x - 1);
+    // this CTA's part of the group is done: count it; the last covering CTA selects
+    const long long first_u = (long long)bg * a.nb_cap, last_u = first_u + a.nb_cap - 1;
+    const int n_cover = sel_cta_of_unit(last_u, grid, U) - sel_cta_of_unit(first_u, grid, U) + 1;
+    sel_sync();                                     // block scores of all consumers stored
+    if (t == 0) {
+      __threadfence();
+      const unsigned prev = atomicAdd(a.counters + bg, 1u);
+      sh.last = (prev == (unsigned)(n_cover - 1));
+      if (sh.last) a.counters[bg] = 0u;
+      __threadfence();
+    }
+    sel_sync();
+    if (sh.last) select_topk(a, bg, gr.T, sh);
+    sel_sync();
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  select_topk(a, bg, T);
-  if (t == 0) a.counters[bg] = 0u;
+}
+
+static int sel_sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 152;
+  }
+  return n[dev];
 }
 
 void launch_forecast_select(const SelectArgs& a, int bg_count, cudaStream_t s) {
-  const size_t smem = smem_select_bytes(a.chunk_blocks);
-  cudaFuncSetAttribute(forecast_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem_select_bytes(64));
-  dim3 grid((a.nb_cap + a.chunk_blocks - 1) / a.chunk_blocks, bg_count);
-  forecast_select_kernel<<<grid, kSelThreads, smem, s>>>(a);
+  cudaFuncSetAttribute(forecast_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+  SelectArgs b = a;
+  b.n_units = bg_count * a.nb_cap;
+  const int by_work = (b.n_units + kSubBlocks - 1) / kSubBlocks;   // >= one sub-chunk each
+  const int grid = by_work < sel_sm_count() ? by_work : sel_sm_count();
+  forecast_select_kernel<<<grid, kSelThreads, kSelSmem, s>>>(b);
 }
 
 }  // namespace sparda
