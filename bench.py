@@ -160,33 +160,39 @@ def build_workload(device, seed, steps_total):
     return shape, stack, T0
 
 
-def kernel_times(stack, reps=10):
-    """Average device time of one forecast_select launch and one sparse_decode_attn launch,
-    timed with CUDA events on the launching stream over back-to-back launches of the step's
-    own calls (same buffers), after the timed region."""
+def kernel_times(stack, reps=4):
+    """Average device time of one forecast_select and one sparse_decode_attn launch: the
+    step's own calls for every layer (same buffers) captured back to back in a CUDA graph,
+    replayed and timed with CUDA events on the launching stream (no host launch overhead)."""
     import torch
     import block_sparse_attention_forecast_gb300.binding as sb
     sh, B, n = stack.shape, stack.batch, stack.n_layers
-    s = torch.cuda.current_stream()
 
-    def sel_loop():
+    def sel_loop(s):
         for L in range(1, n):
             sb.sparda_forecast_select(sh, stack.layers[L].ck, stack.f[L], stack.seq_len, B, stack.idx[L],
                                       stack.cnt[L], stack.ws_sel, stream=s)
 
-    def attn_loop():
+    def attn_loop(s):
         for L in range(n):
             sb.sparda_sparse_decode_attn(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L],
                                          stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
 
     out = {}
     for name, fn, per in (("select", sel_loop, n - 1), ("attn", attn_loop, n)):
-        fn()
+        fn(torch.cuda.current_stream())
         torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            s = torch.cuda.current_stream()
+            for _ in range(reps):
+                fn(s)
+        g.replay()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        for _ in range(reps):
-            fn()
+        g.replay()
         e1.record(s)
         torch.cuda.synchronize()
         out[name] = e0.elapsed_time(e1) * 1e-3 / (reps * per)

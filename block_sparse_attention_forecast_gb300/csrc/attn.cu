@@ -10,7 +10,7 @@
 // Warp 8 is the producer. Its 32 lanes read the metadata of 32 units at a time (sequence
 // length, selection count, block index) in parallel; lane 0 then issues, for every selected
 // block, four tiled TMA loads (K and V, two 64-column halves each, 128-byte swizzle) into a
-// 5-stage shared-memory ring guarded by full/empty mbarriers, and records the block index
+// 4-stage shared-memory ring guarded by full/empty mbarriers, and records the block index
 // beside the stage. Warps 0-7 consume in two groups of four that take alternate blocks, so
 // every SM sub-partition has two warps to switch between. Within a group, warp w takes
 // tokens 16w .. 16w+15 of its block: S = Q K^T with the group's 16 query heads as the M
@@ -18,7 +18,7 @@
 // with P re-packed from the S accumulators.
 //
 // At the end of a (sequence, group) in its range a CTA merges its eight warps' partial
-// results through shared memory. A group covered by one CTA is written out directly;
+// results through shared memory (one write, one read of a padded buffer). A group covered by one CTA is written out directly;
 // otherwise each covering CTA stores (O, max, sum) to the workspace and the last one to
 // arrive (a counter in the workspace, which it resets) merges them with log-sum-exp weights.
 // Because ranges are contiguous, that merge overlaps the producer's loads for the next group.
@@ -31,10 +31,11 @@ constexpr int kGroupWarps = 4;
 constexpr int kConsumerWarps = 2 * kGroupWarps;
 constexpr int kConsumers = kConsumerWarps * 32;             // 256
 constexpr int kAttnThreads = kConsumers + 32;
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kSlotBytes = 2 * kBlockBytes;                 // K + V of one block
 constexpr int kMStride = kHeadDim + 8;      // merge-buffer row stride (floats): no bank conflicts
-constexpr int kMergeFloats = kGroupWarps * (kHeads * kMStride + 2 * kHeads);
+constexpr int kMergeFloats = kConsumerWarps * (kHeads * kMStride + 2 * kHeads);
+constexpr int kMaxInlineSeg = 8;           // partials the last arriver keeps in registers
 constexpr int kAttnSmem = 1024 /*align slack*/ + 1024 /*header*/ + kStages * kSlotBytes +
                           kMergeFloats * 4;
 
@@ -83,9 +84,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
   int* stage_j = reinterpret_cast<int*>(empty + kStages);      // block index per stage
   int* s_flag = stage_j + kStages;
   uint8_t* ring = smem + 1024;
-  float* mO = reinterpret_cast<float*>(ring + kStages * kSlotBytes);    // [4][16][kMStride]
-  float* mM = mO + kGroupWarps * kHeads * kMStride;                     // [4][16]
-  float* mL = mM + kGroupWarps * kHeads;                                // [4][16]
+  float* mO = reinterpret_cast<float*>(ring + kStages * kSlotBytes);    // [8][16][kMStride]
+  float* mM = mO + kConsumerWarps * kHeads * kMStride;                  // [8][16]
+  float* mL = mM + kConsumerWarps * kHeads;                             // [8][16]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long U = (long long)a.n_units;
@@ -292,56 +293,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
     }
 
     // ---------------------------------------------------------- merge the eight warps
-    // group 1 hands its partials to group 0 (same lane layout), group 0 folds them in
     consumer_sync();                           // the merge buffer is free again
-    float* myO = mO + (wq * kHeads + g) * kMStride + 2 * cq;
-    if (grp == 1) {
+    {
+      float* myO = mO + (warp * kHeads + g) * kMStride + 2 * cq;
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         *reinterpret_cast<float2*>(myO + 8 * n) = make_float2(o[n][0], o[n][1]);
         *reinterpret_cast<float2*>(myO + 8 * n + 8 * kMStride) = make_float2(o[n][2], o[n][3]);
       }
       if (cq == 0) {
-        mM[wq * kHeads + g] = m0;
-        mM[wq * kHeads + g + 8] = m1;
-        mL[wq * kHeads + g] = l0;
-        mL[wq * kHeads + g + 8] = l1;
-      }
-    }
-    consumer_sync();
-    if (grp == 0) {
-      const float pm0 = mM[wq * kHeads + g], pm1 = mM[wq * kHeads + g + 8];
-      const float pl0 = mL[wq * kHeads + g], pl1 = mL[wq * kHeads + g + 8];
-      const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
-      const float b0 = (M0 == -INFINITY) ? 0.f : M0, b1 = (M1 == -INFINITY) ? 0.f : M1;
-      const float wa0 = exp2f(m0 - b0), wb0 = exp2f(pm0 - b0);
-      const float wa1 = exp2f(m1 - b1), wb1 = exp2f(pm1 - b1);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float2 x = *reinterpret_cast<const float2*>(myO + 8 * n);
-        const float2 y = *reinterpret_cast<const float2*>(myO + 8 * n + 8 * kMStride);
-        o[n][0] = wa0 * o[n][0] + wb0 * x.x;
-        o[n][1] = wa0 * o[n][1] + wb0 * x.y;
-        o[n][2] = wa1 * o[n][2] + wb1 * y.x;
-        o[n][3] = wa1 * o[n][3] + wb1 * y.y;
-      }
-      l0 = wa0 * l0 + wb0 * pl0;
-      l1 = wa1 * l1 + wb1 * pl1;
-      m0 = M0;
-      m1 = M1;
-    }
-    consumer_sync();
-    if (grp == 0) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        *reinterpret_cast<float2*>(myO + 8 * n) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(myO + 8 * n + 8 * kMStride) = make_float2(o[n][2], o[n][3]);
-      }
-      if (cq == 0) {
-        mM[wq * kHeads + g] = m0;
-        mM[wq * kHeads + g + 8] = m1;
-        mL[wq * kHeads + g] = l0;
-        mL[wq * kHeads + g + 8] = l1;
+        mM[warp * kHeads + g] = m0;
+        mM[warp * kHeads + g + 8] = m1;
+        mL[warp * kHeads + g] = l0;
+        mL[warp * kHeads + g + 8] = l1;
       }
     }
     consumer_sync();
@@ -349,13 +313,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
     const int h = t >> 4, d0 = (t & 15) * 8;
     float Mh = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kGroupWarps; ++w) Mh = fmaxf(Mh, mM[w * kHeads + h]);
+    for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, mM[w * kHeads + h]);
     const float baseh = (Mh == -INFINITY) ? 0.f : Mh;
     float Oh[8], Lh = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) Oh[e] = 0.f;
 #pragma unroll
-    for (int w = 0; w < kGroupWarps; ++w) {
+    for (int w = 0; w < kConsumerWarps; ++w) {
       const float wt = exp2f(mM[w * kHeads + h] - baseh);
       Lh += wt * mL[w * kHeads + h];
       const float4* src = reinterpret_cast<const float4*>(mO + (w * kHeads + h) * kMStride + d0);
@@ -389,37 +353,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
       pml[h] = Mh;
       pml[kHeads + h] = Lh;
     }
-    consumer_sync();                           // all partial stores issued
+    consumer_sync();                           // every consumer's partial stores are issued
     if (t == 0) {
-      __threadfence();
-      *s_flag = (atomicAdd(a.counters + bg, 1u) == (unsigned)(n_seg - 1));
+      // release: this CTA's partials (ordered by the barrier) before the count; acquire:
+      // the other CTAs' partials before the merge below
+      unsigned prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev) : "l"(a.counters + bg) : "memory");
+      *s_flag = (prev == (unsigned)(n_seg - 1));
       if (*s_flag) a.counters[bg] = 0u;
-      __threadfence();
     }
     consumer_sync();
     if (!*s_flag) continue;
     // last arriver: merge the n_seg partials of this group
     const float* pml0 = a.part_ml + (size_t)bg * a.kslots * 2 * kHeads;
     const float* po0 = a.part_o + (size_t)bg * a.kslots * kHeads * kHeadDim + h * kHeadDim + d0;
-    float M = -INFINITY;
-    for (int sg = 0; sg < n_seg; ++sg) M = fmaxf(M, __ldcg(pml0 + sg * 2 * kHeads + h));
-    const float base = (M == -INFINITY) ? 0.f : M;
-    float acc[8], L = 0.f;
+    float acc[8], L = 0.f, M = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int sg = 0; sg < n_seg; ++sg) {
-      const float wt = exp2f(__ldcg(pml0 + sg * 2 * kHeads + h) - base);
-      L += wt * __ldcg(pml0 + sg * 2 * kHeads + kHeads + h);
-      const float4* src = reinterpret_cast<const float4*>(po0 + (size_t)sg * kHeads * kHeadDim);
+    for (int s0 = 0; s0 < n_seg; s0 += kMaxInlineSeg) {
+      // issue every load of up to kMaxInlineSeg partials before combining them
+      float pm[kMaxInlineSeg], pl[kMaxInlineSeg];
+      float4 px[kMaxInlineSeg][2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float4 x = __ldcg(src + e);
-        acc[4 * e] += wt * x.x;
-        acc[4 * e + 1] += wt * x.y;
-        acc[4 * e + 2] += wt * x.z;
-        acc[4 * e + 3] += wt * x.w;
+      for (int q = 0; q < kMaxInlineSeg; ++q) {
+        const bool in = s0 + q < n_seg;
+        const int sg = in ? s0 + q : s0;
+        pm[q] = in ? __ldcg(pml0 + sg * 2 * kHeads + h) : -INFINITY;
+        pl[q] = __ldcg(pml0 + sg * 2 * kHeads + kHeads + h);
+        const float4* src = reinterpret_cast<const float4*>(po0 + (size_t)sg * kHeads * kHeadDim);
+        px[q][0] = __ldcg(src);
+        px[q][1] = __ldcg(src + 1);
       }
+      float Mn = M;
+#pragma unroll
+      for (int q = 0; q < kMaxInlineSeg; ++q) Mn = fmaxf(Mn, pm[q]);
+      const float base = (Mn == -INFINITY) ? 0.f : Mn;
+      const float sc = exp2f(M - base);         // rescale what was merged so far
+      L *= sc;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= sc;
+#pragma unroll
+      for (int q = 0; q < kMaxInlineSeg; ++q) {
+        const float wt = exp2f(pm[q] - base);
+        L += wt * pl[q];
+        acc[0] += wt * px[q][0].x; acc[1] += wt * px[q][0].y;
+        acc[2] += wt * px[q][0].z; acc[3] += wt * px[q][0].w;
+        acc[4] += wt * px[q][1].x; acc[5] += wt * px[q][1].y;
+        acc[6] += wt * px[q][1].z; acc[7] += wt * px[q][1].w;
+      }
+      M = Mn;
     }
     uint32_t pk[4];
 #pragma unroll

@@ -6,17 +6,19 @@
 //
 // Persistent kernel, one CTA per SM. The work is the list of (sequence-group, block) units,
 // B*G*nb_cap of them; CTA c owns the contiguous range [U*c/grid, U*(c+1)/grid), cut into
-// sub-chunks of up to 16 blocks that never cross a group boundary. Warp 8 is the producer:
-// one lane streams the compressed keys each sub-chunk needs (64 windows, 16 KiB, one bulk
-// TMA copy) into an 8-stage shared-memory ring guarded by full/empty mbarriers. Warps 0-7
-// consume: 4 lanes per window, 16-byte shared loads, float32 FMAs against the group's
-// forecast held in registers, a 2-step shuffle reduction, then the max-pool of each block
-// from its five windows (the window left of a sub-chunk is carried over from the previous
-// sub-chunk, or loaded with the first sub-chunk of a range) and a store of the block scores.
+// sub-chunks of up to 31 blocks that never cross a group boundary. Warp 8 is the producer:
+// one lane streams the compressed keys each sub-chunk needs -- its 124 windows plus the one
+// to their left, which the first block's max-pool also reads -- with one bulk TMA copy into
+// a 6-stage shared-memory ring guarded by full/empty mbarriers. Warps 0-7 consume in two
+// groups of four that take alternate sub-chunks: 4 lanes per window, 16-byte shared loads,
+// four independent float32 FMA chains against the group's forecast held in registers, a
+// 2-step shuffle reduction, then (after one group barrier) the max-pool of each block from
+// its five windows and a store of the block scores. Window scores are double-buffered per
+// group, so one barrier per sub-chunk suffices.
 //
 // When a CTA finishes its part of a (sequence, group), it bumps that group's counter in the
-// workspace; the last of the covering CTAs selects the top-k by a 4-pass radix select on
-// order-preserving 32-bit keys (ties to the lower block index) and writes the sorted list.
+// workspace; the last of the covering CTAs selects the top-k (exact; ties to the lower block
+// index, see select_topk) and writes the sorted list.
 // Because ranges are contiguous, that selection overlaps the producer's loads for the next
 // group; only the last group of the last CTA is a tail.
 #include "common.cuh"
@@ -25,12 +27,14 @@
 namespace sparda {
 
 constexpr int kSelConsumerWarps = 8;
+constexpr int kSelGroupWarps = 4;                         // two groups take alternate sub-chunks
 constexpr int kSelConsumers = kSelConsumerWarps * 32;     // 256
+constexpr int kSelGroupThreads = kSelGroupWarps * 32;     // 128
 constexpr int kSelThreads = kSelConsumers + 32;
-constexpr int kSubBlocks = 16;                            // blocks per sub-chunk
-constexpr int kSubWindows = kWinPerBlock * kSubBlocks;    // 64 windows per sub-chunk
-constexpr int kSelStages = 8;
-constexpr int kSelStageBytes = (kSubWindows + 1) * kRowBytes;   // + the left window
+constexpr int kSubBlocks = 31;                            // blocks per sub-chunk
+constexpr int kSubRows = kWinPerBlock * kSubBlocks + 1;   // 125 windows: 4 passes of 32
+constexpr int kSelStages = 6;
+constexpr int kSelStageBytes = kSubRows * kRowBytes;
 constexpr int kMaxBlocksPerSeq = kMaxCtx / kBlock;        // 4096
 constexpr int kKeysPerThread = kMaxBlocksPerSeq / kSelConsumers;  // 16
 constexpr int kSelSmem = 128 /*align slack*/ + 128 /*barriers*/ + kSelStages * kSelStageBytes;
@@ -40,6 +44,10 @@ int select_chunk_blocks(int, int) { return kSubBlocks; }
 
 __device__ __forceinline__ void sel_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kSelConsumers) : "memory");
+}
+
+__device__ __forceinline__ void group_sync(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + grp), "n"(kSelGroupThreads) : "memory");
 }
 
 __device__ __forceinline__ void sel_arrive(uint64_t* bar) {
@@ -69,18 +77,39 @@ __device__ __forceinline__ int sel_scan(int v, int* warp_tot, int* total) {
   return v + before;
 }
 
+constexpr int kMaxList = 512;          // candidates ranked exactly by the fast path
+
 struct TopkShared {
   unsigned hist[256];
   int warp_tot[kSelConsumerWarps];
+  float red_lo[kSelConsumerWarps], red_hi[kSelConsumerWarps];
   uint32_t prefix;
   int krem;
   int last;
+  int bstar;
+  int n_ge;
+  int n_list;
+  float lv[kMaxList];
+  int lj[kMaxList];
+  unsigned char flag[kMaxBlocksPerSeq];
 };
 
+// Bucket of a candidate score in the 256 equal slices of [lo, hi]. Monotone non-decreasing
+// in x (a subtraction and a positive scaling, each rounded), so every candidate in a higher
+// bucket outscores every candidate in a lower one.
+__device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
+  return min(255, max(0, __float2int_rd((x - lo) * scale)));
+}
+
 // Top-k of one (sequence, group) by the 256 consumer threads, from the block scores the
-// covering CTAs stored in the workspace.
+// covering CTAs stored in the workspace. Fast path: min/max of the candidate scores, a
+// 256-bucket histogram over that range, the bucket that holds the k-th score, then exact
+// ranks (score descending, block ascending) among the candidates at or above that bucket --
+// a few dozen for real score distributions. If more than kMaxList candidates share those
+// buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
+// takes over. Either way the result is exact and ties go to the lower block index.
 __device__ void select_topk(const SelectArgs& a, int bg, int T, TopkShared& sh) {
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int kslots = a.topk + 2;
   int32_t* idx = a.idx + (size_t)bg * kslots;
   const bool valid = (T >= 1 && T <= a.max_ctx);
@@ -89,91 +118,147 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T, TopkShared& sh) 
   const int per = (nb + kSelConsumers - 1) / kSelConsumers;
   const int jb = t * per;
   const float* S = a.block_scores + (size_t)bg * a.nb_cap;
-
-  uint32_t key[kKeysPerThread];
-#pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e) {
-    const int j = jb + e;
-    key[e] = (e < per && j >= 1 && j < tb) ? ordered_key(__ldcg(S + j)) : 0u;
-  }
   const int n_cand = max(0, tb - 1);
   const int k_eff = min(a.topk, n_cand);
 
-  // A candidate is kept when key > thr, or key == thr and fewer than take_eq equal keys
-  // sit at lower block indices.
-  uint32_t thr;
-  int take_eq;
-  if (k_eff == n_cand) {
-    thr = 0u;
-    take_eq = 0;
-  } else if (k_eff == 0) {
-    thr = 0xffffffffu;
-    take_eq = 0;
-  } else {
-    uint32_t prefix = 0u, mask = 0u;
-    int krem = k_eff;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      sh.hist[t] = 0u;
-      sel_sync();
-      // Scores cluster in a few exponents, so most keys share a digit in the first passes:
-      // lanes with equal digits add their count with one atomic (warp-aggregated).
-#pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
-        const bool in = key[e] != 0u && (key[e] & mask) == prefix;
-        const unsigned d = in ? (key[e] >> shift) & 255u : 256u;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
-      }
-      sel_sync();
-      const int v = (int)sh.hist[255 - t];      // thread t looks at digit 255 - t
-      int tot;
-      const int incl = sel_scan(v, sh.warp_tot, &tot);
-      const int excl = incl - v;
-      if (excl < krem && incl >= krem) {
-        sh.prefix = prefix | ((uint32_t)(255 - t) << shift);
-        sh.krem = krem - excl;
-      }
-      sel_sync();
-      prefix = sh.prefix;
-      krem = sh.krem;
-      mask |= 255u << shift;
-    }
-    thr = prefix;
-    take_eq = krem;
-  }
-
-  int my_eq = 0;
-#pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e) my_eq += (key[e] != 0u && key[e] == thr);
-  int dummy;
-  int rank = sel_scan(my_eq, sh.warp_tot, &dummy) - my_eq;
-
-  bool sel[kKeysPerThread];
-  int my_sel = 0;
+  float v[kKeysPerThread];
+  bool isc[kKeysPerThread];
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) {
     const int j = jb + e;
-    bool s = false;
-    if (e < per && j < nb) {
-      if (j == 0 || j == tb) {
-        s = true;
-      } else if (key[e] != 0u) {
-        if (key[e] > thr) {
-          s = true;
-        } else if (key[e] == thr) {
-          s = rank < take_eq;
+    isc[e] = e < per && j >= 1 && j < tb;
+    v[e] = isc[e] ? __ldcg(S + j) : 0.f;
+    if (e < per && j < nb) sh.flag[j] = (j == 0 || j == tb) ? 1 : 0;   // the forced blocks
+  }
+
+  if (k_eff == n_cand) {
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e)
+      if (isc[e]) sh.flag[jb + e] = 1;
+  } else if (k_eff > 0) {
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e)
+      if (isc[e]) {
+        lo = fminf(lo, v[e]);
+        hi = fmaxf(hi, v[e]);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+      sh.red_lo[warp] = lo;
+      sh.red_hi[warp] = hi;
+    }
+    sh.hist[t] = 0u;
+    if (t == 0) sh.n_list = 0;
+    sel_sync();
+#pragma unroll
+    for (int w = 0; w < kSelConsumerWarps; ++w) {
+      lo = fminf(lo, sh.red_lo[w]);
+      hi = fmaxf(hi, sh.red_hi[w]);
+    }
+    const float scale = 256.f / (hi - lo);
+    bool fast = hi > lo && isfinite(lo) && isfinite(hi) && isfinite(scale);   // CTA-uniform
+    if (fast) {
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        const unsigned d = isc[e] ? (unsigned)score_bucket(v[e], lo, scale) : 256u;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (isc[e] && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
+      }
+      sel_sync();
+      const int hv = (int)sh.hist[255 - t];      // thread t looks at bucket 255 - t
+      int tot;
+      const int incl = sel_scan(hv, sh.warp_tot, &tot);
+      if (incl - hv < k_eff && incl >= k_eff) {
+        sh.bstar = 255 - t;
+        sh.n_ge = incl;
+      }
+      sel_sync();
+      fast = sh.n_ge <= kMaxList;
+    }
+    if (fast) {
+      const int bstar = sh.bstar;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e)
+        if (isc[e] && score_bucket(v[e], lo, scale) >= bstar) {
+          const int p = atomicAdd(&sh.n_list, 1);
+          sh.lv[p] = v[e];
+          sh.lj[p] = jb + e;
+        }
+      sel_sync();
+      const int c = sh.n_list;
+      for (int i = t; i < c; i += kSelConsumers) {
+        const float vi = sh.lv[i];
+        const int ji = sh.lj[i];
+        int rank = 0;
+        for (int m = 0; m < c; ++m) {
+          const float vm = sh.lv[m];
+          rank += (vm > vi) || (vm == vi && sh.lj[m] < ji);
+        }
+        if (rank < k_eff) sh.flag[ji] = 1;
+      }
+    } else {
+      // radix select on order-preserving keys
+      uint32_t key[kKeysPerThread];
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
+      uint32_t prefix = 0u, mask = 0u;
+      int krem = k_eff;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        sh.hist[t] = 0u;
+        sel_sync();
+#pragma unroll
+        for (int e = 0; e < kKeysPerThread; ++e) {
+          const bool in = key[e] != 0u && (key[e] & mask) == prefix;
+          const unsigned d = in ? (key[e] >> shift) & 255u : 256u;
+          const unsigned peers = __match_any_sync(0xffffffffu, d);
+          if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
+        }
+        sel_sync();
+        const int hv = (int)sh.hist[255 - t];
+        int tot;
+        const int incl = sel_scan(hv, sh.warp_tot, &tot);
+        if (incl - hv < krem && incl >= krem) {
+          sh.prefix = prefix | ((uint32_t)(255 - t) << shift);
+          sh.krem = krem - (incl - hv);
+        }
+        sel_sync();
+        prefix = sh.prefix;
+        krem = sh.krem;
+        mask |= 255u << shift;
+      }
+      int my_eq = 0;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) my_eq += (key[e] != 0u && key[e] == prefix);
+      int dummy;
+      int rank = sel_scan(my_eq, sh.warp_tot, &dummy) - my_eq;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        if (key[e] == 0u) continue;
+        if (key[e] > prefix) {
+          sh.flag[jb + e] = 1;
+        } else if (key[e] == prefix) {
+          if (rank < krem) sh.flag[jb + e] = 1;
           ++rank;
         }
       }
     }
-    sel[e] = s;
-    my_sel += s;
   }
+  sel_sync();
+  // the selected blocks in ascending order
+  int my_sel = 0;
+#pragma unroll
+  for (int e = 0; e < kKeysPerThread; ++e)
+    if (e < per && jb + e < nb) my_sel += sh.flag[jb + e];
   int total;
   int pos = sel_scan(my_sel, sh.warp_tot, &total) - my_sel;
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e)
-    if (sel[e] && pos < kslots) idx[pos++] = jb + e;
+    if (e < per && jb + e < nb && sh.flag[jb + e] && pos < kslots) idx[pos++] = jb + e;
   for (int s = total + t; s < kslots; s += kSelConsumers) idx[s] = -1;
   if (t == 0) a.cnt[bg] = min(total, kslots);
 }
@@ -204,7 +289,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kSelStages;
   uint8_t* ring = smem + 128;
-  __shared__ float s_win[kSubWindows + 1];
+  __shared__ float s_win[2][2][kSubRows + 3];    // [group][buffer][window]
   __shared__ TopkShared sh;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -215,7 +300,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
   if (tid == 0) {
     for (int i = 0; i < kSelStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kSelConsumerWarps);
+      mbar_init(&empty[i], kSelGroupWarps);
     }
     fence_mbar_init();
   }
@@ -234,7 +319,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
       u = seg_end;
       for (int j0 = jseg0; j0 < min(jseg1, gr.nb); j0 += kSubBlocks) {
         const int j1 = min(min(j0 + kSubBlocks, jseg1), gr.nb);
-        const int w0 = (j0 == jseg0) ? max(0, kWinPerBlock * j0 - 1) : kWinPerBlock * j0;
+        const int w0 = max(0, kWinPerBlock * j0 - 1);
         const int w1 = min(gr.W, kWinPerBlock * j1);
         const int stage = it % kSelStages;
         if (it >= kSelStages && !mbar_wait(&empty[stage], ((it / kSelStages) & 1) ^ 1, a.err)) return;
@@ -254,9 +339,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
 
   // ---------------------------------------------------------------- consumers
   const int t = tid;
-  const int c = t & 3;                 // lane within a window: dims 8c + 32k, k = 0..3
-  const int wl = t >> 2;               // window of this thread within a 64-window pass
-  int it = 0;
+  const int grp = warp / kSelGroupWarps;          // takes sub-chunks it % 2 == grp
+  const int gt = t % kSelGroupThreads;            // thread within the group
+  const int c = gt & 3;                           // lane within a window: dims 8c + 32k
+  const int wl = gt >> 2;                         // window of this thread within a pass
+  int it = 0, nbuf = 0;
   bool ok = true;                      // false after a wait ran out: skip compute, keep pace
   for (long long u = J0; u < J1;) {
     const int bg = (int)(u / a.nb_cap);
@@ -282,58 +369,61 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
       }
     }
     float* S = a.block_scores + (size_t)bg * a.nb_cap;
-    float carry = -INFINITY;              // score of the window left of the sub-chunk
-    for (int j0 = jseg0; j0 < min(jseg1, gr.nb); j0 += kSubBlocks) {
+    for (int j0 = jseg0; j0 < min(jseg1, gr.nb); j0 += kSubBlocks, ++it) {
+      if ((it & 1) != grp) continue;
       const int j1 = min(min(j0 + kSubBlocks, jseg1), gr.nb);
-      const int w0 = (j0 == jseg0) ? max(0, kWinPerBlock * j0 - 1) : kWinPerBlock * j0;
+      const int w0 = max(0, kWinPerBlock * j0 - 1);      // tile row 0
       const int w1 = min(gr.W, kWinPerBlock * j1);
       const int nw = max(0, w1 - w0);
       const int stage = it % kSelStages;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kSelStages) & 1, a.err));
-      ++it;
       const uint8_t* tile = ring + stage * kSelStageBytes;
-      for (int base = 0; base < nw; base += kSubWindows) {
+      float* sw = s_win[grp][nbuf & 1];
+      for (int base = 0; base < kSubRows; base += kSelGroupThreads / 4) {
         const int i = base + wl;
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         if (ok && i < nw) {
           const uint8_t* row = tile + (size_t)i * kRowBytes + 16 * c;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(row);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(row + 64);
+          const uint4 x2 = *reinterpret_cast<const uint4*>(row + 128);
+          const uint4 x3 = *reinterpret_cast<const uint4*>(row + 192);
+          const uint32_t w0v[4] = {x0.x, x0.y, x0.z, x0.w}, w1v[4] = {x1.x, x1.y, x1.z, x1.w};
+          const uint32_t w2v[4] = {x2.x, x2.y, x2.z, x2.w}, w3v[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 x = *reinterpret_cast<const uint4*>(row + 64 * k);
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc = fmaf(fr[8 * k + 2 * e], bf16_lo(w[e]), acc);
-              acc = fmaf(fr[8 * k + 2 * e + 1], bf16_hi(w[e]), acc);
-            }
+          for (int e = 0; e < 4; ++e) {
+            a0 = fmaf(fr[2 * e], bf16_lo(w0v[e]), a0);
+            a0 = fmaf(fr[2 * e + 1], bf16_hi(w0v[e]), a0);
+            a1 = fmaf(fr[8 + 2 * e], bf16_lo(w1v[e]), a1);
+            a1 = fmaf(fr[8 + 2 * e + 1], bf16_hi(w1v[e]), a1);
+            a2 = fmaf(fr[16 + 2 * e], bf16_lo(w2v[e]), a2);
+            a2 = fmaf(fr[16 + 2 * e + 1], bf16_hi(w2v[e]), a2);
+            a3 = fmaf(fr[24 + 2 * e], bf16_lo(w3v[e]), a3);
+            a3 = fmaf(fr[24 + 2 * e + 1], bf16_hi(w3v[e]), a3);
           }
         }
+        float acc = (a0 + a1) + (a2 + a3);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        if (c == 0 && i < nw) s_win[i] = acc;
+        if (c == 0 && i < kSubRows) sw[i] = acc;
       }
       __syncwarp();
-      if (lane == 0) sel_arrive(&empty[stage]);
-      sel_sync();                                   // s_win complete
-      if (t < j1 - j0) {                            // block j uses windows 4j-1 .. 4j+3 below W
-        const int j = j0 + t;
+      if ((t & 31) == 0) sel_arrive(&empty[stage]);
+      group_sync(grp);                              // this sub-chunk's window scores complete
+      if (gt < j1 - j0) {                           // block j uses windows 4j-1 .. 4j+3 below W
+        const int j = j0 + gt;
         float m = -INFINITY;
         if (ok) {
 #pragma unroll
           for (int d = -1; d <= 3; ++d) {
             const int w = kWinPerBlock * j + d;
-            if (w < 0 || w >= gr.W) continue;
-            const int li = w - w0;
-            m = fmaxf(m, li < 0 ? carry : s_win[li]);
+            if (w >= 0 && w < gr.W) m = fmaxf(m, sw[w - w0]);
           }
         }
         S[j] = m;
       }
-      const float next_carry = (nw > 0) ? s_win[nw - 1] : -INFINITY;
-      sel_sync();                                   // s_win free again
-      carry = next_carry;
+      ++nbuf;                                       // alternate buffers: no second barrier
     }
-
     // this CTA's part of the group is done: count it; the last covering CTA selects
     const long long first_u = (long long)bg * a.nb_cap, last_u = first_u + a.nb_cap - 1;
     const int n_cover = sel_cta_of_unit(last_u, grid, U) - sel_cta_of_unit(first_u, grid, U) + 1;
