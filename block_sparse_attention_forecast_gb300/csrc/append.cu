@@ -27,6 +27,7 @@ __device__ __forceinline__ uint32_t load_key2(const __nv_bfloat16* k, const __nv
 
 // One CTA per (sequence, group), 64 threads, thread t owns dims 2t and 2t+1.
 __global__ void __launch_bounds__(64) append_kv_kernel(AppendArgs a) {
+  grid_dep_launch();                   // the attention may start its prologue
   const int bg = blockIdx.x;
   const int b = bg / a.G;
   const int t = threadIdx.x;

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
       }
     }
     int it = 0;
+    bool waited = false;
     for (int base = u0; base < u1; base += 32) {
       // lane i prepares unit base + i
       const int u = base + lane;
@@ -139,6 +140,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
         }
       }
       unsigned vmask = __ballot_sync(0xffffffffu, v);
+      // the caches were written by the kernel before this one in the stream (the append)
+      if (!waited) {
+        grid_dep_wait();
+        waited = true;
+      }
       while (vmask) {
         const int i = __ffs(vmask) - 1;
         vmask &= vmask - 1;
@@ -432,7 +438,19 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   AttnArgs b = a;
   b.n_units = bg_count * a.kslots;
   const int grid = b.n_units < sm_count() ? b.n_units : sm_count();
-  sparse_attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(b, mk, mv, hk, hv);
+  // Programmatic serialization: barrier set-up and the unit metadata overlap the append
+  // before it in the stream; the producer waits for it before the first TMA load.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, sparse_attn_kernel, b, mk, mv, hk, hv);
 }
 
 }  // namespace sparda

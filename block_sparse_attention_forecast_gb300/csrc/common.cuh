@@ -24,9 +24,11 @@ constexpr int kRowBytes = kHeadDim * 2;             // one bf16 key/value row: 2
 constexpr int kBlockBytes = kBlock * kRowBytes;     // one 64-token K (or V) block: 16 KiB
 constexpr int kHotSlots = 3;
 
-// Poll limit of every wait on an mbarrier. try_wait suspends the thread for a
-// hardware-chosen time between polls, so this bounds a wait to well under a few seconds.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Every wait on an mbarrier polls with try_wait and a suspend-time hint: a waiting thread
+// sleeps (issuing nothing) until the phase completes or the hint elapses. At most kWaitPolls
+// polls of at most kWaitHintNs each bound a wait to about 2.6 s.
+constexpr uint32_t kWaitHintNs = 10000;
+constexpr uint32_t kWaitPolls = 1u << 18;
 
 __host__ __device__ constexpr int num_windows(int n_tokens) {
   return n_tokens < kWinKernel ? 0 : (n_tokens - kWinKernel) / kWinStride + 1;
@@ -61,10 +63,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
       : "memory");
   return done != 0;
 }
@@ -154,6 +156,13 @@ __device__ __forceinline__ uint32_t ordered_key(float x) {
   uint32_t u = __float_as_uint(x);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the previous kernel in its stream still runs; grid_dep_wait() blocks
+// until that kernel has completed and its writes are visible. grid_dep_launch() lets the
+// next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Hot slot of block j (>= 0) of an offloaded layer.
 __device__ __forceinline__ int hot_slot(int j) { return j == 0 ? 0 : 1 + (j & 1); }

@@ -32,6 +32,7 @@ __global__ void __cluster_dims__(1, kProjSplit, 1) __launch_bounds__(kProjWarps 
   __shared__ float red[kProjWarps][16][8];
   __shared__ float part[16][8];
   cg::cluster_group cluster = cg::this_cluster();
+  grid_dep_launch();                   // the selector may start streaming compressed keys
   const int n0 = blockIdx.x * 8;
   const int split = blockIdx.y;
   const int m0 = blockIdx.z * 16;

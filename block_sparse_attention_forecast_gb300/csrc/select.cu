@@ -165,6 +165,7 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T, TopkShared& sh) 
     if (fast) {
 #pragma unroll
       for (int e = 0; e < kKeysPerThread; ++e) {
+        if (e >= per) break;                       // per is the same in every thread
         const unsigned d = isc[e] ? (unsigned)score_bucket(v[e], lo, scale) : 256u;
         const unsigned peers = __match_any_sync(0xffffffffu, d);
         if (isc[e] && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
@@ -183,23 +184,39 @@ __device__ void select_topk(const SelectArgs& a, int bg, int T, TopkShared& sh) 
     if (fast) {
       const int bstar = sh.bstar;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e)
-        if (isc[e] && score_bucket(v[e], lo, scale) >= bstar) {
-          const int p = atomicAdd(&sh.n_list, 1);
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        if (e >= per) break;                       // per is the same in every thread
+        const bool in = isc[e] && score_bucket(v[e], lo, scale) >= bstar;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&sh.n_list, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (in) {
+          const int p = base + __popc(bal & ((1u << lane) - 1u));
           sh.lv[p] = v[e];
           sh.lj[p] = jb + e;
         }
+      }
       sel_sync();
+      // exact rank of each listed candidate (score descending, block ascending): `split`
+      // threads share one candidate, each scanning a slice of the list
       const int c = sh.n_list;
-      for (int i = t; i < c; i += kSelConsumers) {
-        const float vi = sh.lv[i];
-        const int ji = sh.lj[i];
+      const int split = c <= 32 ? 8 : (c <= 64 ? 4 : (c <= 128 ? 2 : 1));
+      for (int i0 = 0; i0 < c * split; i0 += kSelConsumers) {
+        const int q = i0 + t;
+        const int i = q / split, part = q % split;
         int rank = 0;
-        for (int m = 0; m < c; ++m) {
-          const float vm = sh.lv[m];
-          rank += (vm > vi) || (vm == vi && sh.lj[m] < ji);
+        int ji = 0;
+        if (i < c) {
+          const float vi = sh.lv[i];
+          ji = sh.lj[i];
+          for (int m = part; m < c; m += split) {
+            const float vm = sh.lv[m];
+            rank += (vm > vi) || (vm == vi && sh.lj[m] < ji);
+          }
         }
-        if (rank < k_eff) sh.flag[ji] = 1;
+        for (int o = 1; o < split; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (i < c && part == 0 && rank < k_eff) sh.flag[ji] = 1;
       }
     } else {
       // radix select on order-preserving keys
@@ -344,6 +361,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
   const int c = gt & 3;                           // lane within a window: dims 8c + 32k
   const int wl = gt >> 2;                         // window of this thread within a pass
   int it = 0, nbuf = 0;
+  bool first_seg = true;
   bool ok = true;                      // false after a wait ran out: skip compute, keep pace
   for (long long u = J0; u < J1;) {
     const int bg = (int)(u / a.nb_cap);
@@ -353,7 +371,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
     const int jseg0 = (int)(u - (long long)bg * a.nb_cap);
     const int jseg1 = (int)(seg_end - (long long)bg * a.nb_cap);
     u = seg_end;
-    // forecast slice of this thread
+    // forecast slice of this thread (written by the kernel before this one in the stream)
+    if (first_seg) {
+      grid_dep_wait();
+      first_seg = false;
+    }
     float fr[32];
     {
       const uint4* fp = reinterpret_cast<const uint4*>(a.f + (size_t)bg * kHeadDim);
@@ -460,7 +482,19 @@ void launch_forecast_select(const SelectArgs& a, int bg_count, cudaStream_t s) {
   b.n_units = bg_count * a.nb_cap;
   const int by_work = (b.n_units + kSubBlocks - 1) / kSubBlocks;   // >= one sub-chunk each
   const int grid = by_work < sel_sm_count() ? by_work : sel_sm_count();
-  forecast_select_kernel<<<grid, kSelThreads, kSelSmem, s>>>(b);
+  // Programmatic serialization: the producer starts streaming compressed keys while the
+  // projection that writes the forecast still runs; consumers wait for it (grid_dep_wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = kSelSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, forecast_select_kernel, b);
 }
 
 }  // namespace sparda
