@@ -21,9 +21,9 @@ __all__ = [
     "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes", "sparda_device_error",
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
-    "sparda_prefetch_blocks", "sparda_multihead_select",
+    "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
-    "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
+    "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
 ]
 
@@ -38,6 +38,7 @@ ERR_MISALIGNED = -3
 ERR_NOT_MAPPED_HOST = -4
 ERR_WORKSPACE_TOO_SMALL = -5
 ERR_CUDA = -6
+ERR_STATIC_SCRATCH_LIMIT = -7
 
 DEV_WAIT_TIMEOUT = 1
 DEV_BAD_SEQ_LEN = 2
@@ -92,6 +93,7 @@ def _load():
         "sparda_sparse_decode_attn": (I32, [SH, LY, P, P, P, P, P, P, I32, P, P, SZ, P]),
         "sparda_prefetch_blocks": (I32, [SH, LY, P, P, P, I32, P, P, I32, P]),
         "sparda_multihead_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
+        "sparda_forecast_select_static": (I32, [SH, P, P, P, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -275,3 +277,11 @@ def sparda_multihead_select(shape, ck, q, seq_len, batch, idx, cnt, ws, stream=N
     _check("sparda_multihead_select", lib.sparda_multihead_select(
         ctypes.byref(shape.c()), _ptr(ck), _ptr(q), _ptr(seq_len), int(batch), _ptr(idx),
         _ptr(cnt), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def sparda_forecast_select_static(shape, ck, forecast, seq_len, batch, idx, cnt, stream=None):
+    """sparda_forecast_select without a workspace: for callers that may not allocate device
+    memory. Its scratch is a fixed array inside the library (see include/sparda.h)."""
+    _check("sparda_forecast_select_static", lib.sparda_forecast_select_static(
+        ctypes.byref(shape.c()), _ptr(ck), _ptr(forecast), _ptr(seq_len), int(batch), _ptr(idx),
+        _ptr(cnt), _stream(stream)))

@@ -149,6 +149,8 @@ int32_t layer_status(const sparda_layer_kv* L, bool need_kv) {
 
 }  // namespace
 
+int* sparda::dev_error_word() { return dev_error_ptr(); }
+
 extern "C" {
 
 int32_t sparda_abi_version(void) { return 1; }
@@ -162,6 +164,8 @@ const char* sparda_status_string(int32_t status) {
     case SPARDA_ERR_NOT_MAPPED_HOST: return "host memory not pinned and mapped for the device";
     case SPARDA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case SPARDA_ERR_CUDA: return "CUDA error";
+    case SPARDA_ERR_STATIC_SCRATCH_LIMIT:
+      return "request exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }

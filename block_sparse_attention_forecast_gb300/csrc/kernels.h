@@ -88,6 +88,9 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
                         cudaStream_t s);
 void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s);
 
+// Device address of the library's device error word on the current device (api.cu).
+int* dev_error_word();
+
 // Sizes the C ABI needs to lay out workspaces.
 int select_chunk_blocks(int nb_cap, int bg_count);
 int attn_blocks_per_cta();

@@ -59,6 +59,7 @@ extern "C" {
 #define SPARDA_ERR_NOT_MAPPED_HOST      -4  /* host KV not reachable by the device (UVA)   */
 #define SPARDA_ERR_WORKSPACE_TOO_SMALL  -5
 #define SPARDA_ERR_CUDA                 -6  /* a CUDA runtime/driver call failed           */
+#define SPARDA_ERR_STATIC_SCRATCH_LIMIT -7  /* beyond the allocation-free entry's scratch  */
 
 /* bits of the device error word (sparda_device_error) */
 #define SPARDA_DEV_WAIT_TIMEOUT   1   /* a bounded wait on a copy's completion ran out      */
@@ -242,6 +243,31 @@ int32_t sparda_multihead_select(const sparda_shape* shape, const void* ck, const
                                 const int32_t* seq_len, int32_t batch, int32_t* idx,
                                 int32_t* cnt, void* workspace, size_t workspace_bytes,
                                 void* stream);
+
+/*
+ * sparda_forecast_select_static -- sparda_forecast_select without a workspace argument, for
+ * callers that cannot allocate device memory: a plugin that its host engine hands only the
+ * input and output tensors, or a serving loop that must not allocate once it runs. The
+ * pages have no counterpart; this is a convenience of this library.
+ *
+ * Same inputs, outputs and results as sparda_forecast_select. Its scratch (per-group
+ * counters and block scores) is a fixed array of SPARDA_STATIC_SCRATCH_BYTES in the
+ * library's own device memory, which every device that loads the library holds until the
+ * process exits. It serves batch * n_groups <= SPARDA_STATIC_MAX_GROUPS and
+ * 4 * SPARDA_STATIC_MAX_GROUPS + 4 * batch * n_groups * (max_ctx / 64) <=
+ * SPARDA_STATIC_SCRATCH_BYTES (for example batch 64, 2 groups, max_ctx 131072); larger
+ * requests return SPARDA_ERR_STATIC_SCRATCH_LIMIT without launching anything.
+ * The first call on a device looks up the array's device address (make that first call
+ * before any stream capture). Each call clears the counters with an asynchronous memset on
+ * `stream` and allocates nothing. All calls share the one array, which keeps the last
+ * call's contents: calls that may overlap on the GPU (other streams, other threads) race
+ * and must be serialized by the caller.
+ */
+#define SPARDA_STATIC_SCRATCH_BYTES (4 << 20)
+#define SPARDA_STATIC_MAX_GROUPS 4096
+int32_t sparda_forecast_select_static(const sparda_shape* shape, const void* ck,
+                                      const void* forecast, const int32_t* seq_len,
+                                      int32_t batch, int32_t* idx, int32_t* cnt, void* stream);
 
 #ifdef __cplusplus
 }
