@@ -17,6 +17,7 @@ import torch
 
 __all__ = [
     "lib", "LIB_PATH", "HEADER_PATH", "SpardaError", "Shape", "LayerKV", "workspace",
+    "hot_slot", "fill_hot_from_host",
     "header_functions", "status_string", "num_windows", "c_shape", "c_layer_kv",
     "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes", "sparda_device_error",
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
@@ -201,6 +202,25 @@ class LayerKV:
             hk = hv = None
         ck = torch.zeros((shape.max_batch, G, shape.w_cap, d), dtype=torch.bfloat16, device=device)
         return LayerKV(k, v, ck, hk, hv, on_host)
+
+
+def hot_slot(j):
+    """Hot-ring slot of block j of an offloaded layer (include/sparda.h, sparda_layer_kv)."""
+    return 0 if j == 0 else 1 + (j & 1)
+
+
+def fill_hot_from_host(layer, n_cached):
+    """Set-up after a prefill of an offloaded layer: copy block 0 and the two newest blocks of
+    every sequence from the host cache into the hot ring. n_cached[b] = tokens cached so far.
+    Plain device copies; not part of the decode step."""
+    for b, n in enumerate(n_cached):
+        if n < 1:
+            continue
+        tb = (n - 1) // BLOCK
+        for j in sorted({0, tb, max(tb - 1, 0)}):
+            rows = slice(j * BLOCK, (j + 1) * BLOCK)
+            layer.hot_k[b, :, hot_slot(j)].copy_(layer.k[b, :, rows], non_blocking=False)
+            layer.hot_v[b, :, hot_slot(j)].copy_(layer.v[b, :, rows], non_blocking=False)
 
 
 def workspace(shape, batch, kind, device="cuda"):

@@ -122,6 +122,8 @@ int32_t host_mapped_status(const void* p) {
     return SPARDA_ERR_NOT_MAPPED_HOST;
   }
   if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return SPARDA_ERR_NOT_MAPPED_HOST;
+  // the kernels dereference the pointer as given: it must be the memory's device address
+  if (attr.devicePointer != p) return SPARDA_ERR_NOT_MAPPED_HOST;
   return SPARDA_OK;
 }
 

@@ -21,7 +21,7 @@ def sb(cuda_ok):
     return b
 
 
-def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted):
+def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, offload=(), overlap=True):
     """Seeded caches holding tokens 0..T-2, the step's inputs, and forecast heads; planted
     blocks of each layer are shifted along the forecast (computed by the oracle) that selects
     that layer's blocks."""
@@ -44,14 +44,20 @@ def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted):
             f = O.forecast_project(to64(Wsel), to64(hsel[b])).reshape(G, d)
             for g in range(G):
                 synth.plant(K[b, g], synth.planted_blocks(seed, nb, n_planted, L, b, g), f[g])
-        layer = sb.LayerKV.empty(shape)
-        layer.k.copy_(K.cuda())
-        layer.v.copy_(V.cuda())
+        if L in offload:
+            layer = sb.LayerKV.empty(shape, on_host=True)
+            layer.k.copy_(K)
+            layer.v.copy_(V)
+            sb.fill_hot_from_host(layer, [T - 1] * B)
+        else:
+            layer = sb.LayerKV.empty(shape)
+            layer.k.copy_(K.cuda())
+            layer.v.copy_(V.cuda())
         sb.sparda_compress_keys(shape, layer, torch.full((B,), T - 1, dtype=torch.int32, device="cuda"), B)
         Ks.append(K)
         Vs.append(V)
         layers.append(layer)
-    stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B)
+    stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B, overlap=overlap)
     stack.h.copy_(h.cuda())
     stack.q.copy_(q.cuda())
     stack.k_new.copy_(kn.cuda())
@@ -110,6 +116,28 @@ def test_stack_step_eager_and_graph(sb, n_layers, B, T, topk, max_ctx, hidden):
     # the same step replayed from a CUDA graph: the step rewrites token T-1, so the result
     # is identical
     stack.out.zero_()
+    stack.capture()
+    stack.out.zero_()
+    stack.run()
+    torch.cuda.synchronize()
+    assert torch.equal(stack.idx, eager_idx)
+    assert torch.equal(stack.out, eager_out)
+    assert sb.sparda_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_offloaded_stack_step(sb, overlap):
+    # layer 0 resident, layers 1..3 offloaded to pinned host memory; the gather of layer L+1
+    # runs on its own stream, overlapped with layer L (or waited on at once)
+    n_layers, B, T, topk, max_ctx, hidden = 4, 2, 2500, 8, 4096, 256
+    shape, stack, inputs = make_stack_case(sb, 9, n_layers, B, T, topk, max_ctx, hidden, 8,
+                                           offload={1, 2, 3}, overlap=overlap)
+    sel, out, S = oracle_step(inputs, n_layers, B, T, topk)
+    stack.enqueue()
+    torch.cuda.synchronize()
+    same = compare(stack, sel, out, S, n_layers, B, T, topk)
+    assert same >= n_layers * B * 2 * 3 // 4
+    eager_out, eager_idx = stack.out.clone(), stack.idx.clone()
     stack.capture()
     stack.out.zero_()
     stack.run()
