@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
+    p.add_argument("--offload-steps", type=int, default=20)
     return p.parse_args()
 
 
@@ -208,6 +210,165 @@ def attn_bytes():
     return BATCH * G * ((TOPK + 2) * 64 * D * 2 * 2 + 2 * H * D * 2)
 
 
+# ---------------------------------------------------------------------- offloaded decode
+OFF_BATCH, OFF_DISTINCT, OFF_FFN = 64, 4, 14336
+
+
+def graph_time(fn, reps=1):
+    """Device time of `reps` captured repetitions of fn(stream), per repetition (seconds)."""
+    import torch
+    s = torch.cuda.current_stream()
+    fn(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for _ in range(reps):
+            fn(cs)
+    g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / reps
+
+
+def run_offload(device, seed, steps, warmup):
+    """BASELINE config 4: batch 64, context 131072, 32 layers; layer 0 resident, layers 1-31
+    with their K/V in pinned host memory (gathered over the host link by the persistent UVA
+    kernel on a side stream), compressed keys and hot blocks in HBM, and a stand-in bf16 FFN
+    GEMM [64 x 4096] x [4096 x 14336] after every attention. The host holds 4 distinct K/V
+    pairs (8 GiB each) shared round-robin by layers 1-31: the GPU machine has about 200 GB of RAM,
+    and aliasing leaves the bytes gathered per step unchanged. Measured with the gather
+    overlapped, with it waited on right after selection, and against the same step with
+    every layer resident (4 distinct resident K/V pairs, same aliasing)."""
+    import gc
+    import torch
+    import synth
+    import block_sparse_attention_forecast_gb300.binding as sb
+    from block_sparse_attention_forecast_gb300.step import DecodeStack
+    B = OFF_BATCH
+    shape = sb.Shape(n_groups=G, topk=TOPK, max_ctx=CTX, max_batch=B)
+    steps_total = 1 + warmup + steps
+    T0 = CTX - steps_total + 1
+    seq_c = torch.full((B,), T0 - 1, dtype=torch.int32, device=device)
+    devK, devV, hostK, hostV, cks = [], [], [], [], []
+    for i in range(OFF_DISTINCT):
+        kd = synth.normal_bf16_device((B, G, CTX, D), seed * 1000 + 500 + i, device)
+        vd = synth.normal_bf16_device((B, G, CTX, D), seed * 1000 + 600 + i, device)
+        ck = torch.zeros((B, G, shape.w_cap, D), dtype=torch.bfloat16, device=device)
+        sb.sparda_compress_keys(shape, sb.LayerKV(kd, vd, ck), seq_c, B)
+        hk = torch.empty(kd.shape, dtype=torch.bfloat16, pin_memory=True)
+        hv = torch.empty(vd.shape, dtype=torch.bfloat16, pin_memory=True)
+        hk.copy_(kd)
+        hv.copy_(vd)
+        devK.append(kd); devV.append(vd); hostK.append(hk); hostV.append(hv); cks.append(ck)
+    layers = [sb.LayerKV(devK[0], devV[0], cks[0].clone())]
+    for L in range(1, N_LAYERS):
+        i = (L - 1) % OFF_DISTINCT
+        layer = sb.LayerKV(hostK[i], hostV[i], cks[i].clone(),
+                           torch.zeros((B, G, 3, 64, D), dtype=torch.bfloat16, device=device),
+                           torch.zeros((B, G, 3, 64, D), dtype=torch.bfloat16, device=device), True)
+        sb.fill_hot_from_host(layer, [T0 - 1] * B)
+        layers.append(layer)
+    resident = [layers[0]] + [sb.LayerKV(devK[(L - 1) % OFF_DISTINCT], devV[(L - 1) % OFF_DISTINCT], layers[L].ck)
+                              for L in range(1, N_LAYERS)]
+    W_self0 = synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 701, device, std=0.02)
+    W_next = [synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 702 + L, device, std=0.02)
+              for L in range(N_LAYERS - 1)]
+    Wffn = [synth.normal_bf16_device((HIDDEN, OFF_FFN), seed * 1000 + 800 + i, device, std=0.02)
+            for i in range(OFF_DISTINCT)]
+    x = synth.normal_bf16_device((B, HIDDEN), seed * 1000 + 810, device)
+    y = torch.empty((B, OFF_FFN), dtype=torch.bfloat16, device=device)
+
+    def ffn(L):
+        torch.mm(x, Wffn[L % OFF_DISTINCT], out=y)
+
+    def make(lays, overlap):
+        st = DecodeStack(shape, lays, W_self0, W_next, B, device=device, overlap=overlap, advance=True,
+                         after_attention=ffn)
+        st.h.copy_(synth.normal_bf16_device(st.h.shape, seed * 1000 + 820, device))
+        st.q.copy_(synth.normal_bf16_device(st.q.shape, seed * 1000 + 821, device))
+        st.k_new.copy_(synth.normal_bf16_device(st.k_new.shape, seed * 1000 + 822, device))
+        st.v_new.copy_(synth.normal_bf16_device(st.v_new.shape, seed * 1000 + 823, device))
+        return st
+
+    def time_stack(st):
+        st.seq_len.fill_(T0)
+        st.capture()
+        for _ in range(warmup):
+            st.run()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            st.run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / steps
+
+    res = {}
+    st_ov = make(layers, True)
+    t_ov = time_stack(st_ov)
+    st_pg = make(layers, True)
+    st_pg.gather_ctas = 32                  # the pages' H100 setting for batch >= 32, for context
+    t_pages = time_stack(st_pg)
+    del st_pg
+    t_no = time_stack(make(layers, False))
+    t_res = time_stack(make(resident, True))
+    # the gather alone: the step's own 31 gathers (last step's selections), per launch
+    gbytes = B * G * TOPK * 2 * 64 * D * 2
+
+    def gathers(n_ctas):
+        def fn(s):
+            for L in range(1, N_LAYERS):
+                sb.sparda_prefetch_blocks(shape, st_ov.layers[L], st_ov.idx[L], st_ov.cnt[L], st_ov.seq_len, B,
+                                          st_ov.stage_k[L % 2], st_ov.stage_v[L % 2], n_ctas, stream=s)
+        return graph_time(fn) / (N_LAYERS - 1)
+    st_ov.seq_len.fill_(CTX)
+    sweep = {}
+    for n in (8, 16, 32, 64, 152):
+        sweep[str(n)] = gbytes / gathers(n) / 1e9
+    t_g = gathers(0)
+    # host link: one pinned 1 GiB host-to-device copy
+    hb = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    db.copy_(hb)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    db.copy_(hb, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d = (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    link = max([h2d] + list(sweep.values()))
+    res.update({
+        "workload": "32-layer decode step, batch 64, context 131072, layers 1-31 K/V in pinned host memory, "
+                    "stand-in FFN GEMM 64x4096x14336 per layer",
+        "tok_s_overlap": B / t_ov, "tok_s_no_overlap": B / t_no, "tok_s_resident_same_shapes": B / t_res,
+        "ms_per_step_overlap": t_ov * 1e3, "ms_per_step_no_overlap": t_no * 1e3,
+        "ms_per_step_resident": t_res * 1e3, "offload_vs_resident_time": t_ov / t_res,
+        "tok_s_overlap_32_copy_ctas": B / t_pages,
+        "gather_us_per_layer": t_g * 1e6, "gather_bytes_per_layer": gbytes,
+        "gather_gbs": gbytes / t_g / 1e9, "gather_cta_default": sb.sparda_prefetch_default_ctas(B),
+        "gather_cta_sweep_gbs": sweep, "link_h2d_copy_gbs": h2d,
+        "gather_link_frac": (gbytes / t_g / 1e9) / link,
+        "gather_gbs_while_overlapping": (N_LAYERS - 1) * gbytes / t_ov / 1e9,
+        "gather_link_frac_while_overlapping": (N_LAYERS - 1) * gbytes / t_ov / 1e9 / link,
+        "link_peak_gbs": link,
+        "host_buffers": "4 distinct 8 GiB K/V pairs aliased over layers 1-31 (bytes gathered per step unchanged)",
+        "device_error_flags": sb.sparda_device_error(clear=True),
+    })
+    del st_ov, layers, resident, devK, devV, hostK, hostV, cks, hb, db
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------- CPU oracle sample
 CPU_SAMPLE_SCRIPT = r"""
 import sys, time, json
@@ -341,6 +502,14 @@ def run_ours(args):
     stack.seq_len.fill_(CTX)                 # the kernels below run at context CTX
     kt = kernel_times(stack)
     dev_err |= sb.sparda_device_error(clear=True)
+    launches_per_step = stack.kernel_launches_per_step()
+    offload = None
+    if world == 1 and not args.no_offload:
+        import gc
+        del stack
+        gc.collect()
+        torch.cuda.empty_cache()
+        offload = run_offload(device, args.seed, args.offload_steps, 3)
     if dist:
         tt = torch.tensor([elapsed, e2e_elapsed], device=device, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -377,10 +546,12 @@ def run_ours(args):
         },
         "e2e": {"value": world * BATCH * e2e_steps / e2e_elapsed, "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * stack.kernel_launches_per_step(),
+        "gpu_launches": args.steps * launches_per_step,
         "device_error_flags": dev_err,
         "clocks": clk,
     }
+    if offload is not None:
+        line["offload"] = offload
     if cpu is not None:
         per_step, cores, desc = cpu
         line["cpu_baseline"] = {"value": BATCH / per_step, "unit": "tok/s", "cores": cores, "kind": "oracle",

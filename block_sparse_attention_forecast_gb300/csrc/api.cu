@@ -193,7 +193,7 @@ int32_t sparda_device_error(int32_t* flags, int32_t clear) {
   return SPARDA_OK;
 }
 
-int32_t sparda_prefetch_default_ctas(int32_t batch) { return batch < 32 ? 16 : 32; }
+int32_t sparda_prefetch_default_ctas(int32_t batch) { return batch < 32 ? 64 : 152; }
 
 int32_t sparda_append_kv(const sparda_shape* s, const sparda_layer_kv* L, const void* k_new,
                          const void* v_new, const int32_t* seq_len, int32_t batch, void* stream) {

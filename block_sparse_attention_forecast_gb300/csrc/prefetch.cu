@@ -5,17 +5,23 @@
 //
 // A fixed grid of n_ctas CTAs walks the (sequence, group, slot) items with a grid stride.
 // Each item is one selected block that lives only in host memory: its 16 KiB of K and
-// 16 KiB of V are read over the host link with 16-byte non-caching loads (four in flight
-// per thread) and written to the item's staging slot in device memory. Block 0 and the
-// tail block are skipped: the attention reads them from the hot buffers.
+// 16 KiB of V are read over the host link with 16-byte non-caching loads and written to the
+// item's staging slot in device memory. Block 0 and the tail block are skipped: the
+// attention reads them from the hot buffers.
+//
+// A copy CTA is small -- 128 threads and no shared memory, each keeping sixteen 16-byte
+// loads (32 KiB per CTA) in flight -- so that it fits on an SM beside one CTA of the persistent
+// select or attention kernels, which run while the gather streams; a larger copy CTA would
+// keep those kernels' CTAs off its SM for the whole gather.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sparda {
 
-constexpr int kGatherThreads = 512;
-constexpr int kVecPerBlock = kBlockBytes / 16;           // 1024 16-byte vectors
-constexpr int kVecPerThread = kVecPerBlock / kGatherThreads;   // 2
+constexpr int kGatherThreads = 128;
+constexpr int kVecPerBlock = kBlockBytes / 16;                 // 1024 16-byte vectors
+constexpr int kInFlight = 8;                                   // per tensor (K and V) per pass
+constexpr int kPasses = kVecPerBlock / (kGatherThreads * kInFlight);   // 2
 
 __device__ __forceinline__ uint4 ld_host(const uint4* p) {
   uint4 r;
@@ -50,16 +56,20 @@ __global__ void __launch_bounds__(kGatherThreads) prefetch_kernel(const Prefetch
     const uint4* sv = reinterpret_cast<const uint4*>(a.hv + src);
     uint4* dk = reinterpret_cast<uint4*>(a.sk + dst);
     uint4* dv = reinterpret_cast<uint4*>(a.sv + dst);
-    uint4 rk[kVecPerThread], rv[kVecPerThread];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      rk[u] = ld_host(sk + t + u * kGatherThreads);
-      rv[u] = ld_host(sv + t + u * kGatherThreads);
-    }
+    for (int pass = 0; pass < kPasses; ++pass) {
+      const int base = pass * kGatherThreads * kInFlight + t;
+      uint4 rk[kInFlight], rv[kInFlight];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      dk[t + u * kGatherThreads] = rk[u];
-      dv[t + u * kGatherThreads] = rv[u];
+      for (int u = 0; u < kInFlight; ++u) {
+        rk[u] = ld_host(sk + base + u * kGatherThreads);
+        rv[u] = ld_host(sv + base + u * kGatherThreads);
+      }
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) {
+        dk[base + u * kGatherThreads] = rk[u];
+        dv[base + u * kGatherThreads] = rv[u];
+      }
     }
   }
 }

@@ -34,7 +34,7 @@ class DecodeStack:
     """
 
     def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
-                 overlap=True, advance=False):
+                 overlap=True, advance=False, after_attention=None):
         self.shape = shape
         self.layers = layers
         self.n_layers = len(layers)
@@ -45,6 +45,9 @@ class DecodeStack:
         self.gather_ctas = gather_ctas
         self.overlap = overlap
         self.advance = advance          # move every sequence one token on after each step
+        # optional callable(L) enqueued on the main stream after layer L's attention (for
+        # example the rest of the layer: output projection and FFN)
+        self.after_attention = after_attention
         assert not layers[0].on_host, "layer 0 stays resident"
         G, H, d = shape.n_groups, shape.heads_per_group, shape.head_dim
         hidden = W_self0.shape[1]
@@ -67,7 +70,9 @@ class DecodeStack:
             self.stage_k = [torch.zeros(st, **bf) for _ in range(2)]
             self.stage_v = [torch.zeros(st, **bf) for _ in range(2)]
         self.side = torch.cuda.Stream(device=device)
-        self.gather = torch.cuda.Stream(device=device) if self.any_offload else None
+        # the gather has the highest stream priority: the host link is the scarce resource,
+        # so its CTAs are scheduled ahead of waiting compute CTAs
+        self.gather = (torch.cuda.Stream(device=device, priority=-1) if self.any_offload else None)
         self.graph = None
 
     # ------------------------------------------------------------------ one step
@@ -118,6 +123,8 @@ class DecodeStack:
             else:
                 sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
                                              self.out[L], self.ws_attn, stream=main)
+            if self.after_attention is not None:
+                self.after_attention(L)
             attn_done[L] = ev()
             attn_done[L].record(main)
             if L + 1 < self.n_layers:

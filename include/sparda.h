@@ -132,8 +132,12 @@ size_t sparda_workspace_bytes(const sparda_shape* shape, int32_t batch, int32_t 
  * if clear != 0, resets it. Synchronous: waits for all work on the device. */
 int32_t sparda_device_error(int32_t* flags, int32_t clear);
 
-/* Copy-CTA count the gather uses by default for a batch: 16 below batch 32, 32 from 32 on
- * (the batch-adaptive rule of the techwalker article, section 三). */
+/* Copy-CTA count the gather uses by default for a batch: 64 below batch 32, 152 (one per
+ * GB300 SM) from 32 on. The techwalker article (section 三) uses 16 / 32 copy CTAs on H100;
+ * the same batch-adaptive rule was re-measured here for this library's copy CTAs, which are
+ * small enough (128 threads, no shared memory) to share an SM with the compute kernels:
+ * while the selection and attention run beside it, the gather needs about 100 or more of
+ * them to keep the host link saturated, at almost no cost to the compute. */
 int32_t sparda_prefetch_default_ctas(int32_t batch);
 
 /* ---------------------------------------------------------------- the decode step */
@@ -223,7 +227,7 @@ int32_t sparda_sparse_decode_attn(const sparda_shape* shape, const sparda_layer_
  * For every (b, g) and slot s < cnt[b,g] whose block j = idx[b,g,s] is neither block 0 nor
  * the tail block, copies block j of the offloaded layer's host k and v into slot s of
  * staging_k / staging_v (device bf16 [max_batch, G, topk+2, 64, d]). n_ctas = 0 picks
- * sparda_prefetch_default_ctas(batch). Enqueue it on a side stream after an event recorded
+ * sparda_prefetch_default_ctas(batch); any count from 1 to 4096 is allowed. Enqueue it on a side stream after an event recorded
  * behind the select call, and make the attention wait on an event recorded behind it.
  */
 int32_t sparda_prefetch_blocks(const sparda_shape* shape, const sparda_layer_kv* layer,

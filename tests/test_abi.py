@@ -45,7 +45,7 @@ def test_workspace_sizes():
     assert sb.sparda_workspace_bytes(s, 0, sb.WS_SELECT) == 0
     assert sb.sparda_workspace_bytes(s, 17, sb.WS_SELECT) == 0
     assert sb.sparda_workspace_bytes(s, 4, 99) == 0
-    assert sb.sparda_prefetch_default_ctas(31) == 16 and sb.sparda_prefetch_default_ctas(32) == 32
+    assert sb.sparda_prefetch_default_ctas(31) == 64 and sb.sparda_prefetch_default_ctas(32) == 152
 
 
 def test_bad_arguments_are_rejected_before_any_launch():
