@@ -73,6 +73,13 @@ size_t attn_ml_bytes(const sparda_shape* s) {
   return round256((size_t)s->max_batch * s->n_groups * attn_splits(s) * 2 * kHeads * sizeof(float));
 }
 
+size_t mh_z_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * kHeads * w_cap(s) * sizeof(float));
+}
+size_t mh_stats_bytes(const sparda_shape* s) {
+  return round256((size_t)s->max_batch * s->n_groups * multihead_tiles(w_cap(s)) * kHeads * sizeof(float2));
+}
+
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return SPARDA_OK;
   std::fprintf(stderr, "sparda: CUDA error %s\n", cudaGetErrorString(e));
@@ -179,6 +186,7 @@ size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind
   switch (kind) {
     case SPARDA_WS_SELECT: return counters_bytes(s) + select_data_bytes(s);
     case SPARDA_WS_ATTN: return counters_bytes(s) + attn_o_bytes(s) + attn_ml_bytes(s);
+    case SPARDA_WS_MULTIHEAD: return mh_z_bytes(s) + mh_stats_bytes(s) + select_data_bytes(s);
     default: return 0;
   }
 }
@@ -324,10 +332,24 @@ int32_t sparda_prefetch_blocks(const sparda_shape* s, const sparda_layer_kv* L, 
 int32_t sparda_multihead_select(const sparda_shape* s, const void* ck, const void* q, const int32_t* seq_len,
                                 int32_t batch, int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes,
                                 void* stream) {
-  (void)ck; (void)q; (void)seq_len; (void)idx; (void)cnt; (void)ws; (void)ws_bytes; (void)stream;
   SPARDA_TRY(shape_status(s));
   SPARDA_TRY(batch_status(s, batch));
-  return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  if (!ck || !q || !seq_len || !idx || !cnt || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(ck, 16) || !aligned(q, 16) || !aligned(ws, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
+      !aligned(seq_len, 4))
+    return SPARDA_ERR_MISALIGNED;
+  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_MULTIHEAD)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap mck;
+  SPARDA_TRY(make_kv_map(&mck, ck, (uint64_t)s->max_batch * s->n_groups * w_cap(s)));
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MultiheadArgs a{static_cast<const __nv_bfloat16*>(q), seq_len, idx, cnt, reinterpret_cast<float*>(w),
+                  reinterpret_cast<float2*>(w + mh_z_bytes(s)),
+                  reinterpret_cast<float*>(w + mh_z_bytes(s) + mh_stats_bytes(s)), err, s->n_groups, w_cap(s),
+                  s->max_ctx, nb_cap(s), s->topk, multihead_tiles(w_cap(s))};
+  launch_multihead_select(a, mck, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
 }
 
 }  // extern "C"

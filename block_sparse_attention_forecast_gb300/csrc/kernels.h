@@ -66,6 +66,18 @@ struct AttnArgs {
   int n_units;                   // B*G*kslots, set by the launcher
 };
 
+struct MultiheadArgs {
+  const __nv_bfloat16* q;        // [B, G*H, d]
+  const int32_t* seq_len;
+  int32_t* idx;                  // [B, G, topk+2]
+  int32_t* cnt;                  // [B, G]
+  float* z;                      // workspace [B*G, H, W_cap] head scores (exp2 domain)
+  float2* stats;                 // workspace [B*G, n_tiles, H] per-tile (max, sum exp2)
+  float* block_scores;           // workspace [B*G, nb_cap]
+  int* err;
+  int G, W_cap, max_ctx, nb_cap, topk, n_tiles;
+};
+
 struct PrefetchArgs {
   const __nv_bfloat16* hk;       // host cache (UVA) [B, G, max_ctx, d]
   const __nv_bfloat16* hv;
@@ -87,6 +99,8 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
                         const CUtensorMap& hk, const CUtensorMap& hv, int bg_count,
                         cudaStream_t s);
 void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s);
+void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);
+int multihead_tiles(int w_cap);
 
 // Device address of the library's device error word on the current device (api.cu).
 int* dev_error_word();

@@ -261,3 +261,58 @@ def test_bad_seq_len_and_index_set_device_error(sb):
     q = torch.zeros((2, 32, 128), dtype=torch.bfloat16, device="cuda")
     sb.sparda_sparse_decode_attn(shape, layer, q, idx, cnt, seq, 2, out, wa)
     assert sb.sparda_device_error(clear=True) & sb.DEV_BAD_INDEX
+
+
+# ------------------------------------------------------------------ baseline multi-head selector
+def _mh_case(sb, K, q, T_list, k, max_ctx):
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    ck = torch.zeros((B, 2, shape.w_cap, 128), dtype=torch.bfloat16)
+    Sref = {}
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            W = O.num_windows(T - 1)
+            c = O.compress_keys(to64(K[b, g]), W)
+            ck[b, g, :W] = torch.from_numpy(c).to(torch.bfloat16)
+            s = O.multihead_scores(to64(q[b, 16 * g:16 * g + 16]), c) if W else np.zeros(0)
+            Sref[b, g] = O.pool_to_blocks(s, (T - 1) // 64 + 1)
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    idx = torch.full((B, 2, k + 2), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, 2), -7, dtype=torch.int32, device="cuda")
+    ws = sb.workspace(shape, B, sb.WS_MULTIHEAD)
+    for rep in range(2):
+        sb.sparda_multihead_select(shape, ck.cuda(), q.cuda(), seq, B, idx, cnt, ws)
+        torch.cuda.synchronize()
+        for b, T in enumerate(T_list):
+            for g in range(2):
+                check_selection(idx[b, g].cpu().numpy(), cnt[b, g].item(), Sref[b, g], T, k)
+    _no_device_error(sb)
+    return idx.cpu(), cnt.cpu()
+
+
+@pytest.mark.parametrize("T_list,k,max_ctx", [
+    ([4096], 8, 4096),
+    ([1, 65, 3000, 4097], 8, 8192),
+    ([8192, 5001], 32, 8192),
+])
+def test_multihead_select(sb, T_list, k, max_ctx):
+    B = len(T_list)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 91, B, k)
+    q = synth.normal_bf16((B, 32, 128), 92, B, k)
+    _mh_case(sb, K, q, T_list, k, max_ctx)
+
+
+def test_multihead_with_identical_queries_selects_like_the_forecast(sb):
+    # 16 heads all carrying the forecast vector: the summed per-head softmax is a monotone map
+    # of the single-head score, so both selectors pick the same blocks
+    T_list, k, max_ctx = [4096, 3001], 8, 4096
+    B = len(T_list)
+    case = [synth.tiny_case(s) for s in (5, 6)]
+    K = torch.stack([c["K"][0] for c in case])
+    f = torch.stack([c["f"][0] for c in case])
+    q = f.repeat_interleave(16, dim=1)                       # [B, 32, 128]
+    idx, cnt = _mh_case(sb, K, q, T_list, k, max_ctx)
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            _, S1 = O.forecast_select_one(to64(K[b, g]), to64(f[b, g]), T, k, return_scores=True)
+            check_selection(idx[b, g].numpy(), cnt[b, g].item(), S1, T, k)
