@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
     p.add_argument("--offload-steps", type=int, default=20)
+    p.add_argument("--no-selector-ab", action="store_true", help="skip the selector A/B sweep")
     return p.parse_args()
 
 
@@ -369,6 +370,48 @@ def run_offload(device, seed, steps, warmup):
     return res
 
 
+# ---------------------------------------------------------------------- selector A/B
+def selector_ab(device, seed):
+    """BASELINE config 5: one layer's selection, the Forecast selector (one head per group, no
+    softmax) against the baseline multi-head selector (16 query heads per group, softmax per
+    head, sum, max-pool, top-32), for batch 1..128 at context 131072 and for context 32K..128K
+    at batch 16. Compressed keys, forecasts and queries are seeded N(0,1) bf16 drawn on the
+    device (selection time does not depend on their values). Device time per call from CUDA
+    graph replays; GB/s counts the compressed keys and forecast/query bytes each call reads."""
+    import torch
+    import synth
+    import block_sparse_attention_forecast_gb300.binding as sb
+    out = {"batch_sweep_ctx131072": {}, "context_sweep_batch16": {}}
+
+    def one(B, T):
+        shape = sb.Shape(n_groups=G, topk=TOPK, max_ctx=T, max_batch=B)
+        ck = synth.normal_bf16_device((B, G, shape.w_cap, D), seed * 1000 + 900 + B, device, std=0.18)
+        f = synth.normal_bf16_device((B, G, D), seed * 1000 + 901, device)
+        q = synth.normal_bf16_device((B, G * H, D), seed * 1000 + 902, device)
+        seq = torch.full((B,), T, dtype=torch.int32, device=device)
+        idx = torch.zeros((B, G, TOPK + 2), dtype=torch.int32, device=device)
+        cnt = torch.zeros((B, G), dtype=torch.int32, device=device)
+        ws = sb.workspace(shape, B, sb.WS_SELECT, device)
+        wm = sb.workspace(shape, B, sb.WS_MULTIHEAD, device)
+        from block_sparse_attention_forecast_gb300.binding import num_windows
+        W = num_windows(T - 1)
+        t_f = graph_time(lambda s: sb.sparda_forecast_select(shape, ck, f, seq, B, idx, cnt, ws, stream=s), 8)
+        t_m = graph_time(lambda s: sb.sparda_multihead_select(shape, ck, q, seq, B, idx, cnt, wm, stream=s), 8)
+        bytes_f = B * G * (W * D * 2 + D * 2)
+        bytes_m = B * G * (W * D * 2 + H * D * 2)
+        del ck, ws, wm
+        torch.cuda.empty_cache()
+        return {"forecast_us": t_f * 1e6, "multihead_us": t_m * 1e6, "speedup": t_m / t_f,
+                "forecast_gbs": bytes_f / t_f / 1e9, "multihead_gbs": bytes_m / t_m / 1e9}
+
+    for B in (1, 8, 32, 64, 128):
+        out["batch_sweep_ctx131072"][str(B)] = one(B, CTX)
+    for T in (32768, 65536, 98304, 131072):
+        out["context_sweep_batch16"][str(T)] = one(16, T)
+    out["device_error_flags"] = sb.sparda_device_error(clear=True)
+    return out
+
+
 # ---------------------------------------------------------------------- CPU oracle sample
 CPU_SAMPLE_SCRIPT = r"""
 import sys, time, json
@@ -510,6 +553,9 @@ def run_ours(args):
         gc.collect()
         torch.cuda.empty_cache()
         offload = run_offload(device, args.seed, args.offload_steps, 3)
+    ab = None
+    if world == 1 and not args.no_selector_ab:
+        ab = selector_ab(device, args.seed)
     if dist:
         tt = torch.tensor([elapsed, e2e_elapsed], device=device, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -552,6 +598,8 @@ def run_ours(args):
     }
     if offload is not None:
         line["offload"] = offload
+    if ab is not None:
+        line["selector_ab"] = ab
     if cpu is not None:
         per_step, cores, desc = cpu
         line["cpu_baseline"] = {"value": BATCH / per_step, "unit": "tok/s", "cores": cores, "kind": "oracle",
