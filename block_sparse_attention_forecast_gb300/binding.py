@@ -22,7 +22,7 @@ __all__ = [
     "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes", "sparda_device_error",
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
-    "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static",
+    "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
@@ -95,6 +95,7 @@ def _load():
         "sparda_prefetch_blocks": (I32, [SH, LY, P, P, P, I32, P, P, I32, P]),
         "sparda_multihead_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
         "sparda_forecast_select_static": (I32, [SH, P, P, P, I32, P, P, P]),
+        "sparda_attend_and_select": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, P, P, SZ, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -284,6 +285,14 @@ def sparda_sparse_decode_attn(shape, layer, q, idx, cnt, seq_len, batch, out, ws
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(staging_k), _ptr(staging_v),
         _ptr(q), _ptr(idx), _ptr(cnt), _ptr(seq_len), int(batch), _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def sparda_attend_and_select(shape, layer, q, idx, cnt, out, ws_attn, ck_next, forecast_next, idx_next,
+                             cnt_next, ws_sel, seq_len, batch, staging_k=None, staging_v=None, stream=None):
+    _check("sparda_attend_and_select", lib.sparda_attend_and_select(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(staging_k), _ptr(staging_v), _ptr(q), _ptr(idx),
+        _ptr(cnt), _ptr(out), _ptr(ws_attn), ws_attn.numel(), _ptr(ck_next), _ptr(forecast_next), _ptr(idx_next),
+        _ptr(cnt_next), _ptr(ws_sel), ws_sel.numel(), _ptr(seq_len), int(batch), _stream(stream)))
 
 
 def sparda_prefetch_blocks(shape, layer, idx, cnt, seq_len, batch, staging_k, staging_v,

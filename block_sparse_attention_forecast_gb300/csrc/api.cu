@@ -248,9 +248,14 @@ int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int3
   return cuda_status(cudaGetLastError());
 }
 
-int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void* forecast,
-                               const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
-                               void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks and kernel arguments of the selection call (shared by the standalone and
+// the fused entry points).
+int32_t prepare_select(const sparda_shape* s, const void* ck, const void* forecast, const int32_t* seq_len,
+                       int32_t batch, int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, SelectArgs* out) {
   SPARDA_TRY(shape_status(s));
   SPARDA_TRY(batch_status(s, batch));
   if (!ck || !forecast || !seq_len || !idx || !cnt || !ws) return SPARDA_ERR_INVALID_ARG;
@@ -262,11 +267,62 @@ int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void
   if (!err) return SPARDA_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int bgc = batch * s->n_groups;
-  SelectArgs a{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
-               seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
-               reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
-               s->topk, select_chunk_blocks(nb_cap(s), bgc), 0};
-  launch_forecast_select(a, bgc, static_cast<cudaStream_t>(stream));
+  *out = SelectArgs{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
+                    seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
+                    reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
+                    s->topk, select_chunk_blocks(nb_cap(s), bgc), 0};
+  return SPARDA_OK;
+}
+
+// Argument checks, tensor maps and kernel arguments of the attention call.
+int32_t prepare_attn(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
+                     const void* staging_v, const void* q, const int32_t* idx, const int32_t* cnt,
+                     const int32_t* seq_len, int32_t batch, void* out, void* ws, size_t ws_bytes,
+                     AttnArgs* args, CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* hk, CUtensorMap* hv) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!L || !q || !idx || !cnt || !seq_len || !out || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16) || !aligned(idx, 4) || !aligned(cnt, 4))
+    return SPARDA_ERR_MISALIGNED;
+  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_ATTN)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  const uint64_t bgcap = (uint64_t)s->max_batch * s->n_groups;
+  if (L->on_host) {
+    if (!staging_k || !staging_v || !L->hot_k || !L->hot_v) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(staging_k, 16) || !aligned(staging_v, 16) || !aligned(L->hot_k, 16) || !aligned(L->hot_v, 16))
+      return SPARDA_ERR_MISALIGNED;
+    SPARDA_TRY(make_kv_map(mk, staging_k, bgcap * kslots(s) * kBlock));
+    SPARDA_TRY(make_kv_map(mv, staging_v, bgcap * kslots(s) * kBlock));
+    SPARDA_TRY(make_kv_map(hk, L->hot_k, bgcap * kHotSlots * kBlock));
+    SPARDA_TRY(make_kv_map(hv, L->hot_v, bgcap * kHotSlots * kBlock));
+  } else {
+    if (!L->k || !L->v) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(L->k, 16) || !aligned(L->v, 16)) return SPARDA_ERR_MISALIGNED;
+    SPARDA_TRY(make_kv_map(mk, L->k, bgcap * s->max_ctx));
+    SPARDA_TRY(make_kv_map(mv, L->v, bgcap * s->max_ctx));
+    *hk = *mk;
+    *hv = *mv;
+  }
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  *args = AttnArgs{static_cast<const __nv_bfloat16*>(q), idx, cnt, seq_len, static_cast<__nv_bfloat16*>(out),
+                   reinterpret_cast<float*>(w + counters_bytes(s)),
+                   reinterpret_cast<float*>(w + counters_bytes(s) + attn_o_bytes(s)),
+                   reinterpret_cast<unsigned*>(w), err, s->n_groups, s->max_ctx, kslots(s), attn_splits(s),
+                   L->on_host ? 1 : 0, 0};
+  return SPARDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void* forecast,
+                               const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
+                               void* ws, size_t ws_bytes, void* stream) {
+  SelectArgs a;
+  SPARDA_TRY(prepare_select(s, ck, forecast, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
+  launch_forecast_select(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 
@@ -274,39 +330,28 @@ int32_t sparda_sparse_decode_attn(const sparda_shape* s, const sparda_layer_kv* 
                                   const void* staging_v, const void* q, const int32_t* idx,
                                   const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* out,
                                   void* ws, size_t ws_bytes, void* stream) {
-  SPARDA_TRY(shape_status(s));
-  SPARDA_TRY(batch_status(s, batch));
-  if (!L || !q || !idx || !cnt || !seq_len || !out || !ws) return SPARDA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16) || !aligned(idx, 4) || !aligned(cnt, 4))
-    return SPARDA_ERR_MISALIGNED;
-  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_ATTN)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  AttnArgs a;
   CUtensorMap mk, mv, hk, hv;
-  const uint64_t bgcap = (uint64_t)s->max_batch * s->n_groups;
-  if (L->on_host) {
-    if (!staging_k || !staging_v || !L->hot_k || !L->hot_v) return SPARDA_ERR_INVALID_ARG;
-    if (!aligned(staging_k, 16) || !aligned(staging_v, 16) || !aligned(L->hot_k, 16) || !aligned(L->hot_v, 16))
-      return SPARDA_ERR_MISALIGNED;
-    SPARDA_TRY(make_kv_map(&mk, staging_k, bgcap * kslots(s) * kBlock));
-    SPARDA_TRY(make_kv_map(&mv, staging_v, bgcap * kslots(s) * kBlock));
-    SPARDA_TRY(make_kv_map(&hk, L->hot_k, bgcap * kHotSlots * kBlock));
-    SPARDA_TRY(make_kv_map(&hv, L->hot_v, bgcap * kHotSlots * kBlock));
-  } else {
-    if (!L->k || !L->v) return SPARDA_ERR_INVALID_ARG;
-    if (!aligned(L->k, 16) || !aligned(L->v, 16)) return SPARDA_ERR_MISALIGNED;
-    SPARDA_TRY(make_kv_map(&mk, L->k, bgcap * s->max_ctx));
-    SPARDA_TRY(make_kv_map(&mv, L->v, bgcap * s->max_ctx));
-    hk = mk;
-    hv = mv;
-  }
-  int* err = dev_error_ptr();
-  if (!err) return SPARDA_ERR_CUDA;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  AttnArgs a{static_cast<const __nv_bfloat16*>(q), idx, cnt, seq_len, static_cast<__nv_bfloat16*>(out),
-             reinterpret_cast<float*>(w + counters_bytes(s)),
-             reinterpret_cast<float*>(w + counters_bytes(s) + attn_o_bytes(s)),
-             reinterpret_cast<unsigned*>(w), err, s->n_groups, s->max_ctx, kslots(s), attn_splits(s),
-             L->on_host ? 1 : 0, 0};
+  SPARDA_TRY(prepare_attn(s, L, staging_k, staging_v, q, idx, cnt, seq_len, batch, out, ws, ws_bytes, &a, &mk,
+                          &mv, &hk, &hv));
   launch_sparse_attn(a, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_attend_and_select(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
+                                 const void* staging_v, const void* q, const int32_t* idx, const int32_t* cnt,
+                                 void* out, void* ws_attn, size_t ws_attn_bytes, const void* ck_next,
+                                 const void* forecast_next, int32_t* idx_next, int32_t* cnt_next, void* ws_sel,
+                                 size_t ws_sel_bytes, const int32_t* seq_len, int32_t batch, void* stream) {
+  if (idx_next == idx || cnt_next == cnt || ws_sel == ws_attn) return SPARDA_ERR_INVALID_ARG;
+  AttnArgs a;
+  CUtensorMap mk, mv, hk, hv;
+  SPARDA_TRY(prepare_attn(s, L, staging_k, staging_v, q, idx, cnt, seq_len, batch, out, ws_attn, ws_attn_bytes,
+                          &a, &mk, &mv, &hk, &hv));
+  SelectArgs sa;
+  SPARDA_TRY(prepare_select(s, ck_next, forecast_next, seq_len, batch, idx_next, cnt_next, ws_sel, ws_sel_bytes,
+                            &sa));
+  launch_attend_and_select(a, sa, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

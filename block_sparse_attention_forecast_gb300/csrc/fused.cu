@@ -1,0 +1,62 @@
+// Layer L's block-sparse attention and layer L+1's Forecast selection in one persistent
+// launch. Under lookahead the two are independent (layer L's forecast already exists when
+// layer L attends), and each alone is a persistent kernel that wants every SM, so launched
+// side by side they would only run one after the other. Here the grid is one CTA per SM,
+// split between the two jobs in proportion to the bytes each must stream: CTAs [0, n_attn)
+// run the attention work (attn_cta) over the attention units, the others the selection work
+// (sel_cta) over the selection units, so both jobs stream concurrently from HBM and finish
+// together, with one launch and one start-up per layer.
+#include "attn_body.cuh"
+#include "select_body.cuh"
+
+namespace sparda {
+
+static_assert(kAttnThreads == kSelThreads, "both jobs run with the same CTA shape");
+constexpr int kFusedSmem = kAttnSmem > kSelSmem ? kAttnSmem : kSelSmem;
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
+    const AttnArgs aa, const SelectArgs sa, int n_attn, const __grid_constant__ CUtensorMap mk,
+    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap hk,
+    const __grid_constant__ CUtensorMap hv) {
+  if ((int)blockIdx.x < n_attn)
+    attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x, n_attn);
+  else
+    sel_cta(sa, blockIdx.x - n_attn, gridDim.x - n_attn);
+}
+
+int sm_count();
+
+void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& hk, const CUtensorMap& hv,
+                              int bg_count, cudaStream_t st) {
+  cudaFuncSetAttribute(attend_and_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem);
+  AttnArgs aa = a;
+  SelectArgs sa = s;
+  aa.n_units = bg_count * a.kslots;
+  sa.n_units = bg_count * s.nb_cap;
+  // split the SMs by streamed bytes: an attention unit is one K+V block (32 KiB), a selection
+  // unit one block's four windows of compressed keys (1 KiB); the attention CTAs also merge
+  // split groups, weighted in as about 10% more work per byte
+  const double wa = 1.1 * (double)aa.n_units * (2.0 * kBlockBytes);
+  const double ws = (double)sa.n_units * (kWinPerBlock * kRowBytes);
+  const int sms = sm_count();
+  int n_attn = (int)(sms * wa / (wa + ws) + 0.5);
+  n_attn = n_attn < 1 ? 1 : (n_attn > sms - 1 ? sms - 1 : n_attn);
+  if (n_attn > aa.n_units) n_attn = aa.n_units;
+  int n_sel = sms - n_attn;
+  const int sel_work = (sa.n_units + kSubBlocks - 1) / kSubBlocks;
+  if (n_sel > sel_work) n_sel = sel_work;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_attn + n_sel);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kFusedSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, attend_and_select_kernel, aa, sa, n_attn, mk, mv, hk, hv);
+}
+
+}  // namespace sparda

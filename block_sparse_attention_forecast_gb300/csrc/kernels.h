@@ -99,6 +99,9 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
                         const CUtensorMap& hk, const CUtensorMap& hv, int bg_count,
                         cudaStream_t s);
 void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s);
+void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& hk, const CUtensorMap& hv,
+                              int bg_count, cudaStream_t st);
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);
 int multihead_tiles(int w_cap);
 

@@ -34,7 +34,7 @@ class DecodeStack:
     """
 
     def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
-                 overlap=True, advance=False, after_attention=None):
+                 overlap=True, advance=False, after_attention=None, fused=True):
         self.shape = shape
         self.layers = layers
         self.n_layers = len(layers)
@@ -49,6 +49,11 @@ class DecodeStack:
         # example the rest of the layer: output projection and FFN)
         self.after_attention = after_attention
         assert not layers[0].on_host, "layer 0 stays resident"
+        self.any_offload = any(l.on_host for l in layers)
+        # Resident stacks run layer L's attention and layer L+1's selection as one launch
+        # (sparda_attend_and_select). Offloaded stacks keep them apart: layer L+1's selection
+        # must finish early so that its gather overlaps layer L.
+        self.fused = fused and not self.any_offload
         G, H, d = shape.n_groups, shape.heads_per_group, shape.head_dim
         hidden = W_self0.shape[1]
         n, B = self.n_layers, batch
@@ -64,7 +69,7 @@ class DecodeStack:
         self.seq_len = torch.ones(B, dtype=torch.int32, device=device)
         self.ws_sel = sb.workspace(shape, B, sb.WS_SELECT, device)
         self.ws_attn = sb.workspace(shape, B, sb.WS_ATTN, device)
-        self.any_offload = any(l.on_host for l in layers)
+        self.ws_sel2 = sb.workspace(shape, B, sb.WS_SELECT, device) if self.fused else None
         if self.any_offload:
             st = (shape.max_batch, G, shape.kslots, shape.block, d)
             self.stage_k = [torch.zeros(st, **bf) for _ in range(2)]
@@ -78,6 +83,8 @@ class DecodeStack:
     # ------------------------------------------------------------------ one step
     def enqueue(self):
         """Enqueue one decode step on the current stream (plus the side streams)."""
+        if self.fused:
+            return self._enqueue_fused()
         sh, B = self.shape, self.batch
         main = torch.cuda.current_stream()
         side = self.side
@@ -134,6 +141,34 @@ class DecodeStack:
         if self.advance:
             self.seq_len.add_(1)
 
+    def _enqueue_fused(self):
+        """Resident stack, one stream: per layer the forecast projection for layer L+1, the
+        append of layer L, then layer L's attention together with layer L+1's selection."""
+        sh, B = self.shape, self.batch
+        main = torch.cuda.current_stream()
+        sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
+        sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
+                                  self.idx[0], self.cnt[0], self.ws_sel, stream=main)
+        for L in range(self.n_layers):
+            layer = self.layers[L]
+            last = L + 1 == self.n_layers
+            if not last:
+                sb.sparda_forecast_project(self.W_next[L], self.h[L], self.f[L + 1].view(B, -1), stream=main)
+            sb.sparda_append_kv(sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B, stream=main)
+            if last:
+                sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
+                                             self.out[L], self.ws_attn, stream=main)
+            else:
+                # alternate the selection workspace so that consecutive layers never share one
+                ws = self.ws_sel if L % 2 == 0 else self.ws_sel2
+                sb.sparda_attend_and_select(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.out[L],
+                                            self.ws_attn, self.layers[L + 1].ck, self.f[L + 1],
+                                            self.idx[L + 1], self.cnt[L + 1], ws, self.seq_len, B, stream=main)
+            if self.after_attention is not None:
+                self.after_attention(L)
+        if self.advance:
+            self.seq_len.add_(1)
+
     def capture(self):
         """Capture one step into a CUDA graph (after one eager warm-up step)."""
         s = torch.cuda.Stream(device=self.device)
@@ -155,9 +190,13 @@ class DecodeStack:
             self.enqueue()
 
     def kernel_launches_per_step(self):
-        """Kernels one step launches: per layer append, forecast projection, select (all
-        but the last layer), attention, plus layer 0's own projection and select and one
-        gather per offloaded layer."""
+        """Kernels of libsparda one step launches. Fused: layer 0's own projection and
+        selection, then per layer an append plus (all but the last layer) a projection and an
+        attend-and-select, the last layer's attention alone. Unfused: per layer append and
+        attention, per layer but the last a projection and a selection, one gather per
+        offloaded layer."""
         n = self.n_layers
+        if self.fused:
+            return 2 + n + 2 * (n - 1) + 1
         gathers = sum(1 for l in self.layers[1:] if l.on_host)
         return 2 + n * 2 + (n - 1) * 2 + gathers

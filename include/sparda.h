@@ -219,6 +219,27 @@ int32_t sparda_sparse_decode_attn(const sparda_shape* shape, const sparda_layer_
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sparda_attend_and_select -- layer L's sparda_sparse_decode_attn and layer L+1's
+ * sparda_forecast_select in one launch. Under lookahead the two are independent: layer L's
+ * forecast exists when layer L attends (bittide thread; techwalker section 二). One
+ * persistent grid of one CTA per SM is split between the two jobs in proportion to the
+ * bytes each streams, so both run at once instead of one after the other.
+ *
+ * Arguments and results are exactly those of the two calls: (layer, staging_k, staging_v,
+ * q, idx, cnt, out, ws_attn) as for sparda_sparse_decode_attn on layer L, and (ck_next,
+ * forecast_next, idx_next, cnt_next, ws_sel) as for sparda_forecast_select on layer L+1's
+ * compressed keys; seq_len and batch are shared. idx_next / cnt_next / ws_sel must be other
+ * buffers than idx / cnt / ws_attn (SPARDA_ERR_INVALID_ARG otherwise).
+ */
+int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_kv* layer,
+                                 const void* staging_k, const void* staging_v, const void* q,
+                                 const int32_t* idx, const int32_t* cnt, void* out, void* ws_attn,
+                                 size_t ws_attn_bytes, const void* ck_next,
+                                 const void* forecast_next, int32_t* idx_next, int32_t* cnt_next,
+                                 void* ws_sel, size_t ws_sel_bytes, const int32_t* seq_len,
+                                 int32_t batch, void* stream);
+
+/*
  * sparda_prefetch_blocks -- the gather that hides the host-offload copy (bittide thread:
  * the next layer's blocks are fetched on a separate CUDA stream while the current layer
  * computes; techwalker §三: a persistent kernel with a few copy CTAs reads host memory

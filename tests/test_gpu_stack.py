@@ -21,7 +21,8 @@ def sb(cuda_ok):
     return b
 
 
-def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, offload=(), overlap=True):
+def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, offload=(), overlap=True,
+                    fused=True):
     """Seeded caches holding tokens 0..T-2, the step's inputs, and forecast heads; planted
     blocks of each layer are shifted along the forecast (computed by the oracle) that selects
     that layer's blocks."""
@@ -57,7 +58,8 @@ def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, 
         Ks.append(K)
         Vs.append(V)
         layers.append(layer)
-    stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B, overlap=overlap)
+    stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B, overlap=overlap,
+                        fused=fused)
     stack.h.copy_(h.cuda())
     stack.q.copy_(q.cuda())
     stack.k_new.copy_(kn.cuda())
@@ -144,4 +146,20 @@ def test_offloaded_stack_step(sb, overlap):
     torch.cuda.synchronize()
     assert torch.equal(stack.idx, eager_idx)
     assert torch.equal(stack.out, eager_out)
+    assert sb.sparda_device_error(clear=True) == 0
+
+
+def test_fused_and_separate_launches_agree(sb):
+    # layer L's attention and layer L+1's selection in one launch (the resident default) or
+    # as two kernels on two streams: same kernels' work, bit-identical results
+    n_layers, B, T, topk, max_ctx, hidden = 4, 3, 3001, 8, 4096, 256
+    outs = []
+    for fused in (True, False):
+        shape, stack, inputs = make_stack_case(sb, 11, n_layers, B, T, topk, max_ctx, hidden, 8, fused=fused)
+        assert stack.fused == fused
+        stack.enqueue()
+        torch.cuda.synchronize()
+        outs.append((stack.idx.clone(), stack.cnt.clone(), stack.out.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
     assert sb.sparda_device_error(clear=True) == 0
