@@ -29,7 +29,11 @@ if ROOT not in sys.path:
 
 N_LAYERS, BATCH, CTX, G, H, D, HIDDEN, TOPK, PLANTED = 32, 16, 131072, 2, 16, 128, 4096, 32, 16
 METRIC = "decode tok/s @128K ctx (B=16 resident, B=64 offload); select+attn HBM GB/s"
-WORKLOAD = "32-layer forecast-driven block-sparse decode step, batch 16, context 131072, KV resident"
+def workload_name(n_layers=N_LAYERS):
+    return "%d-layer forecast-driven block-sparse decode step, batch 16, context 131072, KV resident" % n_layers
+
+
+WORKLOAD = workload_name()
 
 
 def parse():
@@ -43,6 +47,9 @@ def parse():
     p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
     p.add_argument("--offload-steps", type=int, default=20)
     p.add_argument("--no-selector-ab", action="store_true", help="skip the selector A/B sweep")
+    p.add_argument("--layers", type=int, default=N_LAYERS,
+                   help="layers of the resident stack (the metric is quoted on 32; fewer only for small "
+                        "profiler captures)")
     return p.parse_args()
 
 
@@ -54,22 +61,36 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def source_sha(name):
-    path = os.path.join(ROOT, "block_sparse_attention_forecast_gb300", "csrc", name)
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+# the sources each profiled kernel is built from (a change to any of them voids its counters)
+KERNEL_SOURCES = {
+    "attend_and_score": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
+    "attend_and_select": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
+    "decode_prologue": ("prologue.cu", "append_body.cuh", "project_body.cuh", "topk.cuh", "common.cuh",
+                        "kernels.h"),
+    "sparse_decode_attn": ("attn.cu", "attn_body.cuh", "common.cuh", "kernels.h"),
+    "forecast_select": ("select.cu", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
+}
 
 
-def ncu_traffic(kernel_file):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source still
-    matches the one profiled (else None)."""
+def source_sha(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_sparse_attention_forecast_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    (profiles/traffic.json), if the kernel's sources still match the ones profiled; else
+    None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             t = json.load(fh)
     except OSError:
         return None
-    e = t.get(kernel_file)
-    if not e or e.get("source_sha") != source_sha(kernel_file):
+    e = t.get(kernel)
+    if not e or e.get("source_sha") != source_sha(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -124,7 +145,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- workload
-def build_workload(device, seed, steps_total):
+def build_workload(device, seed, steps_total, n_layers=N_LAYERS):
     import torch
     import synth
     import block_sparse_attention_forecast_gb300.binding as sb
@@ -137,11 +158,11 @@ def build_workload(device, seed, steps_total):
     g.manual_seed(seed)
     W_self0 = synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 1, device, std=0.02)
     W_next = [synth.normal_bf16_device((G * D, HIDDEN), seed * 1000 + 2 + L, device, std=0.02)
-              for L in range(N_LAYERS - 1)]
-    h = synth.normal_bf16_device((N_LAYERS, BATCH, HIDDEN), seed * 1000 + 40, device)
+              for L in range(n_layers - 1)]
+    h = synth.normal_bf16_device((n_layers, BATCH, HIDDEN), seed * 1000 + 40, device)
     layers = []
     import numpy as np
-    for L in range(N_LAYERS):
+    for L in range(n_layers):
         layer = sb.LayerKV.empty(shape, device=device)
         layer.k.copy_(synth.normal_bf16_device(layer.k.shape, seed * 1000 + 100 + L, device))
         layer.v.copy_(synth.normal_bf16_device(layer.v.shape, seed * 1000 + 200 + L, device))
@@ -164,12 +185,35 @@ def build_workload(device, seed, steps_total):
 
 
 def kernel_times(stack, reps=4):
-    """Average device time of one forecast_select and one sparse_decode_attn launch: the
-    step's own calls for every layer (same buffers) captured back to back in a CUDA graph,
-    replayed and timed with CUDA events on the launching stream (no host launch overhead)."""
-    import torch
+    """Average device time of one launch of each hot kernel, from the step's own calls (same
+    buffers, every layer) captured back to back in a CUDA graph, replayed and timed with CUDA
+    events on the launching stream (no host launch overhead): the step's attend-and-score
+    and decode-prologue launches, and for comparison the attend-and-select launch of the
+    three-launch layout and forecast_select and sparse_decode_attn each launched alone."""
     import block_sparse_attention_forecast_gb300.binding as sb
     sh, B, n = stack.shape, stack.batch, stack.n_layers
+    scores = (stack.ws_sel, stack.ws_sel2)
+
+    def score_loop(s):
+        for L in range(n - 1):
+            sb.sparda_attend_and_score(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
+                                       stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], scores[(L + 1) % 2],
+                                       stack.seq_len, B, stream=s)
+
+    def prologue_loop(s):
+        # the prologues of layers 1 .. n-2 (top-k, append and projection each); the scores
+        # they select from are the ones score_loop left
+        for L in range(1, n - 1):
+            sb.sparda_decode_prologue(sh, stack.layers[L], stack.k_new[L], stack.v_new[L], stack.seq_len, B,
+                                      ws_scores=scores[L % 2], idx=stack.idx[L], cnt=stack.cnt[L],
+                                      W_next=stack.W_next[L], h=stack.h[L], forecast_next=stack.f[L + 1].view(B, -1),
+                                      stream=s)
+
+    def fused_loop(s):
+        for L in range(n - 1):
+            sb.sparda_attend_and_select(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
+                                        stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], stack.idx[L + 1],
+                                        stack.cnt[L + 1], scores[(L + 1) % 2], stack.seq_len, B, stream=s)
 
     def sel_loop(s):
         for L in range(1, n):
@@ -182,33 +226,52 @@ def kernel_times(stack, reps=4):
                                          stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
 
     out = {}
-    for name, fn, per in (("select", sel_loop, n - 1), ("attn", attn_loop, n)):
-        fn(torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            s = torch.cuda.current_stream()
-            for _ in range(reps):
-                fn(s)
-        g.replay()
-        torch.cuda.synchronize()
-        s = torch.cuda.current_stream()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        g.replay()
-        e1.record(s)
-        torch.cuda.synchronize()
-        out[name] = e0.elapsed_time(e1) * 1e-3 / (reps * per)
+    for name, fn, per in (("score", score_loop, n - 1), ("prologue", prologue_loop, n - 2),
+                          ("fused", fused_loop, n - 1), ("select", sel_loop, n - 1), ("attn", attn_loop, n)):
+        if per > 0:
+            out[name] = graph_time(fn, reps) / per
     return out
 
 
-def select_bytes(T):
+def select_bytes(T, batch=BATCH):
+    """Algorithmic bytes of one selection launch: every compressed key of the windows complete
+    within T-1 tokens plus the forecast, per (sequence, group)."""
     from block_sparse_attention_forecast_gb300.binding import num_windows
-    return BATCH * G * (num_windows(T - 1) * D * 2 + D * 2)
+    return batch * G * (num_windows(T - 1) * D * 2 + D * 2)
 
 
-def attn_bytes():
-    return BATCH * G * ((TOPK + 2) * 64 * D * 2 * 2 + 2 * H * D * 2)
+def attn_bytes(batch=BATCH):
+    """Algorithmic bytes of one attention launch: K and V of the k + 2 selected 64-token blocks
+    plus the 16 queries read and the 16 outputs written, per (sequence, group)."""
+    return batch * G * ((TOPK + 2) * 64 * D * 2 * 2 + 2 * H * D * 2)
+
+
+def prologue_bytes(batch=BATCH):
+    """Algorithmic bytes of one decode prologue: the forecast head's weights and the hidden
+    states read and the forecasts written (projection), the block scores read and the
+    selection written (top-k), the token's key and value read and written (append)."""
+    nb = CTX // 64
+    proj = G * D * HIDDEN * 2 + batch * HIDDEN * 2 + batch * G * D * 2
+    topk = batch * G * (nb * 4 + (TOPK + 2) * 4 + 4)
+    append = batch * G * D * 2 * 2 * 2
+    return proj + topk + append
+
+
+def replica_max(values, dist, device):
+    """Max over ranks of each timing (every rank gets the maxima). With one rank the values
+    come back unchanged."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(world, batch, steps, elapsed_max):
+    """Whole-job decode tokens/s of `world` independent replicas, each decoding `batch`
+    sequences for `steps` steps, timed by the slowest replica."""
+    return world * batch * steps / elapsed_max
 
 
 # ---------------------------------------------------------------------- offloaded decode
@@ -490,7 +553,7 @@ def run_ours(args):
         cpu = cpu_oracle_sample(24)          # before any heavy GPU setup; ~15 s of CPU work
 
     steps_total = 1 + args.warmup + args.steps
-    shape, stack, T0 = build_workload(device, args.seed + rank, steps_total)
+    shape, stack, T0 = build_workload(device, args.seed + rank, steps_total, args.layers)
     import block_sparse_attention_forecast_gb300.binding as sb
     stack.capture()                          # one eager step, then the captured graph
     for _ in range(args.warmup):
@@ -556,10 +619,7 @@ def run_ours(args):
     ab = None
     if world == 1 and not args.no_selector_ab:
         ab = selector_ab(device, args.seed)
-    if dist:
-        tt = torch.tensor([elapsed, e2e_elapsed], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed, e2e_elapsed = tt.tolist()
+    elapsed, e2e_elapsed = replica_max([elapsed, e2e_elapsed], dist, device)
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -567,30 +627,35 @@ def run_ours(args):
     peaks, peak_src = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     sel_b, att_b = select_bytes(CTX), attn_bytes()
-    sel_gbs = sel_b / kt["select"] / 1e9
-    att_gbs = att_b / kt["attn"] / 1e9
-    traffic = ncu_traffic("select.cu")
+    kernels = {}
+    for name, key, b in (("attend_and_score", "score", sel_b + att_b), ("attend_and_select", "fused", sel_b + att_b),
+                         ("forecast_select", "select", sel_b), ("sparse_decode_attn", "attn", att_b),
+                         ("decode_prologue", "prologue", prologue_bytes())):
+        if key in kt:
+            gbs = b / kt[key] / 1e9
+            kernels[name] = {"us": kt[key] * 1e6, "alg_bytes": b, "gbs": gbs, "frac": gbs / hbm}
+    # the step's dominant kernel: layer L's attention beside layer L+1's block scoring
+    dom = "attend_and_score" if "attend_and_score" in kernels else "sparse_decode_attn"
+    dk = kernels[dom]
     ms = elapsed / args.steps * 1e3
-    value = world * BATCH * args.steps / elapsed
+    value = replica_throughput(world, BATCH, args.steps, elapsed)
+    n = args.layers
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch_per_gpu": BATCH, "context": CTX, "layers": N_LAYERS,
+        "config": {"workload": workload_name(n), "batch_per_gpu": BATCH, "context": CTX, "layers": n,
                    "kv_heads": G, "q_heads": G * H, "head_dim": D, "topk": TOPK, "block": 64,
                    "window": "32/16", "hidden": HIDDEN, "parallelism": "replicas" if world > 1 else "single",
                    "positions": "%d consecutive decode steps ending at context %d" % (args.steps, T_last),
                    "l2": "inputs larger than L2 (a step reads ~3.4 GB of compressed keys and KV)",
                    "timing": "CUDA graph replay, CUDA events on the launching stream, max over ranks"},
-        "roofline": {"bound": "hbm", "kernel": "forecast_select_kernel", "achieved": sel_gbs, "peak": hbm,
-                     "unit": "GB/s", "frac": sel_gbs / hbm, "peak_source": peak_src + " hbm_gbs (burst)",
-                     "traffic": traffic, "alg_bytes_per_launch": sel_b, "launch_us": kt["select"] * 1e6},
-        "kernels": {
-            "forecast_select": {"us": kt["select"] * 1e6, "alg_bytes": sel_b, "gbs": sel_gbs, "frac": sel_gbs / hbm},
-            "sparse_decode_attn": {"us": kt["attn"] * 1e6, "alg_bytes": att_b, "gbs": att_gbs, "frac": att_gbs / hbm},
-            "select_attn_gbs": (sel_b + att_b) / (kt["select"] + kt["attn"]) / 1e9,
-        },
-        "e2e": {"value": world * BATCH * e2e_steps / e2e_elapsed, "unit": "tok/s",
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": dk["frac"], "peak_source": peak_src + " hbm_gbs (burst copy)",
+                     "traffic": ncu_traffic(dom), "alg_bytes_per_launch": dk["alg_bytes"],
+                     "launch_us": dk["us"]},
+        "kernels": kernels,
+        "e2e": {"value": replica_throughput(world, BATCH, e2e_steps, e2e_elapsed), "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
         "device_error_flags": dev_err,

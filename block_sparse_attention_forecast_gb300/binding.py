@@ -23,6 +23,7 @@ __all__ = [
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
+    "sparda_attend_and_score", "sparda_decode_prologue",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
@@ -96,6 +97,8 @@ def _load():
         "sparda_multihead_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
         "sparda_forecast_select_static": (I32, [SH, P, P, P, I32, P, P, P]),
         "sparda_attend_and_select": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, P, P, SZ, P, I32, P]),
+        "sparda_attend_and_score": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, SZ, P, I32, P]),
+        "sparda_decode_prologue": (I32, [SH, LY, P, P, P, SZ, P, P, P, P, I32, P, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -293,6 +296,25 @@ def sparda_attend_and_select(shape, layer, q, idx, cnt, out, ws_attn, ck_next, f
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(staging_k), _ptr(staging_v), _ptr(q), _ptr(idx),
         _ptr(cnt), _ptr(out), _ptr(ws_attn), ws_attn.numel(), _ptr(ck_next), _ptr(forecast_next), _ptr(idx_next),
         _ptr(cnt_next), _ptr(ws_sel), ws_sel.numel(), _ptr(seq_len), int(batch), _stream(stream)))
+
+
+def sparda_attend_and_score(shape, layer, q, idx, cnt, out, ws_attn, ck_next, forecast_next, ws_scores,
+                            seq_len, batch, staging_k=None, staging_v=None, stream=None):
+    _check("sparda_attend_and_score", lib.sparda_attend_and_score(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(staging_k), _ptr(staging_v), _ptr(q), _ptr(idx),
+        _ptr(cnt), _ptr(out), _ptr(ws_attn), ws_attn.numel(), _ptr(ck_next), _ptr(forecast_next), _ptr(ws_scores),
+        ws_scores.numel(), _ptr(seq_len), int(batch), _stream(stream)))
+
+
+def sparda_decode_prologue(shape, layer, k_new, v_new, seq_len, batch, ws_scores=None, idx=None, cnt=None,
+                           W_next=None, h=None, forecast_next=None, stream=None):
+    """Layer L's top-k (from ws_scores, if given), append, and forecast for layer L+1 (if
+    W_next is given) in one launch."""
+    hidden = int(W_next.shape[1]) if W_next is not None else 0
+    _check("sparda_decode_prologue", lib.sparda_decode_prologue(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(k_new), _ptr(v_new), _ptr(ws_scores),
+        ws_scores.numel() if ws_scores is not None else 0, _ptr(idx), _ptr(cnt), _ptr(W_next), _ptr(h), hidden,
+        _ptr(forecast_next), _ptr(seq_len), int(batch), _stream(stream)))
 
 
 def sparda_prefetch_blocks(shape, layer, idx, cnt, seq_len, batch, staging_k, staging_v,

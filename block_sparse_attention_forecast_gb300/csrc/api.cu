@@ -253,12 +253,15 @@ int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int3
 namespace {
 
 // Argument checks and kernel arguments of the selection call (shared by the standalone and
-// the fused entry points).
+// the fused entry points). With idx == cnt == nullptr only the block scores are wanted
+// (the top-k runs later, in the decode prologue).
 int32_t prepare_select(const sparda_shape* s, const void* ck, const void* forecast, const int32_t* seq_len,
-                       int32_t batch, int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, SelectArgs* out) {
+                       int32_t batch, int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, SelectArgs* out,
+                       bool scores_only = false) {
   SPARDA_TRY(shape_status(s));
   SPARDA_TRY(batch_status(s, batch));
-  if (!ck || !forecast || !seq_len || !idx || !cnt || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!ck || !forecast || !seq_len || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!scores_only && (!idx || !cnt)) return SPARDA_ERR_INVALID_ARG;
   if (!aligned(ck, 16) || !aligned(forecast, 16) || !aligned(ws, 16) || !aligned(idx, 4) ||
       !aligned(cnt, 4) || !aligned(seq_len, 4))
     return SPARDA_ERR_MISALIGNED;
@@ -270,7 +273,7 @@ int32_t prepare_select(const sparda_shape* s, const void* ck, const void* foreca
   *out = SelectArgs{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
                     seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
                     reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
-                    s->topk, select_chunk_blocks(nb_cap(s), bgc), 0};
+                    s->topk, select_chunk_blocks(nb_cap(s), bgc), 0, scores_only ? 0 : 1};
   return SPARDA_OK;
 }
 
@@ -352,6 +355,65 @@ int32_t sparda_attend_and_select(const sparda_shape* s, const sparda_layer_kv* L
   SPARDA_TRY(prepare_select(s, ck_next, forecast_next, seq_len, batch, idx_next, cnt_next, ws_sel, ws_sel_bytes,
                             &sa));
   launch_attend_and_select(a, sa, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_attend_and_score(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
+                                const void* staging_v, const void* q, const int32_t* idx, const int32_t* cnt,
+                                void* out, void* ws_attn, size_t ws_attn_bytes, const void* ck_next,
+                                const void* forecast_next, void* ws_scores, size_t ws_scores_bytes,
+                                const int32_t* seq_len, int32_t batch, void* stream) {
+  if (ws_scores == ws_attn) return SPARDA_ERR_INVALID_ARG;
+  AttnArgs a;
+  CUtensorMap mk, mv, hk, hv;
+  SPARDA_TRY(prepare_attn(s, L, staging_k, staging_v, q, idx, cnt, seq_len, batch, out, ws_attn, ws_attn_bytes,
+                          &a, &mk, &mv, &hk, &hv));
+  SelectArgs sa;
+  SPARDA_TRY(prepare_select(s, ck_next, forecast_next, seq_len, batch, nullptr, nullptr, ws_scores,
+                            ws_scores_bytes, &sa, true));
+  launch_attend_and_select(a, sa, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_decode_prologue(const sparda_shape* s, const sparda_layer_kv* L, const void* k_new,
+                               const void* v_new, const void* ws_scores, size_t ws_scores_bytes, int32_t* idx,
+                               int32_t* cnt, const void* W_next, const void* h, int32_t hidden,
+                               void* forecast_next, const int32_t* seq_len, int32_t batch, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  SPARDA_TRY(layer_status(L, true));
+  if (!k_new || !v_new || !seq_len) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(seq_len, 4)) return SPARDA_ERR_MISALIGNED;
+  if (ws_scores) {
+    if (!idx || !cnt) return SPARDA_ERR_INVALID_ARG;
+    if (!aligned(ws_scores, 16) || !aligned(idx, 4) || !aligned(cnt, 4)) return SPARDA_ERR_MISALIGNED;
+    if (ws_scores_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_SELECT))
+      return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (W_next) {
+    if (!h || !forecast_next) return SPARDA_ERR_INVALID_ARG;
+    if (hidden < 32 || hidden % 32 != 0) return SPARDA_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(W_next, 16) || !aligned(h, 16) || !aligned(forecast_next, 16)) return SPARDA_ERR_MISALIGNED;
+  }
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  PrologueArgs a{};
+  a.ap = AppendArgs{static_cast<__nv_bfloat16*>(L->k), static_cast<__nv_bfloat16*>(L->v),
+                    static_cast<__nv_bfloat16*>(L->ck), static_cast<__nv_bfloat16*>(L->hot_k),
+                    static_cast<__nv_bfloat16*>(L->hot_v), static_cast<const __nv_bfloat16*>(k_new),
+                    static_cast<const __nv_bfloat16*>(v_new), seq_len, err, s->n_groups, s->max_ctx,
+                    w_cap(s), L->on_host ? 1 : 0};
+  a.pj = ProjectArgs{static_cast<const __nv_bfloat16*>(W_next), static_cast<const __nv_bfloat16*>(h),
+                     static_cast<__nv_bfloat16*>(forecast_next), s->n_groups * kHeadDim, hidden, batch};
+  a.block_scores = ws_scores ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws_scores) +
+                                                              counters_bytes(s))
+                             : nullptr;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.topk = s->topk;
+  a.nb_cap = nb_cap(s);
+  a.bg_count = batch * s->n_groups;
+  launch_decode_prologue(a, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

@@ -112,8 +112,10 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         prefetch_tensormap(hv);
       }
     }
+    // the selection and the caches were written by the kernels before this one in the stream
+    // (the decode prologue's top-k and append)
+    grid_dep_wait();
     int it = 0;
-    bool waited = false;
     for (int base = u0; base < u1; base += 32) {
       // lane i prepares unit base + i
       const int u = base + lane;
@@ -140,11 +142,6 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         }
       }
       unsigned vmask = __ballot_sync(0xffffffffu, v);
-      // the caches were written by the kernel before this one in the stream (the append)
-      if (!waited) {
-        grid_dep_wait();
-        waited = true;
-      }
       while (vmask) {
         const int i = __ffs(vmask) - 1;
         vmask &= vmask - 1;

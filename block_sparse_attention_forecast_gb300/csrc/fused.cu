@@ -12,6 +12,9 @@
 namespace sparda {
 
 static_assert(kAttnThreads == kSelThreads, "both jobs run with the same CTA shape");
+// streamed-byte weight of an attention unit against a selection unit when splitting the SMs
+constexpr double kAttnWeightWithTopk = 1.1;
+constexpr double kAttnWeightScoresOnly = 2.3;
 constexpr int kFusedSmem = kAttnSmem > kSelSmem ? kAttnSmem : kSelSmem;
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
@@ -35,9 +38,12 @@ void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUte
   aa.n_units = bg_count * a.kslots;
   sa.n_units = bg_count * s.nb_cap;
   // split the SMs by streamed bytes: an attention unit is one K+V block (32 KiB), a selection
-  // unit one block's four windows of compressed keys (1 KiB); the attention CTAs also merge
-  // split groups, weighted in as about 10% more work per byte
-  const double wa = 1.1 * (double)aa.n_units * (2.0 * kBlockBytes);
+  // unit one block's four windows of compressed keys (1 KiB). An attention CTA streams fewer
+  // bytes per microsecond than a selection CTA (it merges split groups and computes more per
+  // byte); a selection CTA that also runs top-k tails streams fewer. The weights are measured
+  // at 128K context, batch 16.
+  const double w_attn = sa.do_topk ? kAttnWeightWithTopk : kAttnWeightScoresOnly;
+  const double wa = w_attn * (double)aa.n_units * (2.0 * kBlockBytes);
   const double ws = (double)sa.n_units * (kWinPerBlock * kRowBytes);
   const int sms = sm_count();
   int n_attn = (int)(sms * wa / (wa + ws) + 0.5);

@@ -50,6 +50,7 @@ struct SelectArgs {
   int* err;
   int G, W_cap, max_ctx, nb_cap, topk, chunk_blocks;
   int n_units;                   // B*G*nb_cap, set by the launcher
+  int do_topk = 1;               // 0: leave the block scores for a later top-k (decode prologue)
 };
 
 struct AttnArgs {
@@ -102,6 +103,18 @@ void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s);
 void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUtensorMap& mk,
                               const CUtensorMap& mv, const CUtensorMap& hk, const CUtensorMap& hv,
                               int bg_count, cudaStream_t st);
+// One launch of a layer's decode prologue (prologue.cu): the top-k of the layer's block
+// scores, the append of its token and the forecast projection for the next layer.
+struct PrologueArgs {
+  AppendArgs ap;
+  ProjectArgs pj;                // pj.W == nullptr: no projection
+  const float* block_scores;     // [B*G, nb_cap]; nullptr: no top-k
+  int32_t* idx;                  // [B, G, topk+2]
+  int32_t* cnt;                  // [B, G]
+  int topk, nb_cap, bg_count;
+  int n_proj, n_topk;            // CTAs of the projection and top-k roles (multiples of 4)
+};
+void launch_decode_prologue(const PrologueArgs& a, cudaStream_t s);
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);
 int multihead_tiles(int w_cap);
 

@@ -1,0 +1,78 @@
+// A layer's decode prologue: three small, independent jobs of one layer in one launch.
+//
+//   * the top-k of the layer's block scores, which the previous layer's launch computed
+//     while it attended (bittide thread: layer L's forecast selects layer L+1's blocks
+//     while layer L still computes), giving the blocks this layer attends;
+//   * the append of this layer's token key/value and the compressed key of a window that
+//     the token completes (techwalker section 四);
+//   * the forecast projection of this layer's hidden state for the next layer (techwalker
+//     section 二).
+//
+// Each alone is a launch of a few microseconds that leaves most of the GPU idle; together they
+// cost one launch. The grid is cut into role ranges, each a whole number of 4-CTA clusters:
+// projection tiles (the four K-quarters of a tile are one cluster, reduced through distributed
+// shared memory), then one top-k CTA per (sequence, group), then append CTAs of four
+// (sequence, group) pairs each. Every CTA first lets the next launch in the stream begin
+// (programmatic dependent launch: the attention kernel's producers and the selector's loads
+// start early) and then waits for the previous launch to complete.
+#include "append_body.cuh"
+#include "project_body.cuh"
+#include "topk.cuh"
+
+namespace sparda {
+
+static_assert(kTopkThreads == kProjThreads, "the roles share one CTA shape");
+constexpr int kPrologueThreads = kProjThreads;     // 256
+constexpr int kAppendPerCta = kPrologueThreads / 64;
+
+union PrologueShared {
+  ProjShared pj;
+  TopkShared tk;
+};
+
+__global__ void __cluster_dims__(kProjSplit, 1, 1) __launch_bounds__(kPrologueThreads)
+    decode_prologue_kernel(const PrologueArgs a) {
+  __shared__ PrologueShared sh;
+  grid_dep_launch();
+  grid_dep_wait();
+  int c = blockIdx.x;
+  if (c < a.n_proj) {
+    // cluster c / 4 is tile (row tile, sequence tile); its rank is the K-quarter
+    const int tile = c / kProjSplit, n_tiles = a.pj.rows / 8;
+    project_cta(a.pj, tile % n_tiles, c % kProjSplit, tile / n_tiles, sh.pj);
+    return;
+  }
+  c -= a.n_proj;
+  if (c < a.n_topk) {
+    if (c < a.bg_count) {
+      const int T = a.ap.seq_len[c / a.ap.G];
+      topk_select(a.block_scores + (size_t)c * a.nb_cap, a.idx + (size_t)c * (a.topk + 2), a.cnt + c,
+                  a.topk, a.ap.max_ctx, T, sh.tk);
+    }
+    return;
+  }
+  c -= a.n_topk;
+  const int bg = c * kAppendPerCta + (int)threadIdx.x / 64;
+  if (bg < a.bg_count) append_token(a.ap, bg, threadIdx.x % 64);
+}
+
+void launch_decode_prologue(const PrologueArgs& args, cudaStream_t s) {
+  PrologueArgs a = args;
+  auto round4 = [](int x) { return (x + kProjSplit - 1) / kProjSplit * kProjSplit; };
+  a.n_proj = a.pj.W ? (a.pj.rows / 8) * kProjSplit * ((a.pj.batch + 15) / 16) : 0;
+  a.n_topk = a.block_scores ? round4(a.bg_count) : 0;
+  const int n_append = round4((a.bg_count + kAppendPerCta - 1) / kAppendPerCta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_proj + a.n_topk + n_append);
+  cfg.blockDim = dim3(kPrologueThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, decode_prologue_kernel, a);
+}
+
+}  // namespace sparda

@@ -219,6 +219,7 @@ __device__ __forceinline__ void sel_cta(const SelectArgs& a, int cta, int grid) 
       }
       ++nbuf;                                       // alternate buffers: no second barrier
     }
+    if (!a.do_topk) continue;        // the top-k runs in a later launch (decode prologue)
     // this CTA's part of the group is done: count it; the last covering CTA selects
     const long long first_u = (long long)bg * a.nb_cap, last_u = first_u + a.nb_cap - 1;
     const int n_cover = sel_cta_of_unit(last_u, grid, U) - sel_cta_of_unit(first_u, grid, U) + 1;

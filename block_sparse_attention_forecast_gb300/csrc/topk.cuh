@@ -53,6 +53,7 @@ struct TopkShared {
   int n_list;
   float lv[kMaxList];
   int lj[kMaxList];
+  int lr[kMaxList];                    // exact rank of each listed candidate
   unsigned char flag[kMaxBlocksPerSeq];
 };
 
@@ -65,21 +66,25 @@ __device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
 
 // Top-k of one (sequence, group) by 256 threads (threads 0-255 of the CTA, synchronised with
 // named barrier 1), from the block scores S[0 .. nb) in global memory. Writes idx[0 .. topk+2)
-// (sorted, -1 padded) and *cnt_out. Fast path: min/max of the candidate scores, a
-// 256-bucket histogram over that range, the bucket that holds the k-th score, then exact
-// ranks (score descending, block ascending) among the candidates at or above that bucket --
-// a few dozen for real score distributions. If more than kMaxList candidates share those
-// buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
-// takes over. Either way the result is exact and ties go to the lower block index.
+// (block 0, the chosen blocks ascending, the tail block; -1 padded) and *cnt_out.
+//
+// Thread t holds the scores of blocks t, t + 256, t + 512, ... (each warp load is one
+// contiguous 128-byte line). Fast path: min/max of the candidate scores; a 256-bucket
+// histogram over that range (shared-memory atomics); the bucket that holds the k-th score,
+// found by a scan from the top; the candidates at or above that bucket -- a few dozen for real
+// score distributions -- listed in shared memory with one atomic per warp; their exact ranks
+// (score descending, block ascending) by pairwise comparison; and the output position of each
+// chosen block by counting the chosen blocks below it. If more than kMaxList candidates share
+// those buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
+// takes over and the output is assembled from per-block flags. Either way the result is exact
+// and ties go to the lower block index.
 static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_out, int topk, int max_ctx,
-                            int T, TopkShared& sh) {
+                                   int T, TopkShared& sh) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int kslots = topk + 2;
   const bool valid = (T >= 1 && T <= max_ctx);
   const int tb = valid ? (T - 1) / kBlock : -1;
   const int nb = tb + 1;
-  const int per = (nb + kTopkThreads - 1) / kTopkThreads;
-  const int jb = t * per;
   const int n_cand = max(0, tb - 1);
   const int k_eff = min(topk, n_cand);
 
@@ -87,17 +92,12 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
   bool isc[kKeysPerThread];
 #pragma unroll
   for (int e = 0; e < kKeysPerThread; ++e) {
-    const int j = jb + e;
-    isc[e] = e < per && j >= 1 && j < tb;
+    const int j = e * kTopkThreads + t;
+    isc[e] = j >= 1 && j < tb;
     v[e] = isc[e] ? __ldcg(S + j) : 0.f;
-    if (e < per && j < nb) sh.flag[j] = (j == 0 || j == tb) ? 1 : 0;   // the forced blocks
   }
 
-  if (k_eff == n_cand) {
-#pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e)
-      if (isc[e]) sh.flag[jb + e] = 1;
-  } else if (k_eff > 0) {
+  if (k_eff > 0 && k_eff < n_cand) {
     float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
     for (int e = 0; e < kKeysPerThread; ++e)
@@ -126,12 +126,8 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     bool fast = hi > lo && isfinite(lo) && isfinite(hi) && isfinite(scale);   // CTA-uniform
     if (fast) {
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
-        if (e >= per) break;                       // per is the same in every thread
-        const unsigned d = isc[e] ? (unsigned)score_bucket(v[e], lo, scale) : 256u;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (isc[e] && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
-      }
+      for (int e = 0; e < kKeysPerThread; ++e)
+        if (isc[e]) atomicAdd(&sh.hist[score_bucket(v[e], lo, scale)], 1u);
       topk_sync();
       const int hv = (int)sh.hist[255 - t];      // thread t looks at bucket 255 - t
       int tot;
@@ -145,99 +141,134 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     }
     if (fast) {
       const int bstar = sh.bstar;
+      // list the candidates at or above bucket bstar: one shared atomic per warp
+      int mine = 0;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
-        if (e >= per) break;                       // per is the same in every thread
-        const bool in = isc[e] && score_bucket(v[e], lo, scale) >= bstar;
-        const unsigned bal = __ballot_sync(0xffffffffu, in);
-        int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&sh.n_list, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (in) {
-          const int p = base + __popc(bal & ((1u << lane) - 1u));
-          sh.lv[p] = v[e];
-          sh.lj[p] = jb + e;
-        }
+      for (int e = 0; e < kKeysPerThread; ++e)
+        mine += (isc[e] && score_bucket(v[e], lo, scale) >= bstar) ? 1 : 0;
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
       }
+      int base = 0;
+      if (lane == 31 && incl > 0) base = atomicAdd(&sh.n_list, incl);
+      int p = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e)
+        if (isc[e] && score_bucket(v[e], lo, scale) >= bstar) {
+          sh.lv[p] = v[e];
+          sh.lj[p] = e * kTopkThreads + t;
+          ++p;
+        }
       topk_sync();
-      // exact rank of each listed candidate (score descending, block ascending): `split`
-      // threads share one candidate, each scanning a slice of the list
+      // exact rank of each listed candidate: `split` threads share one candidate, each
+      // scanning a slice of the list
       const int c = sh.n_list;
       const int split = c <= 32 ? 8 : (c <= 64 ? 4 : (c <= 128 ? 2 : 1));
       for (int i0 = 0; i0 < c * split; i0 += kTopkThreads) {
         const int q = i0 + t;
         const int i = q / split, part = q % split;
         int rank = 0;
-        int ji = 0;
         if (i < c) {
           const float vi = sh.lv[i];
-          ji = sh.lj[i];
+          const int ji = sh.lj[i];
           for (int m = part; m < c; m += split) {
             const float vm = sh.lv[m];
             rank += (vm > vi) || (vm == vi && sh.lj[m] < ji);
           }
         }
         for (int o = 1; o < split; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        if (i < c && part == 0 && rank < k_eff) sh.flag[ji] = 1;
+        if (i < c && part == 0) sh.lr[i] = rank;
       }
-    } else {
-      // radix select on order-preserving keys
-      uint32_t key[kKeysPerThread];
-#pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
-      uint32_t prefix = 0u, mask = 0u;
-      int krem = k_eff;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        sh.hist[t] = 0u;
-        topk_sync();
-#pragma unroll
-        for (int e = 0; e < kKeysPerThread; ++e) {
-          const bool in = key[e] != 0u && (key[e] & mask) == prefix;
-          const unsigned d = in ? (key[e] >> shift) & 255u : 256u;
-          const unsigned peers = __match_any_sync(0xffffffffu, d);
-          if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (unsigned)__popc(peers));
+      topk_sync();
+      // output: block 0, the chosen blocks in ascending order, the tail block (tb >= 2 here)
+      for (int i0 = 0; i0 < c * split; i0 += kTopkThreads) {
+        const int q = i0 + t;
+        const int i = q / split, part = q % split;
+        int pos = 0;
+        bool chosen = false;
+        int ji = 0;
+        if (i < c) {
+          chosen = sh.lr[i] < k_eff;
+          ji = sh.lj[i];
+          if (chosen)
+            for (int m = part; m < c; m += split) pos += (sh.lr[m] < k_eff && sh.lj[m] < ji);
         }
-        topk_sync();
-        const int hv = (int)sh.hist[255 - t];
-        int tot;
-        const int incl = topk_scan(hv, sh.warp_tot, &tot);
-        if (incl - hv < krem && incl >= krem) {
-          sh.prefix = prefix | ((uint32_t)(255 - t) << shift);
-          sh.krem = krem - (incl - hv);
-        }
-        topk_sync();
-        prefix = sh.prefix;
-        krem = sh.krem;
-        mask |= 255u << shift;
+        for (int o = 1; o < split; o <<= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
+        if (chosen && part == 0) idx[1 + pos] = ji;
       }
-      int my_eq = 0;
+      if (t == 0) {
+        idx[0] = 0;
+        idx[k_eff + 1] = tb;
+        *cnt_out = k_eff + 2;
+      }
+      for (int s = k_eff + 2 + t; s < kslots; s += kTopkThreads) idx[s] = -1;
+      return;
+    }
+  }
+  // -------------------------------------------------------------- flag-based paths
+  // every candidate chosen (k_eff == n_cand), or the radix select for near-constant scores
+  for (int j = t; j < nb; j += kTopkThreads) sh.flag[j] = (j == 0 || j == tb) ? 1 : 0;   // forced blocks
+  topk_sync();
+  if (k_eff == n_cand) {
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) my_eq += (key[e] != 0u && key[e] == prefix);
-      int dummy;
-      int rank = topk_scan(my_eq, sh.warp_tot, &dummy) - my_eq;
+    for (int e = 0; e < kKeysPerThread; ++e)
+      if (isc[e]) sh.flag[e * kTopkThreads + t] = 1;
+  } else if (k_eff > 0) {
+    uint32_t key[kKeysPerThread];
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
+    uint32_t prefix = 0u, mask = 0u;
+    int krem = k_eff;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      sh.hist[t] = 0u;
+      topk_sync();
 #pragma unroll
       for (int e = 0; e < kKeysPerThread; ++e) {
-        if (key[e] == 0u) continue;
-        if (key[e] > prefix) {
-          sh.flag[jb + e] = 1;
-        } else if (key[e] == prefix) {
-          if (rank < krem) sh.flag[jb + e] = 1;
-          ++rank;
-        }
+        const bool in = key[e] != 0u && (key[e] & mask) == prefix;
+        if (in) atomicAdd(&sh.hist[(key[e] >> shift) & 255u], 1u);
       }
+      topk_sync();
+      const int hv = (int)sh.hist[255 - t];
+      int tot;
+      const int incl = topk_scan(hv, sh.warp_tot, &tot);
+      if (incl - hv < krem && incl >= krem) {
+        sh.prefix = prefix | ((uint32_t)(255 - t) << shift);
+        sh.krem = krem - (incl - hv);
+      }
+      topk_sync();
+      prefix = sh.prefix;
+      krem = sh.krem;
+      mask |= 255u << shift;
+    }
+    // keys above the k-th key are chosen; of the keys equal to it, the krem of lowest block
+    // index. Thread t's equal keys sit at blocks t, t + 256, ...: count, per e, the equal keys
+    // of all threads at earlier e or, at the same e, lower t.
+    int eq_before = 0;                    // equal keys at blocks below this thread's current one
+#pragma unroll
+    for (int e = 0; e < kKeysPerThread; ++e) {
+      const bool eq = key[e] != 0u && key[e] == prefix;
+      int tot_e;
+      const int incl_e = topk_scan(eq ? 1 : 0, sh.warp_tot, &tot_e);
+      if (key[e] != 0u && key[e] > prefix) sh.flag[e * kTopkThreads + t] = 1;
+      if (eq && eq_before + incl_e - 1 < krem) sh.flag[e * kTopkThreads + t] = 1;
+      eq_before += tot_e;
     }
   }
   topk_sync();
-  // the selected blocks in ascending order
+  // the selected blocks in ascending order: thread t scans the contiguous range of blocks
+  // [t*per, t*per + per)
+  const int per = (nb + kTopkThreads - 1) / kTopkThreads;
+  const int jb = t * per;
   int my_sel = 0;
-#pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e)
-    if (e < per && jb + e < nb) my_sel += sh.flag[jb + e];
+  for (int e = 0; e < per; ++e)
+    if (jb + e < nb) my_sel += sh.flag[jb + e];
   int total;
   int pos = topk_scan(my_sel, sh.warp_tot, &total) - my_sel;
-#pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e)
-    if (e < per && jb + e < nb && sh.flag[jb + e] && pos < kslots) idx[pos++] = jb + e;
+  for (int e = 0; e < per; ++e)
+    if (jb + e < nb && sh.flag[jb + e] && pos < kslots) idx[pos++] = jb + e;
   for (int s = total + t; s < kslots; s += kTopkThreads) idx[s] = -1;
   if (t == 0) *cnt_out = min(total, kslots);
 }

@@ -2,19 +2,26 @@
 
 Per layer L (bittide thread: layer L's forecast predicts layer L+1's blocks, which layer L+1
 then attends with its own queries; techwalker section 三: layer 0 has no earlier forecast
-and selects its own blocks with a same-layer forecast):
+and selects its own blocks with a same-layer forecast), three ways to launch the same work:
 
-    main stream   append_kv(L) ............................ sparse_decode_attn(L, idx[L])
-    side stream        forecast_project(W_next[L], h[L]) -> forecast_select(ck[L+1]) -> idx[L+1]
-    (join before layer L+1)
+  "pipelined" (resident stacks, the default): two launches per layer on one stream
+      decode_prologue(L)   top-k of layer L's block scores -> idx[L]; append(L);
+                           forecast f[L+1] = W_next[L] h[L]
+      attend_and_score(L)  attention(L, idx[L]) beside the block scores of layer L+1
+  "fused": three launches per layer on one stream
+      forecast_project(L+1); append(L); attend_and_select(L, L+1) (attention beside the
+      whole selection of layer L+1, top-k included)
+  "streams" (always used when a layer is offloaded): one kernel per job, two or three streams
+      main stream   append_kv(L) ............................ sparse_decode_attn(L, idx[L])
+      side stream        forecast_project(W_next[L], h[L]) -> forecast_select(ck[L+1]) -> idx[L+1]
+      (join before layer L+1)
+    Offloaded layers add a third stream that gathers layer L+1's selected blocks from pinned
+    host memory as soon as they are known, into one of two staging buffers; layer L+1's
+    attention waits for that gather.
 
-The forecast branch of layer L only needs layer L's hidden state, so its selection for
-layer L+1 runs concurrently with layer L's attention. Offloaded layers add a third stream
-that gathers layer L+1's selected blocks from pinned host memory as soon as they are known,
-into one of two staging buffers; layer L+1's attention waits for that gather.
-
-Everything here is host-side orchestration of libsparda calls (no arithmetic); the whole step
-can be captured once into a CUDA graph and replayed.
+Every mode computes the same results bit for bit. Everything here is host-side orchestration
+of libsparda calls (no arithmetic); the whole step can be captured once into a CUDA graph and
+replayed.
 """
 from __future__ import annotations
 
@@ -33,8 +40,10 @@ class DecodeStack:
     out. idx[L] / cnt[L] hold the blocks layer L attends at the current step.
     """
 
+    MODES = ("pipelined", "fused", "streams")
+
     def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
-                 overlap=True, advance=False, after_attention=None, fused=True):
+                 overlap=True, advance=False, after_attention=None, mode="pipelined"):
         self.shape = shape
         self.layers = layers
         self.n_layers = len(layers)
@@ -50,10 +59,11 @@ class DecodeStack:
         self.after_attention = after_attention
         assert not layers[0].on_host, "layer 0 stays resident"
         self.any_offload = any(l.on_host for l in layers)
-        # Resident stacks run layer L's attention and layer L+1's selection as one launch
-        # (sparda_attend_and_select). Offloaded stacks keep them apart: layer L+1's selection
-        # must finish early so that its gather overlaps layer L.
-        self.fused = fused and not self.any_offload
+        # Resident stacks run layer L's attention and layer L+1's selection in one launch.
+        # Offloaded stacks keep them apart: layer L+1's selection must finish early so that
+        # its gather overlaps layer L.
+        assert mode in self.MODES, mode
+        self.mode = "streams" if self.any_offload else mode
         G, H, d = shape.n_groups, shape.heads_per_group, shape.head_dim
         hidden = W_self0.shape[1]
         n, B = self.n_layers, batch
@@ -69,7 +79,7 @@ class DecodeStack:
         self.seq_len = torch.ones(B, dtype=torch.int32, device=device)
         self.ws_sel = sb.workspace(shape, B, sb.WS_SELECT, device)
         self.ws_attn = sb.workspace(shape, B, sb.WS_ATTN, device)
-        self.ws_sel2 = sb.workspace(shape, B, sb.WS_SELECT, device) if self.fused else None
+        self.ws_sel2 = sb.workspace(shape, B, sb.WS_SELECT, device) if self.mode != "streams" else None
         if self.any_offload:
             st = (shape.max_batch, G, shape.kslots, shape.block, d)
             self.stage_k = [torch.zeros(st, **bf) for _ in range(2)]
@@ -83,7 +93,9 @@ class DecodeStack:
     # ------------------------------------------------------------------ one step
     def enqueue(self):
         """Enqueue one decode step on the current stream (plus the side streams)."""
-        if self.fused:
+        if self.mode == "pipelined":
+            return self._enqueue_pipelined()
+        if self.mode == "fused":
             return self._enqueue_fused()
         sh, B = self.shape, self.batch
         main = torch.cuda.current_stream()
@@ -141,6 +153,36 @@ class DecodeStack:
         if self.advance:
             self.seq_len.add_(1)
 
+    def _enqueue_pipelined(self):
+        """Resident stack, one stream, two launches per layer: layer L's prologue (its top-k,
+        its append, the forecast for layer L+1), then layer L's attention beside the block
+        scores of layer L+1. Block scores alternate between two workspaces."""
+        sh, B, n = self.shape, self.batch, self.n_layers
+        main = torch.cuda.current_stream()
+        scores = (self.ws_sel, self.ws_sel2)
+        sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
+        sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
+                                  self.idx[0], self.cnt[0], self.ws_sel, stream=main)
+        for L in range(n):
+            layer = self.layers[L]
+            last = L + 1 == n
+            sb.sparda_decode_prologue(
+                sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B,
+                ws_scores=scores[L % 2] if L > 0 else None, idx=self.idx[L], cnt=self.cnt[L],
+                W_next=None if last else self.W_next[L], h=self.h[L],
+                forecast_next=None if last else self.f[L + 1].view(B, -1), stream=main)
+            if last:
+                sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
+                                             self.out[L], self.ws_attn, stream=main)
+            else:
+                sb.sparda_attend_and_score(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.out[L],
+                                           self.ws_attn, self.layers[L + 1].ck, self.f[L + 1],
+                                           scores[(L + 1) % 2], self.seq_len, B, stream=main)
+            if self.after_attention is not None:
+                self.after_attention(L)
+        if self.advance:
+            self.seq_len.add_(1)
+
     def _enqueue_fused(self):
         """Resident stack, one stream: per layer the forecast projection for layer L+1, the
         append of layer L, then layer L's attention together with layer L+1's selection."""
@@ -190,13 +232,16 @@ class DecodeStack:
             self.enqueue()
 
     def kernel_launches_per_step(self):
-        """Kernels of libsparda one step launches. Fused: layer 0's own projection and
-        selection, then per layer an append plus (all but the last layer) a projection and an
-        attend-and-select, the last layer's attention alone. Unfused: per layer append and
-        attention, per layer but the last a projection and a selection, one gather per
-        offloaded layer."""
+        """Kernels of libsparda one step launches. All modes start with layer 0's own
+        projection and selection. Pipelined: then per layer a prologue, per layer but the
+        last an attend-and-score, the last layer's attention alone. Fused: per layer an
+        append, per layer but the last a projection and an attend-and-select, the last
+        layer's attention. Streams: per layer append and attention, per layer but the last a
+        projection and a selection, one gather per offloaded layer."""
         n = self.n_layers
-        if self.fused:
+        if self.mode == "pipelined":
+            return 2 + n + (n - 1) + 1
+        if self.mode == "fused":
             return 2 + n + 2 * (n - 1) + 1
         gathers = sum(1 for l in self.layers[1:] if l.on_host)
         return 2 + n * 2 + (n - 1) * 2 + gathers

@@ -240,6 +240,57 @@ int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_k
                                  int32_t batch, void* stream);
 
 /*
+ * The decode step as two launches per layer (a layer-pipelined split of the same work):
+ *
+ *   sparda_decode_prologue(L):   top-k of layer L's block scores -> idx[L], cnt[L]
+ *                                append of layer L's token (as sparda_append_kv)
+ *                                forecast for layer L+1 (as sparda_forecast_project)
+ *   sparda_attend_and_score(L):  layer L's attention (as sparda_sparse_decode_attn) and the
+ *                                block scores of layer L+1 (the selector's scoring and
+ *                                max-pool, without its top-k)
+ *
+ * Under lookahead layer L's forecast scores layer L+1's blocks while layer L attends
+ * (bittide thread; techwalker section 二); the top-k that turns those scores into layer
+ * L+1's blocks only has to finish before layer L+1 attends, so it runs in layer L+1's
+ * prologue beside that layer's append and projection instead of as a tail of layer L's
+ * launch. Results are exactly those of the one-call-per-step entry points.
+ */
+
+/*
+ * sparda_attend_and_score -- as sparda_attend_and_select, except that the selection half
+ * stops after the block scores: for each (b, g) of layer L+1, S[j] (float32, the max-pooled
+ * forecast scores, j < (T-1)/64 + 1) is left in ws_scores (a SPARDA_WS_SELECT workspace),
+ * for sparda_decode_prologue of layer L+1 to select from. ws_scores must differ from
+ * ws_attn (SPARDA_ERR_INVALID_ARG otherwise).
+ */
+int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv* layer,
+                                const void* staging_k, const void* staging_v, const void* q,
+                                const int32_t* idx, const int32_t* cnt, void* out, void* ws_attn,
+                                size_t ws_attn_bytes, const void* ck_next, const void* forecast_next,
+                                void* ws_scores, size_t ws_scores_bytes, const int32_t* seq_len,
+                                int32_t batch, void* stream);
+
+/*
+ * sparda_decode_prologue -- the small per-layer jobs of layer L in one launch:
+ *   - if ws_scores != NULL: the top-k of the block scores that sparda_attend_and_score left
+ *     there for this layer, written to idx / cnt exactly as sparda_forecast_select writes
+ *     them (block 0, the tail block and the topk best others; ties to the lower block);
+ *   - the append of k_new / v_new (device bf16 [B, G, d]) to `layer`, exactly as
+ *     sparda_append_kv;
+ *   - if W_next != NULL: forecast_next = bf16(W_next . h) for layer L+1, exactly as
+ *     sparda_forecast_project with rows = G*d (W_next: device bf16 [G*d, hidden] row-major,
+ *     h: device bf16 [B, hidden], forecast_next: device bf16 [B, G, d]; hidden a multiple of
+ *     32).
+ * The three jobs read and write disjoint buffers. The launch waits for the previous kernel in
+ * the stream before any of them starts. Errors: as the three separate calls.
+ */
+int32_t sparda_decode_prologue(const sparda_shape* shape, const sparda_layer_kv* layer,
+                               const void* k_new, const void* v_new, const void* ws_scores,
+                               size_t ws_scores_bytes, int32_t* idx, int32_t* cnt, const void* W_next,
+                               const void* h, int32_t hidden, void* forecast_next,
+                               const int32_t* seq_len, int32_t batch, void* stream);
+
+/*
  * sparda_prefetch_blocks -- the gather that hides the host-offload copy (bittide thread:
  * the next layer's blocks are fetched on a separate CUDA stream while the current layer
  * computes; techwalker §三: a persistent kernel with a few copy CTAs reads host memory

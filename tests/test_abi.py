@@ -68,3 +68,27 @@ def test_bad_arguments_are_rejected_before_any_launch():
     offl = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, None, None, 1, 0)
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(offl), fake, fake, fake, 1, fake, fake, 0, None) == sb.ERR_INVALID_ARG
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(resident), fake, fake, fake, 1, fake, fake, -1, None) == sb.ERR_INVALID_ARG
+
+
+def test_pipelined_entries_reject_bad_arguments():
+    s = sb.Shape(max_batch=2, max_ctx=4096)
+    sh = ctypes.byref(s.c())
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    odd = P((1 << 20) + 8)
+    resident = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, None, None, 0, 0)
+    L = ctypes.byref(resident)
+    prologue = sb.lib.sparda_decode_prologue
+    # block scores to select from, but nowhere to write the selection
+    assert prologue(sh, L, fake, fake, fake, 1 << 24, None, None, None, None, 0, None, fake, 1, None) == sb.ERR_INVALID_ARG
+    # a score workspace too small for the batch
+    assert prologue(sh, L, fake, fake, fake, 16, fake, fake, None, None, 0, None, fake, 1, None) == sb.ERR_WORKSPACE_TOO_SMALL
+    # a projection whose hidden size is not a multiple of 32, or without its input
+    assert prologue(sh, L, fake, fake, None, 0, None, None, fake, fake, 100, fake, fake, 1, None) == sb.ERR_UNSUPPORTED_SHAPE
+    assert prologue(sh, L, fake, fake, None, 0, None, None, fake, None, 4096, fake, fake, 1, None) == sb.ERR_INVALID_ARG
+    assert prologue(sh, L, odd, fake, None, 0, None, None, None, None, 0, None, fake, 1, None) == sb.ERR_MISALIGNED
+    assert prologue(sh, L, fake, fake, None, 0, None, None, None, None, 0, None, fake, 3, None) == sb.ERR_INVALID_ARG
+    # the score workspace may not be the attention workspace
+    score = sb.lib.sparda_attend_and_score
+    assert score(sh, L, None, None, fake, fake, fake, fake, fake, 1 << 30, fake, fake, fake, 1 << 30, fake, 1,
+                 None) == sb.ERR_INVALID_ARG

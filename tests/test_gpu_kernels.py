@@ -316,3 +316,98 @@ def test_multihead_with_identical_queries_selects_like_the_forecast(sb):
         for g in range(2):
             _, S1 = O.forecast_select_one(to64(K[b, g]), to64(f[b, g]), T, k, return_scores=True)
             check_selection(idx[b, g].numpy(), cnt[b, g].item(), S1, T, k)
+
+
+# ------------------------------------------------------------------ decode prologue
+def test_decode_prologue_equals_its_three_calls(sb):
+    # the top-k of block scores, the append and the forecast projection in one launch give
+    # exactly what the selector, sparda_append_kv and sparda_forecast_project give
+    T_list, k, max_ctx, hidden = [4096, 3001, 130, 2049], 8, 4096, 512
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 71, 0)
+    V = synth.normal_bf16((B, 2, max_ctx, 128), 71, 1)
+    f = synth.normal_bf16((B, 2, 128), 71, 2).cuda()
+    kn = synth.normal_bf16((B, 2, 128), 71, 3).cuda()
+    vn = synth.normal_bf16((B, 2, 128), 71, 4).cuda()
+    W = synth.normal_bf16((256, hidden), 71, 5, std=0.02).cuda()
+    h = synth.normal_bf16((B, hidden), 71, 6).cuda()
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+
+    def fresh():
+        layer = sb.LayerKV.empty(shape)
+        layer.k.copy_(K.cuda())
+        layer.v.copy_(V.cuda())
+        sb.sparda_compress_keys(shape, layer, seq - 1, B)
+        return layer
+
+    def slots():
+        return (torch.full((B, 2, k + 2), -9, dtype=torch.int32, device="cuda"),
+                torch.full((B, 2), -9, dtype=torch.int32, device="cuda"))
+
+    la, lb = fresh(), fresh()
+    ws = sb.workspace(shape, B, sb.WS_SELECT)
+    idx_a, cnt_a = slots()
+    sb.sparda_forecast_select(shape, la.ck, f, seq, B, idx_a, cnt_a, ws)   # leaves the block scores in ws
+    sb.sparda_append_kv(shape, la, kn, vn, seq, B)
+    f_a = torch.empty((B, 256), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_forecast_project(W, h, f_a)
+    idx_b, cnt_b = slots()
+    f_b = torch.empty((B, 256), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_decode_prologue(shape, lb, kn, vn, seq, B, ws_scores=ws, idx=idx_b, cnt=cnt_b, W_next=W, h=h,
+                              forecast_next=f_b)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_a, idx_b) and torch.equal(cnt_a, cnt_b)
+    assert torch.equal(f_a, f_b)
+    assert torch.equal(la.k, lb.k) and torch.equal(la.v, lb.v) and torch.equal(la.ck, lb.ck)
+    # the append alone (no scores, no projection) leaves the selection untouched
+    idx_c, cnt_c = slots()
+    sb.sparda_decode_prologue(shape, fresh(), kn, vn, seq, B, idx=idx_c, cnt=cnt_c)
+    torch.cuda.synchronize()
+    assert (idx_c == -9).all() and (cnt_c == -9).all()
+    _no_device_error(sb)
+
+
+def test_append_window_means_round_exactly(sb):
+    # The window that token 31 completes, built so that the exact means hit the cases that a
+    # slip in the append's exact summation and rounding would get wrong: halfway cases that
+    # round down or up to even, means of mixed signs and magnitudes, all-zero and negative
+    # zero windows, keys below 2^-40 and of 2^11 or more (summed another way), sums that
+    # carry into the next binade. Compared bit for bit with the oracle's compressed key.
+    T = 32
+    K = synth.normal_bf16((1, 2, 256, 128), 81, 0).double().numpy()
+    W = np.zeros((32, 128))
+    cases = [
+        {0: 32.0, 1: 0.125},                  # mean 1 + 2^-8: halfway, rounds down to even 1.0
+        {0: 32.0, 1: 0.25, 2: 0.125},         # mean 1 + 3*2^-8: halfway, rounds up to 1 + 2^-6
+        {0: -32.0, 1: -0.125},                # negative halfway
+        {0: 32.0, 1: 0.125, 2: 2.0 ** -30},   # just above halfway: rounds up
+        {0: 63.75, 1: 0.125, 2: 0.0625},      # mean 2 - 2^-9 rounds up to 2.0: carries into the exponent
+        {0: 4096.0, 1: 1.0},                  # a key of 2^12: the float64 path
+        {0: 3008.0, 1: -2992.0, 2: 0.5},      # large cancelling keys: the float64 path
+        {0: 2.0 ** -41, 1: 2.0 ** -20},       # a key below 2^-40: the float64 path
+        {0: 2.0 ** -40, 1: 2.0 ** -33},       # the smallest magnitudes the integer path takes
+        {0: 1.0, 1: -1.0},                    # exact zero
+    ]
+    for d, c in enumerate(cases):
+        for r, x in c.items():
+            W[r, d] = x
+    W[:, len(cases)] = -0.0                   # a window of negative zeros
+    W[:, len(cases) + 1:] = K[0, 0, :32, len(cases) + 1:]
+    Kw = torch.from_numpy(W).to(torch.bfloat16)
+    assert torch.equal(Kw.double(), torch.from_numpy(W)), "the crafted keys must be bf16 values"
+    shape = sb.Shape(max_ctx=256, max_batch=1, topk=8)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.zero_()
+    layer.v.zero_()
+    for g in range(2):
+        layer.k[0, g, :31] = Kw[:31].cuda()
+    seq = torch.tensor([T], dtype=torch.int32, device="cuda")
+    kn = torch.stack([Kw[31], Kw[31]]).view(1, 2, 128).cuda()
+    sb.sparda_append_kv(shape, layer, kn, kn, seq, 1)
+    torch.cuda.synchronize()
+    got = layer.ck[0, :, 0].cpu().view(torch.int16)
+    want = torch.from_numpy(O.compress_keys(Kw.double().numpy(), 1)[0]).to(torch.bfloat16).view(torch.int16)
+    for g in range(2):
+        assert torch.equal(got[g], want), (g, (got[g] != want).nonzero())
+    _no_device_error(sb)

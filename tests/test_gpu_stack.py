@@ -22,7 +22,7 @@ def sb(cuda_ok):
 
 
 def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, offload=(), overlap=True,
-                    fused=True):
+                    mode="pipelined"):
     """Seeded caches holding tokens 0..T-2, the step's inputs, and forecast heads; planted
     blocks of each layer are shifted along the forecast (computed by the oracle) that selects
     that layer's blocks."""
@@ -59,7 +59,7 @@ def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, 
         Vs.append(V)
         layers.append(layer)
     stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B, overlap=overlap,
-                        fused=fused)
+                        mode=mode)
     stack.h.copy_(h.cuda())
     stack.q.copy_(q.cuda())
     stack.k_new.copy_(kn.cuda())
@@ -149,17 +149,31 @@ def test_offloaded_stack_step(sb, overlap):
     assert sb.sparda_device_error(clear=True) == 0
 
 
-def test_fused_and_separate_launches_agree(sb):
-    # layer L's attention and layer L+1's selection in one launch (the resident default) or
-    # as two kernels on two streams: same kernels' work, bit-identical results
+def test_all_launch_modes_agree(sb):
+    # the same step launched as two kernels per layer (prologue + attend-and-score), as three
+    # (projection, append, attend-and-select) or as one kernel per job on two streams:
+    # the same arithmetic, bit-identical results
     n_layers, B, T, topk, max_ctx, hidden = 4, 3, 3001, 8, 4096, 256
     outs = []
-    for fused in (True, False):
-        shape, stack, inputs = make_stack_case(sb, 11, n_layers, B, T, topk, max_ctx, hidden, 8, fused=fused)
-        assert stack.fused == fused
+    for mode in ("pipelined", "fused", "streams"):
+        shape, stack, inputs = make_stack_case(sb, 11, n_layers, B, T, topk, max_ctx, hidden, 8, mode=mode)
+        assert stack.mode == mode
         stack.enqueue()
         torch.cuda.synchronize()
         outs.append((stack.idx.clone(), stack.cnt.clone(), stack.out.clone()))
-    for a, b in zip(*outs):
-        assert torch.equal(a, b)
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b)
+    assert sb.sparda_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("mode", ["pipelined", "fused"])
+def test_single_layer_stack(sb, mode):
+    # one layer: layer 0's own selection, its prologue without a top-k or projection, its
+    # attention alone
+    shape, stack, inputs = make_stack_case(sb, 13, 1, 2, 2000, 8, 2048, 256, 8, mode=mode)
+    sel, out, S = oracle_step(inputs, 1, 2, 2000, 8)
+    stack.enqueue()
+    torch.cuda.synchronize()
+    assert compare(stack, sel, out, S, 1, 2, 2000, 8) >= 3
     assert sb.sparda_device_error(clear=True) == 0
