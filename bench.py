@@ -246,15 +246,16 @@ def attn_bytes(batch=BATCH):
     return batch * G * ((TOPK + 2) * 64 * D * 2 * 2 + 2 * H * D * 2)
 
 
-def prologue_bytes(batch=BATCH):
+def prologue_bytes(batch=BATCH, topk=True):
     """Algorithmic bytes of one decode prologue: the forecast head's weights and the hidden
     states read and the forecasts written (projection), the block scores read and the
-    selection written (top-k), the token's key and value read and written (append)."""
+    selection written (top-k, if it runs there), the token's key and value read and written
+    (append)."""
     nb = CTX // 64
     proj = G * D * HIDDEN * 2 + batch * HIDDEN * 2 + batch * G * D * 2
-    topk = batch * G * (nb * 4 + (TOPK + 2) * 4 + 4)
+    sel = batch * G * (nb * 4 + (TOPK + 2) * 4 + 4) if topk else 0
     append = batch * G * D * 2 * 2 * 2
-    return proj + topk + append
+    return proj + sel + append
 
 
 def replica_max(values, dist, device):

@@ -150,9 +150,9 @@ def test_offloaded_stack_step(sb, overlap):
 
 
 def test_all_launch_modes_agree(sb):
-    # the same step launched as two kernels per layer (prologue + attend-and-score), as three
-    # (projection, append, attend-and-select) or as one kernel per job on two streams:
-    # the same arithmetic, bit-identical results
+    # the same step launched as two kernels per layer (prologue with the top-k +
+    # attend-and-score), as three (projection, append, attend-and-select) or as one kernel
+    # per job on two streams: the same arithmetic, bit-identical results
     n_layers, B, T, topk, max_ctx, hidden = 4, 3, 3001, 8, 4096, 256
     outs = []
     for mode in ("pipelined", "fused", "streams"):
