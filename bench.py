@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
     p.add_argument("--offload-steps", type=int, default=20)
     p.add_argument("--no-selector-ab", action="store_true", help="skip the selector A/B sweep")
+    p.add_argument("--layout", default="pipelined", choices=["pipelined", "layer", "fused"],
+                   help="launch layout of the resident step (the same arithmetic in each)")
     p.add_argument("--layers", type=int, default=N_LAYERS,
                    help="layers of the resident stack (the metric is quoted on 32; fewer only for small "
                         "profiler captures)")
@@ -63,6 +65,8 @@ def measured_peaks():
 
 # the sources each profiled kernel is built from (a change to any of them voids its counters)
 KERNEL_SOURCES = {
+    "decode_layer": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "append_body.cuh",
+                     "project_body.cuh", "common.cuh", "kernels.h"),
     "attend_and_score": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
     "attend_and_select": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
     "decode_prologue": ("prologue.cu", "append_body.cuh", "project_body.cuh", "topk.cuh", "common.cuh",
@@ -145,7 +149,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- workload
-def build_workload(device, seed, steps_total, n_layers=N_LAYERS):
+def build_workload(device, seed, steps_total, n_layers=N_LAYERS, layout="pipelined"):
     import torch
     import synth
     import block_sparse_attention_forecast_gb300.binding as sb
@@ -174,7 +178,7 @@ def build_workload(device, seed, steps_total, n_layers=N_LAYERS):
         synth.plant_batched(layer.k, blocks, direction)
         sb.sparda_compress_keys(shape, layer, torch.full((BATCH,), T0 - 1, dtype=torch.int32, device=device), BATCH)
         layers.append(layer)
-    stack = DecodeStack(shape, layers, W_self0, W_next, BATCH, device=device, advance=True)
+    stack = DecodeStack(shape, layers, W_self0, W_next, BATCH, device=device, advance=True, mode=layout)
     stack.h.copy_(h)
     stack.q.copy_(synth.normal_bf16_device(stack.q.shape, seed * 1000 + 41, device))
     stack.k_new.copy_(synth.normal_bf16_device(stack.k_new.shape, seed * 1000 + 42, device))
@@ -198,7 +202,8 @@ def kernel_times(stack, reps=4):
         for L in range(n - 1):
             sb.sparda_attend_and_score(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
                                        stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], scores[(L + 1) % 2],
-                                       stack.seq_len, B, stream=s)
+                                       stack.seq_len, B, l2_next=stack.W_next[L + 1] if L + 2 < n else None,
+                                       stream=s)
 
     def prologue_loop(s):
         # the prologues of layers 1 .. n-2 (top-k, append and projection each); the scores
@@ -208,6 +213,13 @@ def kernel_times(stack, reps=4):
                                       ws_scores=scores[L % 2], idx=stack.idx[L], cnt=stack.cnt[L],
                                       W_next=stack.W_next[L], h=stack.h[L], forecast_next=stack.f[L + 1].view(B, -1),
                                       stream=s)
+
+    def layer_loop(s):
+        for L in range(n - 1):
+            sb.sparda_decode_layer(sh, stack.layers[L], stack.q[L], stack.k_new[L], stack.v_new[L], stack.idx[L],
+                                   stack.cnt[L], stack.out[L], stack.ws_attn, stack.layers[L + 1], stack.W_next[L],
+                                   stack.h[L], stack.f[L + 1].view(B, -1), stack.idx[L + 1], stack.cnt[L + 1],
+                                   scores[(L + 1) % 2], stack.seq_len, B, stream=s)
 
     def fused_loop(s):
         for L in range(n - 1):
@@ -226,7 +238,7 @@ def kernel_times(stack, reps=4):
                                          stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
 
     out = {}
-    for name, fn, per in (("score", score_loop, n - 1), ("prologue", prologue_loop, n - 2),
+    for name, fn, per in (("layer", layer_loop, n - 1), ("score", score_loop, n - 1), ("prologue", prologue_loop, n - 2),
                           ("fused", fused_loop, n - 1), ("select", sel_loop, n - 1), ("attn", attn_loop, n)):
         if per > 0:
             out[name] = graph_time(fn, reps) / per
@@ -554,7 +566,7 @@ def run_ours(args):
         cpu = cpu_oracle_sample(24)          # before any heavy GPU setup; ~15 s of CPU work
 
     steps_total = 1 + args.warmup + args.steps
-    shape, stack, T0 = build_workload(device, args.seed + rank, steps_total, args.layers)
+    shape, stack, T0 = build_workload(device, args.seed + rank, steps_total, args.layers, args.layout)
     import block_sparse_attention_forecast_gb300.binding as sb
     stack.capture()                          # one eager step, then the captured graph
     for _ in range(args.warmup):
@@ -629,14 +641,16 @@ def run_ours(args):
     hbm = float(peaks["hbm_gbs"])
     sel_b, att_b = select_bytes(CTX), attn_bytes()
     kernels = {}
-    for name, key, b in (("attend_and_score", "score", sel_b + att_b), ("attend_and_select", "fused", sel_b + att_b),
+    for name, key, b in (("decode_layer", "layer", sel_b + att_b + prologue_bytes(topk=False)),
+                         ("attend_and_score", "score", sel_b + att_b), ("attend_and_select", "fused", sel_b + att_b),
                          ("forecast_select", "select", sel_b), ("sparse_decode_attn", "attn", att_b),
                          ("decode_prologue", "prologue", prologue_bytes())):
         if key in kt:
             gbs = b / kt[key] / 1e9
             kernels[name] = {"us": kt[key] * 1e6, "alg_bytes": b, "gbs": gbs, "frac": gbs / hbm}
-    # the step's dominant kernel: layer L's attention beside layer L+1's block scoring
-    dom = "attend_and_score" if "attend_and_score" in kernels else "sparse_decode_attn"
+    # the step's dominant kernel: layer L's attention beside layer L+1's selection (with the
+    # append and the forecast, in the one-launch layout)
+    dom = {"layer": "decode_layer", "pipelined": "attend_and_score", "fused": "attend_and_select"}[args.layout]
     dk = kernels[dom]
     ms = elapsed / args.steps * 1e3
     value = replica_throughput(world, BATCH, args.steps, elapsed)
@@ -646,6 +660,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name(n), "batch_per_gpu": BATCH, "context": CTX, "layers": n,
+                   "layout": args.layout,
                    "kv_heads": G, "q_heads": G * H, "head_dim": D, "topk": TOPK, "block": 64,
                    "window": "32/16", "hidden": HIDDEN, "parallelism": "replicas" if world > 1 else "single",
                    "positions": "%d consecutive decode steps ending at context %d" % (args.steps, T_last),

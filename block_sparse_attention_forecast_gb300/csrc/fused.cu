@@ -15,6 +15,8 @@ static_assert(kAttnThreads == kSelThreads, "both jobs run with the same CTA shap
 // streamed-byte weight of an attention unit against a selection unit when splitting the SMs
 constexpr double kAttnWeightWithTopk = 1.1;
 constexpr double kAttnWeightScoresOnly = 2.3;
+// the one-launch decode layer: the selection CTAs also compute the forecast and the appends
+constexpr double kAttnWeightLayer = 1.0;
 constexpr int kFusedSmem = kAttnSmem > kSelSmem ? kAttnSmem : kSelSmem;
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
@@ -42,7 +44,7 @@ void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUte
   // bytes per microsecond than a selection CTA (it merges split groups and computes more per
   // byte); a selection CTA that also runs top-k tails streams fewer. The weights are measured
   // at 128K context, batch 16.
-  const double w_attn = sa.do_topk ? kAttnWeightWithTopk : kAttnWeightScoresOnly;
+  const double w_attn = sa.sync ? kAttnWeightLayer : (sa.do_topk ? kAttnWeightWithTopk : kAttnWeightScoresOnly);
   const double wa = w_attn * (double)aa.n_units * (2.0 * kBlockBytes);
   const double ws = (double)sa.n_units * (kWinPerBlock * kRowBytes);
   const int sms = sm_count();

@@ -51,6 +51,18 @@ struct SelectArgs {
   int G, W_cap, max_ctx, nb_cap, topk, chunk_blocks;
   int n_units;                   // B*G*nb_cap, set by the launcher
   int do_topk = 1;               // 0: leave the block scores for a later top-k (decode prologue)
+  // The one-launch decode layer: before scoring, the selection CTAs compute the forecast
+  // they score with (pj.W != nullptr; n_proj_tiles tiles of 8 rows x 16 sequences) and the
+  // layer's appends (ap.k != nullptr; bg_count of them). sync[0] counts finished projection
+  // tiles, sync[1] the selection CTAs that have seen them all (the last one resets both).
+  ProjectArgs pj{};
+  AppendArgs ap{};
+  unsigned* sync = nullptr;
+  int n_proj_tiles = 0, bg_count = 0;
+  // optional: a buffer the next launches read (the next layer's forecast weights), pulled
+  // into L2 by the selection CTAs once they have issued their last load
+  const void* l2_prefetch = nullptr;
+  size_t l2_prefetch_bytes = 0;
 };
 
 struct AttnArgs {
@@ -65,6 +77,10 @@ struct AttnArgs {
   int* err;
   int G, max_ctx, kslots, n_split, offload;
   int n_units;                   // B*G*kslots, set by the launcher
+  // The one-launch decode layer: the token appended in the same launch, taken from here for
+  // the tail block instead of from the cache (whose row may not hold it yet)
+  const __nv_bfloat16* k_new = nullptr;   // [B, G, d]
+  const __nv_bfloat16* v_new = nullptr;
 };
 
 struct MultiheadArgs {
@@ -112,7 +128,7 @@ struct PrologueArgs {
   int32_t* idx;                  // [B, G, topk+2]
   int32_t* cnt;                  // [B, G]
   int topk, nb_cap, bg_count;
-  int n_proj, n_topk;            // CTAs of the projection and top-k roles (multiples of 4)
+  int n_proj, n_topk;            // CTAs of the projection and top-k roles
 };
 void launch_decode_prologue(const PrologueArgs& a, cudaStream_t s);
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);

@@ -9,10 +9,9 @@
 //     section 二).
 //
 // Each alone is a launch of a few microseconds that leaves most of the GPU idle; together they
-// cost one launch. The grid is cut into role ranges, each a whole number of 4-CTA clusters:
-// projection tiles (the four K-quarters of a tile are one cluster, reduced through distributed
-// shared memory), then one top-k CTA per (sequence, group), then append CTAs of four
-// (sequence, group) pairs each. Every CTA first lets the next launch in the stream begin
+// cost one launch. The grid is cut into role ranges: projection tiles (8 rows x 16 sequences
+// each), then one top-k CTA per (sequence, group), then append CTAs of four (sequence, group)
+// pairs each. Every CTA first lets the next launch in the stream begin
 // (programmatic dependent launch: the attention kernel's producers and the selector's loads
 // start early) and then waits for the previous launch to complete.
 #include "append_body.cuh"
@@ -30,16 +29,14 @@ union PrologueShared {
   TopkShared tk;
 };
 
-__global__ void __cluster_dims__(kProjSplit, 1, 1) __launch_bounds__(kPrologueThreads)
-    decode_prologue_kernel(const PrologueArgs a) {
+__global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const PrologueArgs a) {
   __shared__ PrologueShared sh;
   grid_dep_launch();
   grid_dep_wait();
   int c = blockIdx.x;
   if (c < a.n_proj) {
-    // cluster c / 4 is tile (row tile, sequence tile); its rank is the K-quarter
-    const int tile = c / kProjSplit, n_tiles = a.pj.rows / 8;
-    project_cta(a.pj, tile % n_tiles, c % kProjSplit, tile / n_tiles, sh.pj);
+    const int n_tiles = a.pj.rows / 8;
+    project_rows(a.pj, c % n_tiles, c / n_tiles, sh.pj, 1);
     return;
   }
   c -= a.n_proj;
@@ -58,10 +55,9 @@ __global__ void __cluster_dims__(kProjSplit, 1, 1) __launch_bounds__(kPrologueTh
 
 void launch_decode_prologue(const PrologueArgs& args, cudaStream_t s) {
   PrologueArgs a = args;
-  auto round4 = [](int x) { return (x + kProjSplit - 1) / kProjSplit * kProjSplit; };
-  a.n_proj = a.pj.W ? (a.pj.rows / 8) * kProjSplit * ((a.pj.batch + 15) / 16) : 0;
-  a.n_topk = a.block_scores ? round4(a.bg_count) : 0;
-  const int n_append = round4((a.bg_count + kAppendPerCta - 1) / kAppendPerCta);
+  a.n_proj = a.pj.W ? (a.pj.rows / 8) * ((a.pj.batch + 15) / 16) : 0;
+  a.n_topk = a.block_scores ? a.bg_count : 0;
+  const int n_append = (a.bg_count + kAppendPerCta - 1) / kAppendPerCta;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_proj + a.n_topk + n_append);
   cfg.blockDim = dim3(kPrologueThreads);

@@ -23,8 +23,10 @@
 // group; only the last group of the last CTA is a tail.
 #pragma once
 
+#include "append_body.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "project_body.cuh"
 #include "topk.cuh"
 
 namespace sparda {
@@ -37,6 +39,9 @@ constexpr int kSelThreads = kSelConsumers + 32;
 constexpr int kSubBlocks = 31;                            // blocks per sub-chunk
 constexpr int kSubRows = kWinPerBlock * kSubBlocks + 1;   // 125 windows: 4 passes of 32
 constexpr int kSelStages = 6;
+// the two consumer groups take alternate sub-chunks: an even stage count keeps every stage
+// with one group (a phase-parity wait cannot tell a stage's next phase from its last one)
+static_assert(kSelStages % 2 == 0, "each ring stage must belong to one consumer group");
 constexpr int kSelStageBytes = kSubRows * kRowBytes;
 constexpr int kSelSmem = 128 /*align slack*/ + 128 /*barriers*/ + kSelStages * kSelStageBytes;
 
@@ -124,6 +129,16 @@ __device__ __forceinline__ void sel_cta(const SelectArgs& a, int cta, int grid) 
         ++it;
       }
     }
+    if (a.l2_prefetch) {
+      // this CTA's slice of the buffer the next launches read, into L2 (16-byte granules)
+      const size_t g16 = a.l2_prefetch_bytes / 16;
+      const size_t b0 = g16 * cta / grid * 16, b1 = g16 * (cta + 1) / grid * 16;
+      const char* base = static_cast<const char*>(a.l2_prefetch);
+      for (size_t off = b0; off < b1; off += 32768) {
+        const uint32_t n = (uint32_t)min((size_t)32768, b1 - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
+      }
+    }
     return;
   }
 
@@ -136,6 +151,51 @@ __device__ __forceinline__ void sel_cta(const SelectArgs& a, int cta, int grid) 
   int it = 0, nbuf = 0;
   bool first_seg = true;
   bool ok = true;                      // false after a wait ran out: skip compute, keep pace
+  if (a.sync) {
+    // One-launch decode layer: first the forecast this selection scores with and the
+    // layer's appends, shared out over the selection CTAs (their inputs come from the launches
+    // before this one), while the producer already streams compressed keys.
+    grid_dep_wait();
+    first_seg = false;
+    ProjShared& psh = *reinterpret_cast<ProjShared*>(&sh);     // the top-k has not started
+    const int n_app_items = a.ap.k ? (a.bg_count + 3) / 4 : 0;
+    const int n_items = a.n_proj_tiles + n_app_items;
+    for (int w = cta; w < n_items; w += grid) {
+      if (w < a.n_proj_tiles) {
+        const int n_tiles = a.pj.rows / 8;
+        project_rows(a.pj, w % n_tiles, w / n_tiles, psh, 1);
+        __threadfence();                            // this thread's forecast stores
+        sel_sync();
+        if (t == 0) atomicAdd(a.sync, 1u);          // publish the tile
+      } else {
+        const int bg = (w - a.n_proj_tiles) * 4 + t / 64;
+        if (bg < a.bg_count) append_token(a.ap, bg, t % 64);
+      }
+    }
+    if (a.n_proj_tiles > 0) {
+      if (t == 0) {
+        int good = 1;
+        uint32_t polls = 0;
+        while (ld_acquire_gpu(a.sync) < (unsigned)a.n_proj_tiles) {
+          if (++polls > kWaitPolls) {
+            atomicOr(a.err, SPARDA_DEV_WAIT_TIMEOUT);
+            good = 0;
+            break;
+          }
+          __nanosleep(256);
+        }
+        sh.bstar = good;
+        // the last selection CTA to get here resets both counters for the next launch
+        if (atomicAdd(a.sync + 1, 1u) == (unsigned)(grid - 1)) {
+          a.sync[0] = 0u;
+          a.sync[1] = 0u;
+        }
+      }
+      sel_sync();
+      if (!sh.bstar) ok = false;
+      sel_sync();                                   // sh is the top-k's again
+    }
+  }
   for (long long u = J0; u < J1;) {
     const int bg = (int)(u / a.nb_cap);
     const long long seg_end = min(J1, (long long)(bg + 1) * a.nb_cap);
@@ -154,7 +214,7 @@ __device__ __forceinline__ void sel_cta(const SelectArgs& a, int cta, int grid) 
       const uint4* fp = reinterpret_cast<const uint4*>(a.f + (size_t)bg * kHeadDim);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint4 v = fp[c + 4 * k];
+        const uint4 v = __ldcg(fp + c + 4 * k);   // from L2: other CTAs may have written it
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -50,18 +50,20 @@ struct TopkShared {
   int last;
   int bstar;
   int n_ge;
-  int n_list;
   float lv[kMaxList];
   int lj[kMaxList];
   int lr[kMaxList];                    // exact rank of each listed candidate
   unsigned char flag[kMaxBlocksPerSeq];
 };
 
-// Bucket of a candidate score in the 256 equal slices of [lo, hi]. Monotone non-decreasing
-// in x (a subtraction and a positive scaling, each rounded), so every candidate in a higher
+// Bucket of a candidate score in the 256 equal slices of [lo, hi]: floor((x - lo) * scale),
+// taken as the low mantissa bits of 2^23 + that product added with rounding down (an FP32
+// add instead of a float-to-int conversion). Monotone non-decreasing in x (a subtraction, a
+// positive scaling and a rounded-down add, each monotone), so every candidate in a higher
 // bucket outscores every candidate in a lower one.
 __device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
-  return min(255, max(0, __float2int_rd((x - lo) * scale)));
+  const float y = __fadd_rd(fmaxf((x - lo) * scale, 0.f), 8388608.f);
+  return min(255, __float_as_int(y) & 0x7fffff);
 }
 
 // Top-k of one (sequence, group) by 256 threads (threads 0-255 of the CTA, synchronised with
@@ -72,7 +74,7 @@ __device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
 // contiguous 128-byte line). Fast path: min/max of the candidate scores; a 256-bucket
 // histogram over that range (shared-memory atomics); the bucket that holds the k-th score,
 // found by a scan from the top; the candidates at or above that bucket -- a few dozen for real
-// score distributions -- listed in shared memory with one atomic per warp; their exact ranks
+// score distributions -- listed in shared memory by ballots and per-warp counts; their exact ranks
 // (score descending, block ascending) by pairwise comparison; and the output position of each
 // chosen block by counting the chosen blocks below it. If more than kMaxList candidates share
 // those buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
@@ -115,7 +117,6 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
       sh.red_hi[warp] = hi;
     }
     sh.hist[t] = 0u;
-    if (t == 0) sh.n_list = 0;
     topk_sync();
 #pragma unroll
     for (int w = 0; w < kTopkWarps; ++w) {
@@ -124,10 +125,13 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     }
     const float scale = 256.f / (hi - lo);
     bool fast = hi > lo && isfinite(lo) && isfinite(hi) && isfinite(scale);   // CTA-uniform
+    int bk[kKeysPerThread];
     if (fast) {
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e)
-        if (isc[e]) atomicAdd(&sh.hist[score_bucket(v[e], lo, scale)], 1u);
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        bk[e] = isc[e] ? score_bucket(v[e], lo, scale) : -1;
+        if (isc[e]) atomicAdd(&sh.hist[bk[e]], 1u);
+      }
       topk_sync();
       const int hv = (int)sh.hist[255 - t];      // thread t looks at bucket 255 - t
       int tot;
@@ -141,31 +145,35 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     }
     if (fast) {
       const int bstar = sh.bstar;
-      // list the candidates at or above bucket bstar: one shared atomic per warp
-      int mine = 0;
+      // list the candidates at or above bucket bstar, in (warp, e, lane) order: one ballot
+      // per register slot, per-warp totals exchanged once
+      unsigned bal[kKeysPerThread];
+      int wcount = 0;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e)
-        mine += (isc[e] && score_bucket(v[e], lo, scale) >= bstar) ? 1 : 0;
-      int incl = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        bal[e] = __ballot_sync(0xffffffffu, bk[e] >= bstar);
+        wcount += __popc(bal[e]);
       }
-      int base = 0;
-      if (lane == 31 && incl > 0) base = atomicAdd(&sh.n_list, incl);
-      int p = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+      if (lane == 0) sh.warp_tot[warp] = wcount;
+      topk_sync();
+      int p = 0;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e)
-        if (isc[e] && score_bucket(v[e], lo, scale) >= bstar) {
-          sh.lv[p] = v[e];
-          sh.lj[p] = e * kTopkThreads + t;
-          ++p;
+      for (int w = 0; w < kTopkWarps; ++w)
+        if (w < warp) p += sh.warp_tot[w];
+      const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+      for (int e = 0; e < kKeysPerThread; ++e) {
+        if (bk[e] >= bstar) {
+          const int q = p + __popc(bal[e] & below);
+          sh.lv[q] = v[e];
+          sh.lj[q] = e * kTopkThreads + t;
         }
+        p += __popc(bal[e]);
+      }
       topk_sync();
       // exact rank of each listed candidate: `split` threads share one candidate, each
       // scanning a slice of the list
-      const int c = sh.n_list;
+      const int c = sh.n_ge;
       const int split = c <= 32 ? 8 : (c <= 64 ? 4 : (c <= 128 ? 2 : 1));
       for (int i0 = 0; i0 < c * split; i0 += kTopkThreads) {
         const int q = i0 + t;
