@@ -31,7 +31,15 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   AttnArgs b = a;
   b.n_units = bg_count * a.kslots;
-  const int grid = b.n_units < sm_count() ? b.n_units : sm_count();
+  int grid = b.n_units < sm_count() ? b.n_units : sm_count();
+  // a whole number of CTAs per (sequence, group) when the groups fit the SMs: no CTA spans
+  // two groups
+  if (bg_count <= sm_count()) {
+    int sg = sm_count() / bg_count;
+    if (sg > a.kslots) sg = a.kslots;
+    b.seg_per_group = sg;
+    grid = sg * bg_count;
+  }
   // Programmatic serialization: barrier set-up and the unit metadata overlap the append
   // before it in the stream; the producer waits for it before the first TMA load.
   cudaLaunchConfig_t cfg = {};

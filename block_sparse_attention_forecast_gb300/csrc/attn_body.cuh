@@ -96,7 +96,10 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long U = (long long)a.n_units;
-  const int u0 = (int)(U * c / grid), u1 = (int)(U * (c + 1) / grid);
+  // this CTA's units: an equal share of one group's slots, or a contiguous balanced range
+  const int sg = a.seg_per_group;
+  const int u0 = sg > 0 ? (c / sg) * a.kslots + a.kslots * (c % sg) / sg : (int)(U * c / grid);
+  const int u1 = sg > 0 ? (c / sg) * a.kslots + a.kslots * (c % sg + 1) / sg : (int)(U * (c + 1) / grid);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -361,8 +364,8 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
       }
     }
     const long long first = (long long)bg * a.kslots, last = first + a.kslots - 1;
-    const int c_first = cta_of_unit(first, grid, U);
-    const int n_seg = cta_of_unit(last, grid, U) - c_first + 1;
+    const int c_first = sg > 0 ? (c / sg) * sg : cta_of_unit(first, grid, U);
+    const int n_seg = sg > 0 ? sg : cta_of_unit(last, grid, U) - c_first + 1;
     uint4* outp = reinterpret_cast<uint4*>(a.out + ((size_t)bg * kHeads + h) * kHeadDim + d0);
     if (n_seg == 1) {
       uint32_t pk[4];

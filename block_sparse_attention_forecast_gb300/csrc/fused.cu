@@ -14,7 +14,7 @@ namespace sparda {
 static_assert(kAttnThreads == kSelThreads, "both jobs run with the same CTA shape");
 // streamed-byte weight of an attention unit against a selection unit when splitting the SMs
 constexpr double kAttnWeightWithTopk = 1.1;
-constexpr double kAttnWeightScoresOnly = 2.3;
+constexpr double kAttnWeightScoresOnly = 1.9;
 // the one-launch decode layer: the selection CTAs also compute the forecast and the appends
 constexpr double kAttnWeightLayer = 1.0;
 constexpr int kFusedSmem = kAttnSmem > kSelSmem ? kAttnSmem : kSelSmem;
@@ -51,6 +51,18 @@ void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUte
   int n_attn = (int)(sms * wa / (wa + ws) + 0.5);
   n_attn = n_attn < 1 ? 1 : (n_attn > sms - 1 ? sms - 1 : n_attn);
   if (n_attn > aa.n_units) n_attn = aa.n_units;
+  // Prefer a whole number of attention CTAs per (sequence, group), so that no CTA spans two
+  // groups (a group boundary costs a CTA a merge and a fresh start of its pipeline), when
+  // that lands within about a third of the byte-proportional count.
+  const int per = aa.kslots;
+  int sg = (n_attn + bg_count / 2) / bg_count;
+  if (sg < 1) sg = 1;
+  if (sg > per) sg = per;
+  const int aligned = sg * bg_count;
+  if (aligned <= sms - 1 && 3 * abs(aligned - n_attn) <= n_attn) {
+    n_attn = aligned;
+    aa.seg_per_group = sg;
+  }
   int n_sel = sms - n_attn;
   const int sel_work = (sa.n_units + kSubBlocks - 1) / kSubBlocks;
   if (n_sel > sel_work) n_sel = sel_work;

@@ -77,6 +77,9 @@ struct AttnArgs {
   int* err;
   int G, max_ctx, kslots, n_split, offload;
   int n_units;                   // B*G*kslots, set by the launcher
+  // > 0: the grid is seg_per_group CTAs per (sequence, group), each taking an equal share of
+  // that group's slots (no CTA spans two groups); 0: contiguous balanced unit ranges
+  int seg_per_group = 0;
   // The one-launch decode layer: the token appended in the same launch, taken from here for
   // the tail block instead of from the cache (whose row may not hold it yet)
   const __nv_bfloat16* k_new = nullptr;   // [B, G, d]
