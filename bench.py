@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
     p.add_argument("--offload-steps", type=int, default=20)
     p.add_argument("--no-selector-ab", action="store_true", help="skip the selector A/B sweep")
-    p.add_argument("--layout", default="pipelined", choices=["pipelined", "layer", "fused"],
+    p.add_argument("--layout", default="pipelined", choices=["pipelined", "fused"],
                    help="launch layout of the resident step (the same arithmetic in each)")
     p.add_argument("--layers", type=int, default=N_LAYERS,
                    help="layers of the resident stack (the metric is quoted on 32; fewer only for small "
@@ -65,8 +65,6 @@ def measured_peaks():
 
 # the sources each profiled kernel is built from (a change to any of them voids its counters)
 KERNEL_SOURCES = {
-    "decode_layer": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "append_body.cuh",
-                     "project_body.cuh", "common.cuh", "kernels.h"),
     "attend_and_score": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
     "attend_and_select": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
     "decode_prologue": ("prologue.cu", "append_body.cuh", "project_body.cuh", "topk.cuh", "common.cuh",
@@ -214,13 +212,6 @@ def kernel_times(stack, reps=4):
                                       W_next=stack.W_next[L], h=stack.h[L], forecast_next=stack.f[L + 1].view(B, -1),
                                       stream=s)
 
-    def layer_loop(s):
-        for L in range(n - 1):
-            sb.sparda_decode_layer(sh, stack.layers[L], stack.q[L], stack.k_new[L], stack.v_new[L], stack.idx[L],
-                                   stack.cnt[L], stack.out[L], stack.ws_attn, stack.layers[L + 1], stack.W_next[L],
-                                   stack.h[L], stack.f[L + 1].view(B, -1), stack.idx[L + 1], stack.cnt[L + 1],
-                                   scores[(L + 1) % 2], stack.seq_len, B, stream=s)
-
     def fused_loop(s):
         for L in range(n - 1):
             sb.sparda_attend_and_select(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
@@ -238,7 +229,7 @@ def kernel_times(stack, reps=4):
                                          stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
 
     out = {}
-    for name, fn, per in (("layer", layer_loop, n - 1), ("score", score_loop, n - 1), ("prologue", prologue_loop, n - 2),
+    for name, fn, per in (("score", score_loop, n - 1), ("prologue", prologue_loop, n - 2),
                           ("fused", fused_loop, n - 1), ("select", sel_loop, n - 1), ("attn", attn_loop, n)):
         if per > 0:
             out[name] = graph_time(fn, reps) / per
@@ -641,8 +632,7 @@ def run_ours(args):
     hbm = float(peaks["hbm_gbs"])
     sel_b, att_b = select_bytes(CTX), attn_bytes()
     kernels = {}
-    for name, key, b in (("decode_layer", "layer", sel_b + att_b + prologue_bytes(topk=False)),
-                         ("attend_and_score", "score", sel_b + att_b), ("attend_and_select", "fused", sel_b + att_b),
+    for name, key, b in (("attend_and_score", "score", sel_b + att_b), ("attend_and_select", "fused", sel_b + att_b),
                          ("forecast_select", "select", sel_b), ("sparse_decode_attn", "attn", att_b),
                          ("decode_prologue", "prologue", prologue_bytes())):
         if key in kt:
@@ -650,7 +640,7 @@ def run_ours(args):
             kernels[name] = {"us": kt[key] * 1e6, "alg_bytes": b, "gbs": gbs, "frac": gbs / hbm}
     # the step's dominant kernel: layer L's attention beside layer L+1's selection (with the
     # append and the forecast, in the one-launch layout)
-    dom = {"layer": "decode_layer", "pipelined": "attend_and_score", "fused": "attend_and_select"}[args.layout]
+    dom = {"pipelined": "attend_and_score", "fused": "attend_and_select"}[args.layout]
     dk = kernels[dom]
     ms = elapsed / args.steps * 1e3
     value = replica_throughput(world, BATCH, args.steps, elapsed)

@@ -23,7 +23,7 @@ __all__ = [
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
-    "sparda_attend_and_score", "sparda_decode_prologue", "sparda_decode_layer",
+    "sparda_attend_and_score", "sparda_decode_prologue",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
@@ -99,7 +99,6 @@ def _load():
         "sparda_attend_and_select": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, P, P, SZ, P, I32, P]),
         "sparda_attend_and_score": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, SZ, P, SZ, P, I32, P]),
         "sparda_decode_prologue": (I32, [SH, LY, P, P, P, SZ, P, P, P, P, I32, P, P, I32, P]),
-        "sparda_decode_layer": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, LY, P, P, I32, P, P, P, P, SZ, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -297,17 +296,6 @@ def sparda_attend_and_select(shape, layer, q, idx, cnt, out, ws_attn, ck_next, f
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(staging_k), _ptr(staging_v), _ptr(q), _ptr(idx),
         _ptr(cnt), _ptr(out), _ptr(ws_attn), ws_attn.numel(), _ptr(ck_next), _ptr(forecast_next), _ptr(idx_next),
         _ptr(cnt_next), _ptr(ws_sel), ws_sel.numel(), _ptr(seq_len), int(batch), _stream(stream)))
-
-
-def sparda_decode_layer(shape, layer, q, k_new, v_new, idx, cnt, out, ws_attn, next_layer, W_next, h, forecast_next,
-                        idx_next, cnt_next, ws_sel, seq_len, batch, stream=None):
-    """Layer L's append, attention, forecast for layer L+1 and layer L+1's selection in one
-    launch."""
-    _check("sparda_decode_layer", lib.sparda_decode_layer(
-        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(idx), _ptr(cnt),
-        _ptr(out), _ptr(ws_attn), ws_attn.numel(), ctypes.byref(next_layer.c()), _ptr(W_next), _ptr(h),
-        int(W_next.shape[1]), _ptr(forecast_next), _ptr(idx_next), _ptr(cnt_next), _ptr(ws_sel), ws_sel.numel(),
-        _ptr(seq_len), int(batch), _stream(stream)))
 
 
 def sparda_attend_and_score(shape, layer, q, idx, cnt, out, ws_attn, ck_next, forecast_next, ws_scores,

@@ -60,8 +60,8 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspaces are laid out for max_batch sequences so that their counters sit at the same
 // place whatever batch a call uses: [counters: max_batch*G u32][data]. The selection
-// workspace starts with kSyncBytes of launch-wide counters (the one-launch decode layer).
-constexpr size_t kSyncBytes = 256;
+// workspace starts with kQueueBytes for the dynamic selection's work counter.
+constexpr size_t kQueueBytes = 256;
 size_t counters_bytes(const sparda_shape* s) {
   return round256((size_t)s->max_batch * s->n_groups * sizeof(unsigned));
 }
@@ -186,7 +186,7 @@ int32_t sparda_check_shape(const sparda_shape* shape) { return shape_status(shap
 size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind) {
   if (shape_status(s) != SPARDA_OK || batch < 1 || batch > s->max_batch) return 0;
   switch (kind) {
-    case SPARDA_WS_SELECT: return kSyncBytes + counters_bytes(s) + select_data_bytes(s);
+    case SPARDA_WS_SELECT: return kQueueBytes + counters_bytes(s) + select_data_bytes(s);
     case SPARDA_WS_ATTN: return counters_bytes(s) + attn_o_bytes(s) + attn_ml_bytes(s);
     case SPARDA_WS_MULTIHEAD: return mh_z_bytes(s) + mh_stats_bytes(s) + select_data_bytes(s);
     default: return 0;
@@ -270,12 +270,15 @@ int32_t prepare_select(const sparda_shape* s, const void* ck, const void* foreca
   if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_SELECT)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
   int* err = dev_error_ptr();
   if (!err) return SPARDA_ERR_CUDA;
-  uint8_t* w = static_cast<uint8_t*>(ws) + kSyncBytes;
+  uint8_t* w = static_cast<uint8_t*>(ws) + kQueueBytes;
   const int bgc = batch * s->n_groups;
   *out = SelectArgs{static_cast<const __nv_bfloat16*>(ck), static_cast<const __nv_bfloat16*>(forecast),
                     seq_len, idx, cnt, reinterpret_cast<float*>(w + counters_bytes(s)),
                     reinterpret_cast<unsigned*>(w), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s),
                     s->topk, select_chunk_blocks(nb_cap(s), bgc), 0, scores_only ? 0 : 1};
+  // the scores-only selection hands out its sub-chunks dynamically when the forecasts of all
+  // its (sequence, group)s fit in shared memory beside the ring
+  if (scores_only && bgc <= kSelDynMaxGroups) out->queue = static_cast<unsigned*>(ws);
   return SPARDA_OK;
 }
 
@@ -360,41 +363,6 @@ int32_t sparda_attend_and_select(const sparda_shape* s, const sparda_layer_kv* L
   return cuda_status(cudaGetLastError());
 }
 
-int32_t sparda_decode_layer(const sparda_shape* s, const sparda_layer_kv* L, const void* q, const void* k_new,
-                            const void* v_new, const int32_t* idx, const int32_t* cnt, void* out, void* ws_attn,
-                            size_t ws_attn_bytes, const sparda_layer_kv* next, const void* W_next, const void* h,
-                            int32_t hidden, void* forecast_next, int32_t* idx_next, int32_t* cnt_next, void* ws_sel,
-                            size_t ws_sel_bytes, const int32_t* seq_len, int32_t batch, void* stream) {
-  if (!L || !next || L->on_host) return SPARDA_ERR_INVALID_ARG;            // resident layers only
-  if (idx_next == idx || cnt_next == cnt || ws_sel == ws_attn || !k_new || !v_new || !W_next || !h ||
-      !forecast_next)
-    return SPARDA_ERR_INVALID_ARG;
-  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(W_next, 16) || !aligned(h, 16) ||
-      !aligned(forecast_next, 16))
-    return SPARDA_ERR_MISALIGNED;
-  if (hidden < 32 || hidden % 32 != 0) return SPARDA_ERR_UNSUPPORTED_SHAPE;
-  SPARDA_TRY(layer_status(L, true));
-  AttnArgs a;
-  CUtensorMap mk, mv, hk, hv;
-  SPARDA_TRY(prepare_attn(s, L, nullptr, nullptr, q, idx, cnt, seq_len, batch, out, ws_attn, ws_attn_bytes, &a,
-                          &mk, &mv, &hk, &hv));
-  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  SelectArgs sa;
-  SPARDA_TRY(prepare_select(s, next->ck, forecast_next, seq_len, batch, idx_next, cnt_next, ws_sel, ws_sel_bytes,
-                            &sa));
-  sa.pj = ProjectArgs{static_cast<const __nv_bfloat16*>(W_next), static_cast<const __nv_bfloat16*>(h),
-                      static_cast<__nv_bfloat16*>(forecast_next), s->n_groups * kHeadDim, hidden, batch};
-  sa.ap = AppendArgs{static_cast<__nv_bfloat16*>(L->k), static_cast<__nv_bfloat16*>(L->v),
-                     static_cast<__nv_bfloat16*>(L->ck), nullptr, nullptr, static_cast<const __nv_bfloat16*>(k_new),
-                     static_cast<const __nv_bfloat16*>(v_new), seq_len, a.err, s->n_groups, s->max_ctx, w_cap(s), 0};
-  sa.sync = static_cast<unsigned*>(ws_sel);
-  sa.n_proj_tiles = (s->n_groups * kHeadDim / 8) * ((batch + 15) / 16);
-  sa.bg_count = batch * s->n_groups;
-  launch_attend_and_select(a, sa, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
-  return cuda_status(cudaGetLastError());
-}
-
 int32_t sparda_attend_and_score(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
                                 const void* staging_v, const void* q, const int32_t* idx, const int32_t* cnt,
                                 void* out, void* ws_attn, size_t ws_attn_bytes, const void* ck_next,
@@ -447,7 +415,7 @@ int32_t sparda_decode_prologue(const sparda_shape* s, const sparda_layer_kv* L, 
   a.pj = ProjectArgs{static_cast<const __nv_bfloat16*>(W_next), static_cast<const __nv_bfloat16*>(h),
                      static_cast<__nv_bfloat16*>(forecast_next), s->n_groups * kHeadDim, hidden, batch};
   a.block_scores = ws_scores ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws_scores) +
-                                                              kSyncBytes + counters_bytes(s))
+                                                              kQueueBytes + counters_bytes(s))
                              : nullptr;
   a.idx = idx;
   a.cnt = cnt;

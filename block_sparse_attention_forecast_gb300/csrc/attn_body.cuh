@@ -206,14 +206,6 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     if (s_begin < s_stop) {
-      // one-launch decode layer: this launch appends the token at T-1, so the tail block's row
-      // for it is taken from the inputs (each lane holds dims 4*lane .. 4*lane+3)
-      const int p_tok = gi.T - 1;
-      uint2 knw = make_uint2(0u, 0u), vnw = make_uint2(0u, 0u);
-      if (a.k_new) {
-        knw = __ldcg(reinterpret_cast<const uint2*>(a.k_new + (size_t)bg * kHeadDim) + lane);
-        vnw = __ldcg(reinterpret_cast<const uint2*>(a.v_new + (size_t)bg * kHeadDim) + lane);
-      }
       uint32_t qf[8][4];
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)bg * kHeads + g) * kHeadDim);
       const uint32_t* q1 = q0 + 8 * (kHeadDim / 2);
@@ -232,15 +224,6 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         const int j = stage_j[stage];
         const uint8_t* Kt = ring + stage * kSlotBytes;
         const uint8_t* Vt = Kt + kBlockBytes;
-        if (a.k_new && j == gi.tb && wq == ((p_tok & (kBlock - 1)) >> 4)) {
-          // only this warp reads row p_tok of the block (its 16 tokens), in K and in V
-          const int r = p_tok & (kBlock - 1);
-          const uint32_t ka = swz(Kt, r, lane >> 1) + 8 * (lane & 1);
-          const uint32_t va = swz(Vt, r, lane >> 1) + 8 * (lane & 1);
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(ka), "r"(knw.x), "r"(knw.y) : "memory");
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(va), "r"(vnw.x), "r"(vnw.y) : "memory");
-          __syncwarp();
-        }
 
         // S = Q K^T, two independent accumulator chains per n-tile
         float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};

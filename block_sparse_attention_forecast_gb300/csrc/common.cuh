@@ -164,12 +164,6 @@ __device__ __forceinline__ uint32_t ordered_key(float x) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Hot slot of block j (>= 0) of an offloaded layer.
 __device__ __forceinline__ int hot_slot(int j) { return j == 0 ? 0 : 1 + (j & 1); }
 

@@ -15,9 +15,9 @@ static_assert(kAttnThreads == kSelThreads, "both jobs run with the same CTA shap
 // streamed-byte weight of an attention unit against a selection unit when splitting the SMs
 constexpr double kAttnWeightWithTopk = 1.1;
 constexpr double kAttnWeightScoresOnly = 1.9;
-// the one-launch decode layer: the selection CTAs also compute the forecast and the appends
-constexpr double kAttnWeightLayer = 1.0;
 constexpr int kFusedSmem = kAttnSmem > kSelSmem ? kAttnSmem : kSelSmem;
+static_assert(kFusedSmem >= 256 + kSelStages * kSelStageBytes + kSelDynMaxGroups * kHeadDim * 2,
+              "the dynamic selection's forecast table fits beside its ring");
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
     const AttnArgs aa, const SelectArgs sa, int n_attn, const __grid_constant__ CUtensorMap mk,
@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
     const __grid_constant__ CUtensorMap hv) {
   if ((int)blockIdx.x < n_attn)
     attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x, n_attn);
+  else if (sa.queue)
+    sel_cta_dyn(sa, blockIdx.x - n_attn, gridDim.x - n_attn);
   else
     sel_cta(sa, blockIdx.x - n_attn, gridDim.x - n_attn);
 }
@@ -44,7 +46,7 @@ void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUte
   // bytes per microsecond than a selection CTA (it merges split groups and computes more per
   // byte); a selection CTA that also runs top-k tails streams fewer. The weights are measured
   // at 128K context, batch 16.
-  const double w_attn = sa.sync ? kAttnWeightLayer : (sa.do_topk ? kAttnWeightWithTopk : kAttnWeightScoresOnly);
+  const double w_attn = sa.do_topk ? kAttnWeightWithTopk : kAttnWeightScoresOnly;
   const double wa = w_attn * (double)aa.n_units * (2.0 * kBlockBytes);
   const double ws = (double)sa.n_units * (kWinPerBlock * kRowBytes);
   const int sms = sm_count();

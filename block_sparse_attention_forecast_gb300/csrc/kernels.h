@@ -10,6 +10,10 @@
 
 namespace sparda {
 
+// The scores-only selection of the fused launch hands out its work dynamically for up to this
+// many (sequence, group)s: their forecasts must fit in shared memory beside its ring.
+constexpr int kSelDynMaxGroups = 35;
+
 struct AppendArgs {
   __nv_bfloat16* k;
   __nv_bfloat16* v;
@@ -51,14 +55,10 @@ struct SelectArgs {
   int G, W_cap, max_ctx, nb_cap, topk, chunk_blocks;
   int n_units;                   // B*G*nb_cap, set by the launcher
   int do_topk = 1;               // 0: leave the block scores for a later top-k (decode prologue)
-  // The one-launch decode layer: before scoring, the selection CTAs compute the forecast
-  // they score with (pj.W != nullptr; n_proj_tiles tiles of 8 rows x 16 sequences) and the
-  // layer's appends (ap.k != nullptr; bg_count of them). sync[0] counts finished projection
-  // tiles, sync[1] the selection CTAs that have seen them all (the last one resets both).
-  ProjectArgs pj{};
-  AppendArgs ap{};
-  unsigned* sync = nullptr;
-  int n_proj_tiles = 0, bg_count = 0;
+  // scores-only selection of the fused launch with at most 35 (sequence, group)s: sub-chunks
+  // are handed out from queue[0] (queue[1] counts the producers that finished); nullptr:
+  // contiguous ranges
+  unsigned* queue = nullptr;
   // optional: a buffer the next launches read (the next layer's forecast weights), pulled
   // into L2 by the selection CTAs once they have issued their last load
   const void* l2_prefetch = nullptr;
@@ -80,10 +80,6 @@ struct AttnArgs {
   // > 0: the grid is seg_per_group CTAs per (sequence, group), each taking an equal share of
   // that group's slots (no CTA spans two groups); 0: contiguous balanced unit ranges
   int seg_per_group = 0;
-  // The one-launch decode layer: the token appended in the same launch, taken from here for
-  // the tail block instead of from the cache (whose row may not hold it yet)
-  const __nv_bfloat16* k_new = nullptr;   // [B, G, d]
-  const __nv_bfloat16* v_new = nullptr;
 };
 
 struct MultiheadArgs {

@@ -8,9 +8,8 @@
 // partial tiles are then added in warp order through shared memory. The contraction index may
 // be permuted as long as A and B use the same permutation, so in each chunk lane (g, c) loads
 // 8 consecutive elements of W row g and of h rows g and g+8 and feeds elements 0-3 to one MMA
-// and 4-7 to the next. Every launch that projects (the standalone projection, the decode
-// prologue, the one-launch decode layer) runs this same arithmetic, so their forecasts agree
-// bit for bit.
+// and 4-7 to the next. Every launch that projects (the standalone projection and the decode
+// prologue) runs this same arithmetic, so their forecasts agree bit for bit.
 #pragma once
 
 #include "common.cuh"

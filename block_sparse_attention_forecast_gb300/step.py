@@ -8,10 +8,6 @@ and selects its own blocks with a same-layer forecast), three ways to launch the
       decode_prologue(L)   top-k of layer L's block scores -> idx[L]; append(L);
                            forecast f[L+1] = W_next[L] h[L]
       attend_and_score(L)  attention(L, idx[L]) beside the block scores of layer L+1
-  "layer": one launch per layer on one stream
-      decode_layer(L)      append(L); attention(L, idx[L]) with the token taken from the
-                           inputs; forecast f[L+1]; selection of layer L+1 -> idx[L+1]
-      (the last layer: decode_prologue for its append, then its attention)
   "fused": three launches per layer on one stream
       forecast_project(L+1); append(L); attend_and_select(L, L+1) (attention beside the
       whole selection of layer L+1, top-k included)
@@ -44,7 +40,7 @@ class DecodeStack:
     out. idx[L] / cnt[L] hold the blocks layer L attends at the current step.
     """
 
-    MODES = ("pipelined", "layer", "fused", "streams")
+    MODES = ("pipelined", "fused", "streams")
 
     def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
                  overlap=True, advance=False, after_attention=None, mode="pipelined"):
@@ -99,8 +95,6 @@ class DecodeStack:
         """Enqueue one decode step on the current stream (plus the side streams)."""
         if self.mode == "pipelined":
             return self._enqueue_pipelined()
-        if self.mode == "layer":
-            return self._enqueue_layer()
         if self.mode == "fused":
             return self._enqueue_fused()
         sh, B = self.shape, self.batch
@@ -191,32 +185,6 @@ class DecodeStack:
         if self.advance:
             self.seq_len.add_(1)
 
-    def _enqueue_layer(self):
-        """Resident stack, one stream, one launch per layer (sparda_decode_layer); the last
-        layer appends in a prologue launch and attends alone. Selection workspaces
-        alternate."""
-        sh, B, n = self.shape, self.batch, self.n_layers
-        main = torch.cuda.current_stream()
-        ws = (self.ws_sel, self.ws_sel2)
-        sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
-        sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
-                                  self.idx[0], self.cnt[0], self.ws_sel, stream=main)
-        for L in range(n):
-            layer = self.layers[L]
-            if L + 1 < n:
-                sb.sparda_decode_layer(sh, layer, self.q[L], self.k_new[L], self.v_new[L], self.idx[L], self.cnt[L],
-                                       self.out[L], self.ws_attn, self.layers[L + 1], self.W_next[L], self.h[L],
-                                       self.f[L + 1].view(B, -1), self.idx[L + 1], self.cnt[L + 1], ws[(L + 1) % 2],
-                                       self.seq_len, B, stream=main)
-            else:
-                sb.sparda_decode_prologue(sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B, stream=main)
-                sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
-                                             self.out[L], self.ws_attn, stream=main)
-            if self.after_attention is not None:
-                self.after_attention(L)
-        if self.advance:
-            self.seq_len.add_(1)
-
     def _enqueue_fused(self):
         """Resident stack, one stream: per layer the forecast projection for layer L+1, the
         append of layer L, then layer L's attention together with layer L+1's selection."""
@@ -268,16 +236,13 @@ class DecodeStack:
     def kernel_launches_per_step(self):
         """Kernels of libsparda one step launches. All modes start with layer 0's own
         projection and selection. Pipelined: then per layer a prologue, per layer but the
-        last an attend-and-score, the last layer's attention alone. Layer: one launch per
-        layer but the last, which takes a prologue and an attention. Fused: per layer an
+        last an attend-and-score, the last layer's attention alone. Fused: per layer an
         append, per layer but the last a projection and an attend-and-select, the last
         layer's attention. Streams: per layer append and attention, per layer but the last a
         projection and a selection, one gather per offloaded layer."""
         n = self.n_layers
         if self.mode == "pipelined":
             return 2 + n + (n - 1) + 1
-        if self.mode == "layer":
-            return 2 + (n - 1) + 2
         if self.mode == "fused":
             return 2 + n + 2 * (n - 1) + 1
         gathers = sum(1 for l in self.layers[1:] if l.on_host)

@@ -257,33 +257,6 @@ int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_k
  */
 
 /*
- * sparda_decode_layer -- one resident layer L of the decode step in ONE launch (the layout of
- * the step with the fewest launches; bittide thread and techwalker section 二 for the
- * lookahead; section 四 for the compression window):
- *   - the append of k_new / v_new (device bf16 [B, G, d]) to `layer`, exactly as
- *     sparda_append_kv;
- *   - layer L's attention, exactly as sparda_sparse_decode_attn with idx / cnt; the current
- *     token's key and value are taken from k_new / v_new;
- *   - the forecast for layer L+1, forecast_next = bf16(W_next . h), exactly as
- *     sparda_forecast_project (W_next: bf16 [G*d, hidden], h: bf16 [B, hidden], hidden a
- *     multiple of 32; forecast_next: bf16 [B, G, d], written);
- *   - layer L+1's selection from next->ck with that forecast, exactly as
- *     sparda_forecast_select, into idx_next / cnt_next (ws_sel: SPARDA_WS_SELECT).
- * One persistent grid of one CTA per SM: attention CTAs stream layer L's blocks from the
- * start; selection CTAs first share out the projection tiles and the appends, publish the
- * forecast through a counter in ws_sel that they wait on (a bounded wait: on timeout they set
- * SPARDA_DEV_WAIT_TIMEOUT and skip the scoring), then score and select. Everything this launch
- * reads must have been written by launches before it. Resident layers only; idx_next,
- * cnt_next and ws_sel must differ from idx, cnt and ws_attn (SPARDA_ERR_INVALID_ARG).
- */
-int32_t sparda_decode_layer(const sparda_shape* shape, const sparda_layer_kv* layer, const void* q,
-                            const void* k_new, const void* v_new, const int32_t* idx, const int32_t* cnt,
-                            void* out, void* ws_attn, size_t ws_attn_bytes, const sparda_layer_kv* next,
-                            const void* W_next, const void* h, int32_t hidden, void* forecast_next,
-                            int32_t* idx_next, int32_t* cnt_next, void* ws_sel, size_t ws_sel_bytes,
-                            const int32_t* seq_len, int32_t batch, void* stream);
-
-/*
  * sparda_attend_and_score -- as sparda_attend_and_select, except that the selection half
  * stops after the block scores: for each (b, g) of layer L+1, S[j] (float32, the max-pooled
  * forecast scores, j < (T-1)/64 + 1) is left in ws_scores (a SPARDA_WS_SELECT workspace),

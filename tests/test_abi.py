@@ -98,24 +98,3 @@ def test_pipelined_entries_reject_bad_arguments():
     assert score(sh, L, None, None, fake, fake, fake, fake, fake, 1 << 30, fake, fake, P(1 << 22), 1 << 30, fake, 100,
                  fake, 1, None) == sb.ERR_MISALIGNED
 
-
-def test_decode_layer_rejects_bad_arguments():
-    s = sb.Shape(max_batch=2, max_ctx=4096)
-    sh = ctypes.byref(s.c())
-    P = ctypes.c_void_p
-    fake, fake2, odd = P(1 << 20), P(1 << 21), P((1 << 20) + 8)
-    resident = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, None, None, 0, 0)
-    offloaded = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 0)
-    L, N = ctypes.byref(resident), ctypes.byref(resident)
-    layer = sb.lib.sparda_decode_layer
-
-    def call(layer_kv=L, nxt=N, k_new=fake, hidden=4096, idx_next=fake2, ws_sel=fake2):
-        return layer(sh, layer_kv, fake, k_new, fake, fake, fake, fake, fake, 1 << 30, nxt, fake, fake, hidden, fake,
-                     idx_next, fake2, ws_sel, 1 << 30, fake, 1, None)
-    assert call(nxt=None) == sb.ERR_INVALID_ARG                   # no next layer
-    assert call(layer_kv=ctypes.byref(offloaded)) == sb.ERR_INVALID_ARG
-    assert call(idx_next=fake) == sb.ERR_INVALID_ARG              # the selection would overwrite its input
-    assert call(ws_sel=fake) == sb.ERR_INVALID_ARG                # shares the attention workspace
-    assert call(k_new=None) == sb.ERR_INVALID_ARG
-    assert call(k_new=odd) == sb.ERR_MISALIGNED
-    assert call(hidden=100) == sb.ERR_UNSUPPORTED_SHAPE

@@ -101,7 +101,7 @@ def compare(stack, sel, out, S, n_layers, B, T, topk):
     return same
 
 
-@pytest.mark.parametrize("mode", ["pipelined", "layer"])
+@pytest.mark.parametrize("mode", ["pipelined", "fused"])
 @pytest.mark.parametrize("n_layers,B,T,topk,max_ctx,hidden", [
     (3, 2, 1500, 8, 2048, 256),
     (4, 3, 4097, 32, 8192, 4096),
@@ -151,12 +151,12 @@ def test_offloaded_stack_step(sb, overlap):
 
 
 def test_all_launch_modes_agree(sb):
-    # the same step launched as one kernel per layer (decode_layer), two (prologue with the
-    # top-k + attend-and-score), three (projection, append, attend-and-select) or one kernel
-    # per job on two streams: the same arithmetic, bit-identical results
+    # the same step launched as two kernels per layer (prologue with the top-k +
+    # attend-and-score), three (projection, append, attend-and-select) or one kernel per job
+    # on two streams: the same arithmetic, bit-identical results
     n_layers, B, T, topk, max_ctx, hidden = 4, 3, 3001, 8, 4096, 256
     outs = []
-    for mode in ("pipelined", "layer", "fused", "streams"):
+    for mode in ("pipelined", "fused", "streams"):
         shape, stack, inputs = make_stack_case(sb, 11, n_layers, B, T, topk, max_ctx, hidden, 8, mode=mode)
         assert stack.mode == mode
         stack.enqueue()
@@ -168,7 +168,7 @@ def test_all_launch_modes_agree(sb):
     assert sb.sparda_device_error(clear=True) == 0
 
 
-@pytest.mark.parametrize("mode", ["pipelined", "layer", "fused"])
+@pytest.mark.parametrize("mode", ["pipelined", "fused"])
 def test_single_layer_stack(sb, mode):
     # one layer: layer 0's own selection, its prologue without a top-k or projection, its
     # attention alone
