@@ -638,8 +638,7 @@ def run_ours(args):
         if key in kt:
             gbs = b / kt[key] / 1e9
             kernels[name] = {"us": kt[key] * 1e6, "alg_bytes": b, "gbs": gbs, "frac": gbs / hbm}
-    # the step's dominant kernel: layer L's attention beside layer L+1's selection (with the
-    # append and the forecast, in the one-launch layout)
+    # the step's dominant kernel: layer L's attention beside layer L+1's selection
     dom = {"pipelined": "attend_and_score", "fused": "attend_and_select"}[args.layout]
     dk = kernels[dom]
     ms = elapsed / args.steps * 1e3
