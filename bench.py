@@ -585,33 +585,37 @@ def run_ours(args):
     elapsed = e0.elapsed_time(e1) * 1e-3
     T_last = int(stack.seq_len[0].item()) - 1      # context of the last timed step
 
-    # end to end through the public API: per step, H2D of the step's inputs from pinned host
-    # memory, the step, D2H of the attention outputs
-    import synth
-    host_in = [torch.empty_like(t, device="cpu").pin_memory() for t in (stack.h, stack.q, stack.k_new, stack.v_new)]
-    for hb, t in zip(host_in, (stack.h, stack.q, stack.k_new, stack.v_new)):
-        hb.copy_(t.cpu())
-    host_out = torch.empty_like(stack.out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    # the per-launch kernel times (roofline) before the end-to-end leg, so that its host
+    # traffic cannot colour them
+    stack.seq_len.fill_(CTX)                 # the kernels below run at context CTX
+    kt = kernel_times(stack)
+    dev_err |= sb.sparda_device_error(clear=True)
+
+    # end to end through the public API: every step copies its inputs from pinned host memory
+    # and its attention outputs back to pinned host memory (DecodeStack.attach_host_io: inside
+    # the captured step, the first layers' inputs and the last layers' outputs go by copy
+    # kernel on the compute stream, the rest by DMA on the I/O stream, overlapped with the
+    # compute); wall-clock time around the replays, synchronised at the end
+    host_in = stack.pinned_inputs()
+    for n in stack.IO_INPUTS:
+        host_in[n].copy_(getattr(stack, n).cpu())
+    host_out = torch.zeros_like(stack.out, device="cpu").pin_memory()
+    stack.attach_host_io(host_in, host_out)
+    h2d, d2h = stack.io_bytes()
     e2e_steps = min(args.steps, 200)
-    stack.seq_len.fill_(CTX - e2e_steps)
+    stack.seq_len.fill_(CTX - e2e_steps - 2)   # the capture's eager step and one replay advance it
+    stack.capture()
     stack.run()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        for hb, t in zip(host_in, (stack.h, stack.q, stack.k_new, stack.v_new)):
-            t.copy_(hb, non_blocking=True)
         stack.run()
-        host_out.copy_(stack.out, non_blocking=True)
     torch.cuda.synchronize()
     e2e_elapsed = time.perf_counter() - t0
+    stack.attach_host_io(None, None)
 
-    stack.seq_len.fill_(CTX)                 # the kernels below run at context CTX
-    kt = kernel_times(stack)
-    dev_err |= sb.sparda_device_error(clear=True)
     launches_per_step = stack.kernel_launches_per_step()
     offload = None
     if world == 1 and not args.no_offload:

@@ -99,6 +99,7 @@ def _load():
         "sparda_attend_and_select": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, P, P, SZ, P, I32, P]),
         "sparda_attend_and_score": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, SZ, P, SZ, P, I32, P]),
         "sparda_decode_prologue": (I32, [SH, LY, P, P, P, SZ, P, P, P, P, I32, P, P, I32, P]),
+        "sparda_copy": (I32, [P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -324,6 +325,15 @@ def sparda_prefetch_blocks(shape, layer, idx, cnt, seq_len, batch, staging_k, st
     _check("sparda_prefetch_blocks", lib.sparda_prefetch_blocks(
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(idx), _ptr(cnt), _ptr(seq_len),
         int(batch), _ptr(staging_k), _ptr(staging_v), int(n_ctas), _stream(stream)))
+
+
+def sparda_copy(dst, src, stream=None):
+    """Device-side copy of src into dst (same byte size, each contiguous): device tensors or
+    pinned host tensors (see include/sparda.h)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes or not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("sparda_copy needs two contiguous tensors of the same byte size")
+    _check("sparda_copy", lib.sparda_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)))
 
 
 def sparda_multihead_select(shape, ck, q, seq_len, batch, idx, cnt, ws, stream=None):

@@ -9,6 +9,10 @@
 
 using namespace sparda;
 
+namespace sparda {
+void launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);   // copy.cu
+}
+
 // The device error word (bits SPARDA_DEV_*). Kernels receive its device address.
 __device__ int g_sparda_dev_error;
 
@@ -136,6 +140,17 @@ int32_t host_mapped_status(const void* p) {
   return SPARDA_OK;
 }
 
+// Memory the kernels can dereference as given: device memory, or mapped pinned host memory.
+int32_t device_addressable_status(const void* p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SPARDA_ERR_NOT_MAPPED_HOST;
+  }
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) return SPARDA_OK;
+  return host_mapped_status(p);
+}
+
 int32_t layer_status(const sparda_layer_kv* L, bool need_kv) {
   if (!L || !L->ck) return SPARDA_ERR_INVALID_ARG;
   if (!aligned(L->ck, 16)) return SPARDA_ERR_MISALIGNED;
@@ -204,6 +219,15 @@ int32_t sparda_device_error(int32_t* flags, int32_t clear) {
 }
 
 int32_t sparda_prefetch_default_ctas(int32_t batch) { return batch < 32 ? 64 : 152; }
+
+int32_t sparda_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (!dst || !src || bytes == 0 || bytes % 16 != 0) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(dst, 16) || !aligned(src, 16)) return SPARDA_ERR_MISALIGNED;
+  SPARDA_TRY(device_addressable_status(dst));
+  SPARDA_TRY(device_addressable_status(src));
+  launch_copy16(dst, src, bytes, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
 
 int32_t sparda_append_kv(const sparda_shape* s, const sparda_layer_kv* L, const void* k_new,
                          const void* v_new, const int32_t* seq_len, int32_t batch, void* stream) {

@@ -21,7 +21,8 @@ and selects its own blocks with a same-layer forecast), three ways to launch the
 
 Every mode computes the same results bit for bit. Everything here is host-side orchestration
 of libsparda calls (no arithmetic); the whole step can be captured once into a CUDA graph and
-replayed.
+replayed. With host I/O attached (attach_host_io), every step also brings its inputs from
+pinned host memory and returns its attention outputs there, overlapped with the compute.
 """
 from __future__ import annotations
 
@@ -68,10 +69,19 @@ class DecodeStack:
         hidden = W_self0.shape[1]
         n, B = self.n_layers, batch
         bf = dict(dtype=torch.bfloat16, device=device)
-        self.h = torch.zeros((n, B, hidden), **bf)
-        self.q = torch.zeros((n, B, G * H, d), **bf)
-        self.k_new = torch.zeros((n, B, G, d), **bf)
-        self.v_new = torch.zeros((n, B, G, d), **bf)
+        # The per-step inputs share one buffer, layer-major: layer L's h, q, k_new and v_new
+        # are adjacent (each padded to 256 bytes), so the host-I/O copy of a range of layers is
+        # a single copy. h, q, k_new, v_new are [n, ...] views of it; each layer's slice is
+        # contiguous.
+        self._in_layout = []
+        row = 0
+        for name, shp in (("h", (B, hidden)), ("q", (B, G * H, d)), ("k_new", (B, G, d)), ("v_new", (B, G, d))):
+            nbytes = 2 * B * int(torch.Size(shp[1:]).numel())
+            self._in_layout.append((name, row, nbytes, shp))
+            row += (nbytes + 255) // 256 * 256
+        self._in_dev = torch.zeros((n, row), dtype=torch.uint8, device=device)
+        for name, view in self._input_views(self._in_dev).items():
+            setattr(self, name, view)
         self.out = torch.zeros((n, B, G * H, d), **bf)
         self.f = torch.zeros((n + 1, B, G, d), **bf)        # f[L]: forecast for layer L
         self.idx = torch.full((n, B, G, shape.kslots), -1, dtype=torch.int32, device=device)
@@ -89,14 +99,153 @@ class DecodeStack:
         # so its CTAs are scheduled ahead of waiting compute CTAs
         self.gather = (torch.cuda.Stream(device=device, priority=-1) if self.any_offload else None)
         self.graph = None
+        self.io = torch.cuda.Stream(device=device)
+        self.host_in = None
+        self.host_out = None
+
+    # ------------------------------------------------------------------ host I/O
+    IO_INPUTS = ("h", "q", "k_new", "v_new")
+
+    def _input_views(self, packed):
+        n = self.n_layers
+        return {name: packed[:, o:o + nb].view(torch.bfloat16).view(n, *shp)
+                for name, o, nb, shp in self._in_layout}
+
+    def pinned_inputs(self):
+        """Pinned host staging for the per-step inputs, laid out like the device buffers: a
+        dict of CPU views 'h', 'q', 'k_new', 'v_new' (shaped like the device tensors of the
+        same names) and 'packed', the pinned uint8 buffer [n_layers, row bytes] they view."""
+        packed = torch.zeros(tuple(self._in_dev.shape), dtype=torch.uint8).pin_memory()
+        views = self._input_views(packed)
+        views["packed"] = packed
+        return views
+
+    def attach_host_io(self, host_in, host_out):
+        """Make every step read its inputs from pinned host memory and write its attention
+        outputs back to it. host_in: the dict pinned_inputs() returns (the caller writes each
+        step's inputs into its views); host_out: a pinned CPU tensor shaped like out.
+        (None, None) detaches. Inside the step, the first layers' inputs are copied in and the
+        last layers' outputs out by a copy kernel on the compute stream; the other layers' go
+        by DMA on an I/O stream, the inputs ahead of the first launch that reads them and the
+        outputs as soon as their attention has run, overlapped with the compute (_in_plan,
+        _out_plan). Capture again after attaching or detaching."""
+        if host_in is None and host_out is None:
+            self.host_in = self.host_out = None
+            return
+        packed = host_in.get("packed") if isinstance(host_in, dict) else None
+        if (packed is None or packed.device.type != "cpu" or not packed.is_pinned()
+                or packed.shape != self._in_dev.shape or packed.dtype != torch.uint8):
+            raise ValueError("host inputs must be the dict DecodeStack.pinned_inputs() returns")
+        base = packed.untyped_storage().data_ptr()
+        for name, view in self._input_views(packed).items():
+            t = host_in.get(name)
+            if (t is None or t.untyped_storage().data_ptr() != base or t.storage_offset() != view.storage_offset()
+                    or t.shape != view.shape or t.stride() != view.stride()):
+                raise ValueError("host input %s is not the view of the packed buffer" % name)
+        if (host_out.device.type != "cpu" or not host_out.is_pinned() or host_out.shape != self.out.shape
+                or host_out.dtype != self.out.dtype):
+            raise ValueError("host output must be a pinned CPU tensor of shape %s" % (tuple(self.out.shape),))
+        self.host_in = packed
+        self.host_out = host_out
+
+    def io_bytes(self):
+        """(host-to-device, device-to-host) bytes one step copies with host I/O attached."""
+        if self.host_in is None:
+            return 0, 0
+        return self._in_dev.numel(), self.out.numel() * self.out.element_size()
+
+    # The compute stream copies the first layers' inputs in and the last layers' outputs out
+    # itself (sparda_copy: a copy kernel over the host link), because a DMA copy takes tens of
+    # microseconds from submission to completion and those copies sit on the critical path.
+    # The rest goes by DMA on the I/O stream, overlapped with the compute.
+    IO_HEAD = 4
+    IO_TAIL = 2
+
+    def _in_plan(self):
+        """[(first layer, end layer, how)]: the 'kernel' range is copied on the compute stream
+        at the start of the step; the 'dma' range by one copy on the I/O stream, waited on
+        before the first launch that reads it (layer IO_HEAD's prologue, ~4 layers later)."""
+        n = self.n_layers
+        k = min(self.IO_HEAD, n)
+        return [(0, k, "kernel")] + ([(k, n, "dma")] if k < n else [])
+
+    def _out_plan(self):
+        """[(first layer, end layer, how)]: 'dma' ranges (at most three) are copied on the I/O
+        stream once the attention of their last layer has run; the last IO_TAIL layers are
+        copied on the compute stream after the step's last launch."""
+        n = self.n_layers
+        m = n - min(self.IO_TAIL, n)
+        edges = sorted({0, m, m // 3, 2 * m // 3})
+        plan = [(a, b, "dma") for a, b in zip(edges[:-1], edges[1:]) if a < b]
+        return plan + [(m, n, "kernel")]
+
+    def _io_begin(self, main):
+        self._in_ready = {}
+        self._in_waited = set()
+        self._io_used = False
+        if self.host_in is None:
+            return
+        plan = self._in_plan()
+        for a, b, how in plan:
+            if how == "kernel":
+                sb.sparda_copy(self._in_dev[a:b], self.host_in[a:b], stream=main)
+        # the DMA starts once the first layers' inputs are in: both share the host link, and
+        # the first launches wait for those
+        for a, b, how in plan:
+            if how == "dma":
+                self._io_fork(main)
+                with torch.cuda.stream(self.io):
+                    self._in_dev[a:b].copy_(self.host_in[a:b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self.io)
+                self._in_ready[(a, b)] = ev
+
+    def _io_need_inputs(self, main, L):
+        """Before the first launch that reads layer L's inputs."""
+        for (a, b), ev in self._in_ready.items():
+            if a <= L < b and (a, b) not in self._in_waited:
+                main.wait_event(ev)
+                self._in_waited.add((a, b))
+
+    def _io_output_ready(self, main, L):
+        """After the launch that writes out[L]."""
+        if self.host_out is None:
+            return
+        for a, b, how in self._out_plan():
+            if b - 1 != L:
+                continue
+            if how == "kernel":
+                sb.sparda_copy(self.host_out[a:b], self.out[a:b], stream=main)
+            else:
+                self._io_fork(main)
+                with torch.cuda.stream(self.io):
+                    self.host_out[a:b].copy_(self.out[a:b], non_blocking=True)
+
+    def _io_fork(self, main):
+        """Order the I/O stream's next work after everything enqueued on main so far."""
+        ev = torch.cuda.Event()
+        ev.record(main)
+        self.io.wait_event(ev)
+        self._io_used = True
+
+    def _io_end(self, main):
+        if self._io_used:
+            main.wait_stream(self.io)
 
     # ------------------------------------------------------------------ one step
     def enqueue(self):
         """Enqueue one decode step on the current stream (plus the side streams)."""
+        main = torch.cuda.current_stream()
+        self._io_begin(main)
         if self.mode == "pipelined":
-            return self._enqueue_pipelined()
-        if self.mode == "fused":
-            return self._enqueue_fused()
+            self._enqueue_pipelined()
+        elif self.mode == "fused":
+            self._enqueue_fused()
+        else:
+            self._enqueue_streams()
+        self._io_end(main)
+
+    def _enqueue_streams(self):
         sh, B = self.shape, self.batch
         main = torch.cuda.current_stream()
         side = self.side
@@ -105,11 +254,13 @@ class DecodeStack:
         gather_done = [None] * self.n_layers
 
         # layer 0 selects its own blocks from a same-layer forecast
+        self._io_need_inputs(main, 0)
         sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
         sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
                                   self.idx[0], self.cnt[0], self.ws_sel, stream=main)
         for L in range(self.n_layers):
             layer = self.layers[L]
+            self._io_need_inputs(main, L)
             fork = ev()
             fork.record(main)
             if L + 1 < self.n_layers:
@@ -142,6 +293,7 @@ class DecodeStack:
             else:
                 sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
                                              self.out[L], self.ws_attn, stream=main)
+            self._io_output_ready(main, L)
             if self.after_attention is not None:
                 self.after_attention(L)
             attn_done[L] = ev()
@@ -160,12 +312,14 @@ class DecodeStack:
         sh, B, n = self.shape, self.batch, self.n_layers
         main = torch.cuda.current_stream()
         scores = (self.ws_sel, self.ws_sel2)
+        self._io_need_inputs(main, 0)
         sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
         sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
                                   self.idx[0], self.cnt[0], self.ws_sel, stream=main)
         for L in range(n):
             layer = self.layers[L]
             last = L + 1 == n
+            self._io_need_inputs(main, L)
             sb.sparda_decode_prologue(
                 sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B,
                 ws_scores=scores[L % 2] if L > 0 else None, idx=self.idx[L], cnt=self.cnt[L],
@@ -180,6 +334,7 @@ class DecodeStack:
                 sb.sparda_attend_and_score(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.out[L],
                                            self.ws_attn, self.layers[L + 1].ck, self.f[L + 1],
                                            scores[(L + 1) % 2], self.seq_len, B, l2_next=W2, stream=main)
+            self._io_output_ready(main, L)
             if self.after_attention is not None:
                 self.after_attention(L)
         if self.advance:
@@ -190,12 +345,14 @@ class DecodeStack:
         append of layer L, then layer L's attention together with layer L+1's selection."""
         sh, B = self.shape, self.batch
         main = torch.cuda.current_stream()
+        self._io_need_inputs(main, 0)
         sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
         sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
                                   self.idx[0], self.cnt[0], self.ws_sel, stream=main)
         for L in range(self.n_layers):
             layer = self.layers[L]
             last = L + 1 == self.n_layers
+            self._io_need_inputs(main, L)
             if not last:
                 sb.sparda_forecast_project(self.W_next[L], self.h[L], self.f[L + 1].view(B, -1), stream=main)
             sb.sparda_append_kv(sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B, stream=main)
@@ -208,6 +365,7 @@ class DecodeStack:
                 sb.sparda_attend_and_select(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.out[L],
                                             self.ws_attn, self.layers[L + 1].ck, self.f[L + 1],
                                             self.idx[L + 1], self.cnt[L + 1], ws, self.seq_len, B, stream=main)
+            self._io_output_ready(main, L)
             if self.after_attention is not None:
                 self.after_attention(L)
         if self.advance:

@@ -311,6 +311,21 @@ int32_t sparda_prefetch_blocks(const sparda_shape* shape, const sparda_layer_kv*
                                int32_t n_ctas, void* stream);
 
 /*
+ * sparda_copy -- a device-side copy of `bytes` bytes from src to dst, where each of them is
+ * device memory or pinned host memory mapped into the device's address space (its device
+ * address equals its host address). It serves the decode step's host I/O: the step's first
+ * inputs in and its last outputs out, on the compute stream, where a DMA copy's start-up
+ * latency (tens of microseconds on the host link) would sit on the critical path. Not an
+ * operation of the pages: plumbing around the step.
+ *
+ * dst and src 16-byte aligned, bytes a positive multiple of 16, the ranges not overlapping.
+ * Errors: SPARDA_ERR_INVALID_ARG (null pointer, zero or non-multiple-of-16 size),
+ * SPARDA_ERR_MISALIGNED, SPARDA_ERR_NOT_MAPPED_HOST (a pointer the device cannot address as
+ * given: pageable host memory, or pinned memory whose device address differs).
+ */
+int32_t sparda_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * sparda_multihead_select -- the baseline query-driven selector the pages compare against
  * (bittide thread; 10100 "先把痛点讲透"): every query head of the group scores every
  * compressed key (scale 1/sqrt(d)), a softmax per head over the windows, a sum over the

@@ -68,6 +68,11 @@ def test_bad_arguments_are_rejected_before_any_launch():
     offl = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, None, None, 1, 0)
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(offl), fake, fake, fake, 1, fake, fake, 0, None) == sb.ERR_INVALID_ARG
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(resident), fake, fake, fake, 1, fake, fake, -1, None) == sb.ERR_INVALID_ARG
+    assert sb.lib.sparda_copy(None, fake, 256, None) == sb.ERR_INVALID_ARG
+    assert sb.lib.sparda_copy(fake, fake, 0, None) == sb.ERR_INVALID_ARG
+    assert sb.lib.sparda_copy(fake, fake, 100, None) == sb.ERR_INVALID_ARG            # not a multiple of 16
+    assert sb.lib.sparda_copy(odd, fake, 256, None) == sb.ERR_MISALIGNED
+    assert sb.lib.sparda_copy(fake, odd, 256, None) == sb.ERR_MISALIGNED
 
 
 def test_pipelined_entries_reject_bad_arguments():

@@ -411,3 +411,27 @@ def test_append_window_means_round_exactly(sb):
     for g in range(2):
         assert torch.equal(got[g], want), (g, (got[g] != want).nonzero())
     _no_device_error(sb)
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096 + 16, 1 << 20, (64 << 20) + 48])
+def test_copy_between_device_and_pinned_host(sb, nbytes):
+    # sparda_copy: device to device, pinned host to device, device to pinned host; sizes from
+    # one 16-byte word to more words than one pass of the grid covers
+    n = nbytes // 2
+    g = torch.Generator().manual_seed(nbytes)
+    src_host = torch.randint(-30000, 30000, (n,), dtype=torch.int16, generator=g).pin_memory()
+    dev = torch.empty(n, dtype=torch.int16, device="cuda")
+    sb.sparda_copy(dev, src_host)
+    dev2 = torch.empty_like(dev)
+    sb.sparda_copy(dev2, dev)
+    back = torch.zeros(n, dtype=torch.int16).pin_memory()
+    sb.sparda_copy(back, dev2)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src_host)
+    assert torch.equal(dev2.cpu(), src_host)
+
+
+def test_copy_rejects_pageable_host_memory(sb):
+    dev = torch.empty(64, dtype=torch.int16, device="cuda")
+    with pytest.raises(sb.SpardaError):
+        sb.sparda_copy(dev, torch.zeros(64, dtype=torch.int16))          # not pinned

@@ -178,3 +178,54 @@ def test_single_layer_stack(sb, mode):
     torch.cuda.synchronize()
     assert compare(stack, sel, out, S, 1, 2, 2000, 8) >= 3
     assert sb.sparda_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("mode,offload", [("pipelined", ()), ("fused", ()), ("streams", ()), ("streams", (2, 3))])
+def test_host_io_step(sb, mode, offload):
+    # inputs from pinned host memory and outputs back to it, copied inside the step on the
+    # I/O stream: the same results as with the inputs already on the device, eager and from a
+    # CUDA graph
+    n_layers, B, T, topk, max_ctx, hidden = 6, 2, 2500, 8, 4096, 256
+    shape, stack, inputs = make_stack_case(sb, 15, n_layers, B, T, topk, max_ctx, hidden, 8, mode=mode,
+                                           offload=set(offload))
+    stack.enqueue()
+    torch.cuda.synchronize()
+    ref_out, ref_idx = stack.out.clone(), stack.idx.clone()
+    names = ("h", "q", "k_new", "v_new")
+    host_in = stack.pinned_inputs()
+    for n in names:
+        host_in[n].copy_(getattr(stack, n).cpu())
+    host_out = torch.zeros_like(stack.out, device="cpu").pin_memory()
+    with pytest.raises(ValueError):
+        stack.attach_host_io({**host_in, "q": host_in["q"].clone()}, host_out)   # not a view of packed
+    with pytest.raises(ValueError):
+        stack.attach_host_io({n: host_in[n] for n in names}, host_out)          # no packed buffer
+    with pytest.raises(ValueError):
+        stack.attach_host_io(host_in, host_out.clone())                        # output not pinned
+    stack.attach_host_io(host_in, host_out)
+    assert stack.io_bytes() == (host_in["packed"].numel(), stack.out.numel() * 2)
+    assert host_in["packed"].numel() >= sum(getattr(stack, n).numel() * 2 for n in names)
+
+    def clear():
+        for n in names:
+            getattr(stack, n).zero_()
+        stack.out.zero_()
+        stack.idx.fill_(-1)
+        host_out.zero_()
+        torch.cuda.synchronize()
+
+    clear()
+    stack.enqueue()
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, ref_out.cpu())
+    assert torch.equal(stack.idx, ref_idx)
+    clear()
+    stack.capture()
+    clear()
+    stack.run()
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, ref_out.cpu())
+    assert torch.equal(stack.idx, ref_idx)
+    stack.attach_host_io(None, None)
+    assert stack.io_bytes() == (0, 0)
+    assert sb.sparda_device_error(clear=True) == 0
