@@ -41,6 +41,8 @@ constexpr int kSelStages = 6;
 // with one group (a phase-parity wait cannot tell a stage's next phase from its last one)
 static_assert(kSelStages % 2 == 0, "each ring stage must belong to one consumer group");
 constexpr int kSelStageBytes = kSubRows * kRowBytes;
+// Queue ids a producer of the queue-fed selection holds before their use (see sel_cta_dyn).
+constexpr int kSelIdAhead = 2;
 constexpr int kSelSmem = 128 /*align slack*/ + 128 /*barriers*/ + kSelStages * kSelStageBytes;
 
 
@@ -312,11 +314,20 @@ __device__ __forceinline__ void sel_cta_dyn(const SelectArgs& a, int cta, int gr
     if (lane != 0) return;
     int it = 0;
     int ends = 0;                               // end markers pushed (one per consumer group)
+    // Queue ids are taken kSelIdAhead ahead of their use, so that the atomic's round trip
+    // (about a microsecond under load, longer when the counter's memory sits far from the SM)
+    // overlaps the wait for a free stage instead of adding to it.
+    int pend[kSelIdAhead];
+#pragma unroll
+    for (int k = 0; k < kSelIdAhead; ++k) pend[k] = (int)atomicAdd(a.queue, 1u);
     while (ends < 2) {
       int4 m = make_int4(-1, 0, 0, 0);
       int w0 = 0, w1 = 0;
       if (ends == 0) {
-        const int id = (int)atomicAdd(a.queue, 1u);
+        const int id = pend[0];
+#pragma unroll
+        for (int k = 0; k + 1 < kSelIdAhead; ++k) pend[k] = pend[k + 1];
+        pend[kSelIdAhead - 1] = id < n_items ? (int)atomicAdd(a.queue, 1u) : n_items;
         if (id < n_items) {
           const int bg = id / ipg, j0 = (id % ipg) * kSubBlocks;
           const SelGroup gr = sel_group(a, bg);
