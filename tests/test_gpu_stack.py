@@ -150,11 +150,14 @@ def test_offloaded_stack_step(sb, overlap):
     assert sb.sparda_device_error(clear=True) == 0
 
 
-def test_all_launch_modes_agree(sb):
+@pytest.mark.parametrize("B", [3, 17, 18])
+def test_all_launch_modes_agree(sb, B):
     # the same step launched as two kernels per layer (prologue with the top-k +
     # attend-and-score), three (projection, append, attend-and-select) or one kernel per job
-    # on two streams: the same arithmetic, bit-identical results
-    n_layers, B, T, topk, max_ctx, hidden = 4, 3, 3001, 8, 4096, 256
+    # on two streams: the same arithmetic, bit-identical results. B = 17 is the largest batch
+    # whose selection (34 sequence-groups) attend-and-score hands out from a queue; from
+    # B = 18 (36) each selection CTA takes a fixed range instead.
+    n_layers, T, topk, max_ctx, hidden = 4, 3001, 8, 4096, 256
     outs = []
     for mode in ("pipelined", "fused", "streams"):
         shape, stack, inputs = make_stack_case(sb, 11, n_layers, B, T, topk, max_ctx, hidden, 8, mode=mode)
