@@ -1,4 +1,4 @@
-// The standalone Forecast projection launch: one CTA per tile of 8 rows x 16 sequences (the
+// The standalone Forecast projection launch: one CTA per tile of 8 rows x kProjSeqs sequences (the
 // computation is project_rows in project_body.cuh).
 #include "project_body.cuh"
 
@@ -11,7 +11,7 @@ __global__ void __launch_bounds__(kProjThreads) forecast_project_kernel(const Pr
 }
 
 void launch_forecast_project(const ProjectArgs& a, cudaStream_t s) {
-  dim3 grid(a.rows / 8, (a.batch + 15) / 16);
+  dim3 grid(a.rows / 8, (a.batch + kProjSeqs - 1) / kProjSeqs);
   forecast_project_kernel<<<grid, kProjThreads, 0, s>>>(a);
 }
 

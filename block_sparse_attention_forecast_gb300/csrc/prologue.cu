@@ -9,8 +9,8 @@
 //     section 二).
 //
 // Each alone is a launch of a few microseconds that leaves most of the GPU idle; together they
-// cost one launch. The grid is cut into role ranges: projection tiles (8 rows x 16 sequences
-// each), then one top-k CTA per (sequence, group), then append CTAs of four (sequence, group)
+// cost one launch. The grid is cut into role ranges: projection tiles (8 rows x kProjSeqs
+// sequences each), then one top-k CTA per (sequence, group), then append CTAs of four (sequence, group)
 // pairs each. Every CTA first lets the next launch in the stream begin
 // (programmatic dependent launch: the attention kernel's producers and the selector's loads
 // start early) and then waits for the previous launch to complete.
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const
 
 void launch_decode_prologue(const PrologueArgs& args, cudaStream_t s) {
   PrologueArgs a = args;
-  a.n_proj = a.pj.W ? (a.pj.rows / 8) * ((a.pj.batch + 15) / 16) : 0;
+  a.n_proj = a.pj.W ? proj_ctas(a.pj.rows, a.pj.batch) : 0;
   a.n_topk = a.block_scores ? a.bg_count : 0;
   const int n_append = (a.bg_count + kAppendPerCta - 1) / kAppendPerCta;
   cudaLaunchConfig_t cfg = {};
