@@ -80,29 +80,37 @@ __device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
 // those buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
 // takes over and the output is assembled from per-block flags. Either way the result is exact
 // and ties go to the lower block index.
-static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_out, int topk, int max_ctx,
-                                   int T, TopkShared& sh) {
+template <int KPT>
+static __device__ void topk_select_impl(const float* S, int32_t* idx, int32_t* cnt_out, int topk, int max_ctx,
+                                        int T, TopkShared& sh) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // The loads of the whole score row (max_ctx / 64 entries: each stays inside it) do not wait
+  // for T, so they share one memory round trip with the caller's read of the sequence length.
+  const int nb_row = max_ctx / kBlock;
+  float v[KPT];
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    const int j = e * kTopkThreads + t;
+    v[e] = j < nb_row ? __ldcg(S + j) : 0.f;
+  }
   const int kslots = topk + 2;
   const bool valid = (T >= 1 && T <= max_ctx);
   const int tb = valid ? (T - 1) / kBlock : -1;
   const int nb = tb + 1;
   const int n_cand = max(0, tb - 1);
   const int k_eff = min(topk, n_cand);
-
-  float v[kKeysPerThread];
-  bool isc[kKeysPerThread];
+  bool isc[KPT];
 #pragma unroll
-  for (int e = 0; e < kKeysPerThread; ++e) {
+  for (int e = 0; e < KPT; ++e) {
     const int j = e * kTopkThreads + t;
     isc[e] = j >= 1 && j < tb;
-    v[e] = isc[e] ? __ldcg(S + j) : 0.f;
+    if (!isc[e]) v[e] = 0.f;
   }
 
   if (k_eff > 0 && k_eff < n_cand) {
     float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e)
+    for (int e = 0; e < KPT; ++e)
       if (isc[e]) {
         lo = fminf(lo, v[e]);
         hi = fmaxf(hi, v[e]);
@@ -125,10 +133,10 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     }
     const float scale = 256.f / (hi - lo);
     bool fast = hi > lo && isfinite(lo) && isfinite(hi) && isfinite(scale);   // CTA-uniform
-    int bk[kKeysPerThread];
+    int bk[KPT];
     if (fast) {
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
+      for (int e = 0; e < KPT; ++e) {
         bk[e] = isc[e] ? score_bucket(v[e], lo, scale) : -1;
         if (isc[e]) atomicAdd(&sh.hist[bk[e]], 1u);
       }
@@ -147,10 +155,10 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
       const int bstar = sh.bstar;
       // list the candidates at or above bucket bstar, in (warp, e, lane) order: one ballot
       // per register slot, per-warp totals exchanged once
-      unsigned bal[kKeysPerThread];
+      unsigned bal[KPT];
       int wcount = 0;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
+      for (int e = 0; e < KPT; ++e) {
         bal[e] = __ballot_sync(0xffffffffu, bk[e] >= bstar);
         wcount += __popc(bal[e]);
       }
@@ -162,7 +170,7 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
         if (w < warp) p += sh.warp_tot[w];
       const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
+      for (int e = 0; e < KPT; ++e) {
         if (bk[e] >= bstar) {
           const int q = p + __popc(bal[e] & below);
           sh.lv[q] = v[e];
@@ -222,19 +230,19 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
   topk_sync();
   if (k_eff == n_cand) {
 #pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e)
+    for (int e = 0; e < KPT; ++e)
       if (isc[e]) sh.flag[e * kTopkThreads + t] = 1;
   } else if (k_eff > 0) {
-    uint32_t key[kKeysPerThread];
+    uint32_t key[KPT];
 #pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
+    for (int e = 0; e < KPT; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
     uint32_t prefix = 0u, mask = 0u;
     int krem = k_eff;
     for (int shift = 24; shift >= 0; shift -= 8) {
       sh.hist[t] = 0u;
       topk_sync();
 #pragma unroll
-      for (int e = 0; e < kKeysPerThread; ++e) {
+      for (int e = 0; e < KPT; ++e) {
         const bool in = key[e] != 0u && (key[e] & mask) == prefix;
         if (in) atomicAdd(&sh.hist[(key[e] >> shift) & 255u], 1u);
       }
@@ -256,7 +264,7 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
     // of all threads at earlier e or, at the same e, lower t.
     int eq_before = 0;                    // equal keys at blocks below this thread's current one
 #pragma unroll
-    for (int e = 0; e < kKeysPerThread; ++e) {
+    for (int e = 0; e < KPT; ++e) {
       const bool eq = key[e] != 0u && key[e] == prefix;
       int tot_e;
       const int incl_e = topk_scan(eq ? 1 : 0, sh.warp_tot, &tot_e);
@@ -281,5 +289,16 @@ static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_ou
   if (t == 0) *cnt_out = min(total, kslots);
 }
 
+
+// Thread t holds the scores of blocks t, t + 256, ...: 8 of them up to 2048 blocks (128K
+// tokens), 16 beyond. The two instantiations run the same steps; the smaller one does half
+// the register work in every phase.
+static __device__ void topk_select(const float* S, int32_t* idx, int32_t* cnt_out, int topk, int max_ctx,
+                                   int T, TopkShared& sh) {
+  if (max_ctx / kBlock <= 8 * kTopkThreads)
+    topk_select_impl<8>(S, idx, cnt_out, topk, max_ctx, T, sh);
+  else
+    topk_select_impl<kKeysPerThread>(S, idx, cnt_out, topk, max_ctx, T, sh);
+}
 
 }  // namespace sparda

@@ -144,6 +144,7 @@ def test_select_tiny_planted(sb):
     ([4096, 4000, 1000, 3333], 8, 4096),
     ([8192, 7777, 5000, 6401], 32, 8192),     # k = 32, ragged tails
     ([16384, 9999], 62, 16384),               # the largest k
+    ([140000, 131073], 32, 262144),           # the largest context: 16 scores per top-k thread
 ])
 def test_select_ragged(sb, T_list, k, max_ctx):
     B = len(T_list)
