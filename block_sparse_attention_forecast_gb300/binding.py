@@ -23,7 +23,7 @@ __all__ = [
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
-    "sparda_attend_and_score", "sparda_decode_prologue",
+    "sparda_attend_and_score", "sparda_decode_prologue", "sparda_forecast_score", "sparda_copy",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
@@ -100,6 +100,7 @@ def _load():
         "sparda_attend_and_score": (I32, [SH, LY, P, P, P, P, P, P, P, SZ, P, P, P, SZ, P, SZ, P, I32, P]),
         "sparda_decode_prologue": (I32, [SH, LY, P, P, P, SZ, P, P, P, P, I32, P, P, I32, P]),
         "sparda_copy": (I32, [P, P, SZ, P]),
+        "sparda_forecast_score": (I32, [SH, P, P, P, I32, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -325,6 +326,14 @@ def sparda_prefetch_blocks(shape, layer, idx, cnt, seq_len, batch, staging_k, st
     _check("sparda_prefetch_blocks", lib.sparda_prefetch_blocks(
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(idx), _ptr(cnt), _ptr(seq_len),
         int(batch), _ptr(staging_k), _ptr(staging_v), int(n_ctas), _stream(stream)))
+
+
+def sparda_forecast_score(shape, ck, forecast, seq_len, batch, ws, stream=None):
+    """Block scores of the Forecast selector without the top-k, into the select workspace ws
+    (for sparda_decode_prologue's ws_scores)."""
+    _check("sparda_forecast_score", lib.sparda_forecast_score(
+        ctypes.byref(shape.c()), _ptr(ck), _ptr(forecast), _ptr(seq_len), int(batch), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def sparda_copy(dst, src, stream=None):

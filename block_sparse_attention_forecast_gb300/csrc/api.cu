@@ -11,6 +11,7 @@ using namespace sparda;
 
 namespace sparda {
 void launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);   // copy.cu
+void launch_forecast_score(const SelectArgs& a, int bg_count, cudaStream_t s);  // select.cu
 }
 
 // The device error word (bits SPARDA_DEV_*). Kernels receive its device address.
@@ -355,6 +356,15 @@ int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void
   SelectArgs a;
   SPARDA_TRY(prepare_select(s, ck, forecast, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
   launch_forecast_select(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_forecast_score(const sparda_shape* s, const void* ck, const void* forecast,
+                              const int32_t* seq_len, int32_t batch, void* ws, size_t ws_bytes,
+                              void* stream) {
+  SelectArgs a;
+  SPARDA_TRY(prepare_select(s, ck, forecast, seq_len, batch, nullptr, nullptr, ws, ws_bytes, &a, true));
+  launch_forecast_score(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

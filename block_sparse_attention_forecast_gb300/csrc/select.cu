@@ -11,6 +11,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) forecast_select_kernel(const S
   sel_cta(a, blockIdx.x, gridDim.x);
 }
 
+// The selection's block scores without the top-k, on every SM: sub-chunks handed out from the
+// workspace's queue when the forecasts of all (sequence, group)s fit beside the ring, fixed
+// ranges otherwise.
+constexpr int kScoreSmem = 256 + kSelStages * kSelStageBytes + kSelDynMaxGroups * kHeadDim * 2;
+static_assert(kScoreSmem <= 227 * 1024, "the queue-fed selection's ring and forecast table fit");
+
+__global__ void __launch_bounds__(kSelThreads, 1) forecast_score_kernel(const SelectArgs a) {
+  if (a.queue)
+    sel_cta_dyn(a, blockIdx.x, gridDim.x);
+  else
+    sel_cta(a, blockIdx.x, gridDim.x);
+}
+
 static int sel_sm_count() {
   static int n[64] = {0};
   int dev = 0;
@@ -43,6 +56,25 @@ void launch_forecast_select(const SelectArgs& a, int bg_count, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, forecast_select_kernel, b);
+}
+
+void launch_forecast_score(const SelectArgs& a, int bg_count, cudaStream_t s) {
+  cudaFuncSetAttribute(forecast_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+  SelectArgs b = a;
+  b.n_units = bg_count * a.nb_cap;
+  const int by_work = (b.n_units + kSubBlocks - 1) / kSubBlocks;
+  const int grid = by_work < sel_sm_count() ? by_work : sel_sm_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = kScoreSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, forecast_score_kernel, b);
 }
 
 }  // namespace sparda

@@ -308,21 +308,22 @@ class DecodeStack:
     def _enqueue_pipelined(self):
         """Resident stack, one stream, two launches per layer: layer L's prologue (its top-k,
         its append, the forecast for layer L+1), then layer L's attention beside the block
-        scores of layer L+1. Block scores alternate between two workspaces."""
+        scores of layer L+1. Block scores alternate between two workspaces. Layer 0's own
+        scores come first, from its same-layer forecast."""
         sh, B, n = self.shape, self.batch, self.n_layers
         main = torch.cuda.current_stream()
         scores = (self.ws_sel, self.ws_sel2)
         self._io_need_inputs(main, 0)
+        # layer 0's own selection: its block scores on every SM, its top-k in its prologue
         sb.sparda_forecast_project(self.W_self0, self.h[0], self.f[0].view(B, -1), stream=main)
-        sb.sparda_forecast_select(sh, self.layers[0].ck, self.f[0], self.seq_len, B,
-                                  self.idx[0], self.cnt[0], self.ws_sel, stream=main)
+        sb.sparda_forecast_score(sh, self.layers[0].ck, self.f[0], self.seq_len, B, scores[0], stream=main)
         for L in range(n):
             layer = self.layers[L]
             last = L + 1 == n
             self._io_need_inputs(main, L)
             sb.sparda_decode_prologue(
                 sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B,
-                ws_scores=scores[L % 2] if L > 0 else None, idx=self.idx[L], cnt=self.cnt[L],
+                ws_scores=scores[L % 2], idx=self.idx[L], cnt=self.cnt[L],
                 W_next=None if last else self.W_next[L], h=self.h[L],
                 forecast_next=None if last else self.f[L + 1].view(B, -1), stream=main)
             if last:

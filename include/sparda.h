@@ -199,6 +199,16 @@ int32_t sparda_forecast_select(const sparda_shape* shape, const void* ck, const 
                                void* stream);
 
 /*
+ * sparda_forecast_score -- sparda_forecast_select without its top-k: the block scores S[j]
+ * (float32, j < (T-1)/64 + 1) are left in the workspace (SPARDA_WS_SELECT), for
+ * sparda_decode_prologue's top-k (its ws_scores) to select from, as sparda_attend_and_score
+ * leaves them. All SMs stream the compressed keys. Errors: as sparda_forecast_select.
+ */
+int32_t sparda_forecast_score(const sparda_shape* shape, const void* ck, const void* forecast,
+                              const int32_t* seq_len, int32_t batch, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * sparda_sparse_decode_attn -- block-sparse GQA decode attention (bittide thread: the next
  * layer's own queries attend the selected blocks; techwalker §六: the sparse attention
  * itself is unchanged by SparDA). For every query head h of group g:

@@ -68,6 +68,9 @@ def test_bad_arguments_are_rejected_before_any_launch():
     offl = sb.c_layer_kv(1 << 20, 1 << 20, 1 << 20, None, None, 1, 0)
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(offl), fake, fake, fake, 1, fake, fake, 0, None) == sb.ERR_INVALID_ARG
     assert sb.lib.sparda_prefetch_blocks(sh, ctypes.byref(resident), fake, fake, fake, 1, fake, fake, -1, None) == sb.ERR_INVALID_ARG
+    assert sb.lib.sparda_forecast_score(sh, None, fake, fake, 1, fake, 1 << 20, None) == sb.ERR_INVALID_ARG
+    assert sb.lib.sparda_forecast_score(sh, odd, fake, fake, 1, fake, 1 << 20, None) == sb.ERR_MISALIGNED
+    assert sb.lib.sparda_forecast_score(sh, fake, fake, fake, 1, fake, 16, None) == sb.ERR_WORKSPACE_TOO_SMALL
     assert sb.lib.sparda_copy(None, fake, 256, None) == sb.ERR_INVALID_ARG
     assert sb.lib.sparda_copy(fake, fake, 0, None) == sb.ERR_INVALID_ARG
     assert sb.lib.sparda_copy(fake, fake, 100, None) == sb.ERR_INVALID_ARG            # not a multiple of 16

@@ -369,6 +369,36 @@ def test_decode_prologue_equals_its_three_calls(sb):
     _no_device_error(sb)
 
 
+@pytest.mark.parametrize("B", [3, 18])
+def test_score_then_prologue_top_k_equals_select(sb, B):
+    # sparda_forecast_score leaves the block scores that sparda_decode_prologue's top-k turns
+    # into exactly the selection sparda_forecast_select makes; B = 3 takes the queue-fed
+    # scoring (6 sequence-groups), B = 18 the fixed ranges (36)
+    k, max_ctx = 8, 4096
+    T_list = [max_ctx - 7 * b for b in range(B)]
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 73, B)
+    f = synth.normal_bf16((B, 2, 128), 74, B).cuda()
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    sb.sparda_compress_keys(shape, layer, seq - 1, B)
+    idx_a = torch.full((B, 2, k + 2), -9, dtype=torch.int32, device="cuda")
+    cnt_a = torch.full((B, 2), -9, dtype=torch.int32, device="cuda")
+    idx_b, cnt_b = idx_a.clone(), cnt_a.clone()
+    ws_a = sb.workspace(shape, B, sb.WS_SELECT)
+    ws_b = sb.workspace(shape, B, sb.WS_SELECT)
+    sb.sparda_forecast_select(shape, layer.ck, f, seq, B, idx_a, cnt_a, ws_a)
+    kn = torch.zeros((B, 2, 128), dtype=torch.bfloat16, device="cuda")
+    for rep in range(2):                                  # the workspace is reusable as left
+        sb.sparda_forecast_score(shape, layer.ck, f, seq, B, ws_b)
+        sb.sparda_decode_prologue(shape, sb.LayerKV.empty(shape), kn, kn, seq, B, ws_scores=ws_b, idx=idx_b,
+                                  cnt=cnt_b)
+        torch.cuda.synchronize()
+        assert torch.equal(idx_a, idx_b) and torch.equal(cnt_a, cnt_b)
+    _no_device_error(sb)
+
+
 def test_append_window_means_round_exactly(sb):
     # The window that token 31 completes, built so that the exact means hit the cases that a
     # slip in the append's exact summation and rounding would get wrong: halfway cases that
