@@ -133,7 +133,7 @@ __device__ __forceinline__ float2 lse_combine(float2 x, float2 y) {
   return make_float2(M, x.y * exp2f(x.x - M) + y.y * exp2f(y.x - M));
 }
 
-__global__ void __launch_bounds__(kTopkThreads) multihead_pool_topk_kernel(const MultiheadArgs a) {
+__global__ void __launch_bounds__(kTopkThreads, 1) multihead_pool_topk_kernel(const MultiheadArgs a) {
   extern __shared__ float s_win[];                 // [W_cap] summed probabilities
   __shared__ TopkShared sh;
   __shared__ float s_M[kHeads], s_invL[kHeads];
