@@ -12,6 +12,7 @@ using namespace sparda;
 namespace sparda {
 void launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);   // copy.cu
 void launch_forecast_score(const SelectArgs& a, int bg_count, cudaStream_t s);  // select.cu
+void launch_select_topk(const SelectArgs& a, int bg_count, cudaStream_t s);     // select.cu
 }
 
 // The device error word (bits SPARDA_DEV_*). Kernels receive its device address.
@@ -355,7 +356,20 @@ int32_t sparda_forecast_select(const sparda_shape* s, const void* ck, const void
                                void* ws, size_t ws_bytes, void* stream) {
   SelectArgs a;
   SPARDA_TRY(prepare_select(s, ck, forecast, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
-  launch_forecast_select(a, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  const int bgc = batch * s->n_groups;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bgc <= kSelDynMaxGroups) {
+    // the block scores on every SM, handed out from the workspace's queue, then one top-k CTA
+    // per (sequence, group): the queue keeps the SMs busy to the end, which a top-k tail on
+    // the last CTA of each group does not
+    SelectArgs sc = a;
+    sc.queue = static_cast<unsigned*>(ws);
+    sc.do_topk = 0;
+    launch_forecast_score(sc, bgc, st);
+    launch_select_topk(a, bgc, st);
+  } else {
+    launch_forecast_select(a, bgc, st);
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -1,5 +1,6 @@
-// Launch of the standalone Forecast selector kernel; its per-CTA work is sel_cta
-// (select_body.cuh), which the fused attend-and-select kernel (fused.cu) shares.
+// Launches of the standalone Forecast selector: the selector kernel, whose per-CTA work is
+// sel_cta (select_body.cuh, shared with the fused attend-and-select kernel, fused.cu); the
+// scores-only kernel (queue-fed when it can be); and the top-k behind it.
 #include "select_body.cuh"
 
 namespace sparda {
@@ -56,6 +57,31 @@ void launch_forecast_select(const SelectArgs& a, int bg_count, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, forecast_select_kernel, b);
+}
+
+// The top-k of block scores a scoring launch left in the workspace: one CTA per (sequence,
+// group), launched behind that scoring launch (programmatic dependent launch).
+__global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectArgs a) {
+  __shared__ TopkShared sh;
+  const int bg = blockIdx.x;
+  grid_dep_wait();
+  const int T = a.seq_len[bg / a.G];
+  topk_select(a.block_scores + (size_t)bg * a.nb_cap, a.idx + (size_t)bg * (a.topk + 2), a.cnt + bg, a.topk,
+              a.max_ctx, T, sh);
+}
+
+void launch_select_topk(const SelectArgs& a, int bg_count, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(bg_count);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, select_topk_kernel, a);
 }
 
 void launch_forecast_score(const SelectArgs& a, int bg_count, cudaStream_t s) {
