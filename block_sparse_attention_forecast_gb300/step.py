@@ -143,8 +143,9 @@ class DecodeStack:
                     or t.shape != view.shape or t.stride() != view.stride()):
                 raise ValueError("host input %s is not the view of the packed buffer" % name)
         if (host_out.device.type != "cpu" or not host_out.is_pinned() or host_out.shape != self.out.shape
-                or host_out.dtype != self.out.dtype):
-            raise ValueError("host output must be a pinned CPU tensor of shape %s" % (tuple(self.out.shape),))
+                or host_out.dtype != self.out.dtype or not host_out.is_contiguous()):
+            raise ValueError("host output must be a contiguous pinned CPU tensor of shape %s"
+                             % (tuple(self.out.shape),))
         self.host_in = packed
         self.host_out = host_out
 
