@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
     const AttnArgs aa, const SelectArgs sa, int n_attn, const __grid_constant__ CUtensorMap mk,
     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap hk,
     const __grid_constant__ CUtensorMap hv) {
+  grid_dep_launch();                   // the next prologue's projection may take freed SMs
   if ((int)blockIdx.x < n_attn)
     attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x, n_attn);
   else if (sa.queue)

@@ -11,9 +11,14 @@
 // Each alone is a launch of a few microseconds that leaves most of the GPU idle; together they
 // cost one launch. The grid is cut into role ranges: projection tiles (8 rows x kProjSeqs
 // sequences each), then one top-k CTA per (sequence, group), then append CTAs of four (sequence, group)
-// pairs each. Every CTA first lets the next launch in the stream begin
-// (programmatic dependent launch: the attention kernel's producers and the selector's loads
-// start early) and then waits for the previous launch to complete.
+// pairs each. The projection reads only the layer's hidden state and weights, which no
+// launch of the step writes, so its CTAs neither wait for the previous launch nor hold back
+// the next: the previous launch (attention beside the selection) lets this one begin while it
+// runs, and the projection tiles, first in the grid, start on the SMs its attention CTAs
+// release while its selection CTAs still stream. The top-k and append CTAs wait for the
+// previous launch to complete, and only then let the next launch begin (programmatic
+// dependent launch: its selection producers start streaming compressed keys during the top-k),
+// so the next launch never begins before the previous one has completed.
 #include "append_body.cuh"
 #include "project_body.cuh"
 #include "topk.cuh"
@@ -31,14 +36,15 @@ union PrologueShared {
 
 __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const PrologueArgs a) {
   __shared__ PrologueShared sh;
-  grid_dep_launch();
-  grid_dep_wait();
   int c = blockIdx.x;
-  if (c < a.n_proj) {
+  if (c < a.n_proj) {                  // reads only the layer's inputs and weights: no wait
+    grid_dep_launch();
     const int n_tiles = a.pj.rows / 8;
     project_rows(a.pj, c % n_tiles, c / n_tiles, sh.pj, 1);
     return;
   }
+  grid_dep_wait();
+  grid_dep_launch();                   // only once the previous launch has completed
   c -= a.n_proj;
   if (c < a.n_topk) {
     if (c < a.bg_count) {

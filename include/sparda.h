@@ -274,7 +274,9 @@ int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_k
  * ws_attn (SPARDA_ERR_INVALID_ARG otherwise). l2_next (optional, NULL for none; 16-byte
  * aligned, l2_next_bytes a multiple of 16) names device memory that the next launches will
  * read, such as layer L+1's forecast weights for its prologue: the selection CTAs pull it
- * into L2 after issuing their last load. It changes no result.
+ * into L2 after issuing their last load. It changes no result. Every CTA lets the next
+ * launch in the stream begin as soon as it starts (programmatic dependent launch), so a
+ * following sparda_decode_prologue's projection starts on the SMs that finished CTAs free.
  */
 int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv* layer,
                                 const void* staging_k, const void* staging_v, const void* q,
@@ -294,8 +296,13 @@ int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv
  *     sparda_forecast_project with rows = G*d (W_next: device bf16 [G*d, hidden] row-major,
  *     h: device bf16 [B, hidden], forecast_next: device bf16 [B, G, d]; hidden a multiple of
  *     32).
- * The three jobs read and write disjoint buffers. The launch waits for the previous kernel in
- * the stream before any of them starts. Errors: as the three separate calls.
+ * The three jobs read and write disjoint buffers. The top-k and the append wait for the
+ * previous kernel in the stream to complete. The projection does not wait: when that kernel
+ * is sparda_attend_and_score or sparda_attend_and_select (which let the next launch begin
+ * once all their CTAs run), it runs on the SMs they release, beside their last CTAs. So
+ * W_next and h must not be written, nor forecast_next read, by the kernel just before this
+ * launch in the stream (no kernel of this library writes them). Errors: as the three
+ * separate calls.
  */
 int32_t sparda_decode_prologue(const sparda_shape* shape, const sparda_layer_kv* layer,
                                const void* k_new, const void* v_new, const void* ws_scores,
