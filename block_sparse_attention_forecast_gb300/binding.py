@@ -19,7 +19,8 @@ __all__ = [
     "lib", "LIB_PATH", "HEADER_PATH", "SpardaError", "Shape", "LayerKV", "workspace",
     "hot_slot", "fill_hot_from_host",
     "header_functions", "status_string", "num_windows", "c_shape", "c_layer_kv",
-    "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes", "sparda_device_error",
+    "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes",
+    "sparda_block_scores_offset", "sparda_device_error",
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
@@ -86,6 +87,7 @@ def _load():
         "sparda_status_string": (ctypes.c_char_p, [I32]),
         "sparda_check_shape": (I32, [SH]),
         "sparda_workspace_bytes": (SZ, [SH, I32, I32]),
+        "sparda_block_scores_offset": (SZ, [SH]),
         "sparda_device_error": (I32, [ctypes.POINTER(I32), I32]),
         "sparda_prefetch_default_ctas": (I32, [I32]),
         "sparda_append_kv": (I32, [SH, LY, P, P, P, I32, P]),
@@ -248,6 +250,10 @@ def sparda_check_shape(shape):
 
 def sparda_workspace_bytes(shape, batch, kind):
     return lib.sparda_workspace_bytes(ctypes.byref(shape.c()), int(batch), int(kind))
+
+
+def sparda_block_scores_offset(shape):
+    return lib.sparda_block_scores_offset(ctypes.byref(shape.c()))
 
 
 def sparda_device_error(clear=True):

@@ -210,6 +210,10 @@ size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind
   }
 }
 
+size_t sparda_block_scores_offset(const sparda_shape* s) {
+  return shape_status(s) == SPARDA_OK ? kQueueBytes + counters_bytes(s) : 0;
+}
+
 int32_t sparda_device_error(int32_t* flags, int32_t clear) {
   if (!flags) return SPARDA_ERR_INVALID_ARG;
   int* p = dev_error_ptr();
@@ -463,7 +467,7 @@ int32_t sparda_decode_prologue(const sparda_shape* s, const sparda_layer_kv* L, 
   a.pj = ProjectArgs{static_cast<const __nv_bfloat16*>(W_next), static_cast<const __nv_bfloat16*>(h),
                      static_cast<__nv_bfloat16*>(forecast_next), s->n_groups * kHeadDim, hidden, batch};
   a.block_scores = ws_scores ? reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws_scores) +
-                                                              kQueueBytes + counters_bytes(s))
+                                                              sparda_block_scores_offset(s))
                              : nullptr;
   a.idx = idx;
   a.cnt = cnt;

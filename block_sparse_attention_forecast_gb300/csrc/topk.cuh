@@ -40,46 +40,51 @@ __device__ __forceinline__ int topk_scan(int v, int* warp_tot, int* total) {
 }
 
 constexpr int kMaxList = 512;          // candidates ranked exactly by the fast path
+static_assert(kMaxTopk <= 64, "the chosen blocks fit TopkShared::sel");
+
+// Order-preserving 32-bit key of a block score, with -0 keyed as +0 so that equal scores get
+// equal keys (ties then go to the lower block, as for any other equal pair). Every finite
+// score's key is above 0, the key of a non-candidate.
+__device__ __forceinline__ uint32_t score_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return ordered_key(__uint_as_float(u == 0x80000000u ? 0u : u));
+}
 
 struct TopkShared {
   unsigned hist[256];
   int warp_tot[kTopkWarps];
-  float red_lo[kTopkWarps], red_hi[kTopkWarps];
+  uint32_t warp_th[kTopkWarps];
+  int warp_bad[kTopkWarps];
   uint32_t prefix;
   int krem;
   int last;
-  int bstar;
-  int n_ge;
-  float lv[kMaxList];
-  int lj[kMaxList];
-  int lr[kMaxList];                    // exact rank of each listed candidate
+  uint64_t lp[kMaxList];               // listed candidates: score key << 32 | ~block
+  int sel[64];                         // the chosen blocks, by rank
   unsigned char flag[kMaxBlocksPerSeq];
 };
-
-// Bucket of a candidate score in the 256 equal slices of [lo, hi]: floor((x - lo) * scale),
-// taken as the low mantissa bits of 2^23 + that product added with rounding down (an FP32
-// add instead of a float-to-int conversion). Monotone non-decreasing in x (a subtraction, a
-// positive scaling and a rounded-down add, each monotone), so every candidate in a higher
-// bucket outscores every candidate in a lower one.
-__device__ __forceinline__ int score_bucket(float x, float lo, float scale) {
-  const float y = __fadd_rd(fmaxf((x - lo) * scale, 0.f), 8388608.f);
-  return min(255, __float_as_int(y) & 0x7fffff);
-}
 
 // Top-k of one (sequence, group) by 256 threads (threads 0-255 of the CTA, synchronised with
 // named barrier 1), from the block scores S[0 .. nb) in global memory. Writes idx[0 .. topk+2)
 // (block 0, the chosen blocks ascending, the tail block; -1 padded) and *cnt_out.
 //
 // Thread t holds the scores of blocks t, t + 256, t + 512, ... (each warp load is one
-// contiguous 128-byte line). Fast path: min/max of the candidate scores; a 256-bucket
-// histogram over that range (shared-memory atomics); the bucket that holds the k-th score,
-// found by a scan from the top; the candidates at or above that bucket -- a few dozen for real
-// score distributions -- listed in shared memory by ballots and per-warp counts; their exact ranks
-// (score descending, block ascending) by pairwise comparison; and the output position of each
-// chosen block by counting the chosen blocks below it. If more than kMaxList candidates share
-// those buckets (near-constant scores), a 4-pass radix select on order-preserving 32-bit keys
-// takes over and the output is assembled from per-block flags. Either way the result is exact
-// and ties go to the lower block index.
+// contiguous 128-byte line). Fast path, four barriers in all:
+//   * a threshold that at least k candidates reach: each warp takes the q-th largest of its
+//     32 lane maxima (q = ceil(k / 8)) by q warp-wide max reductions of order-preserving keys,
+//     and the threshold is the smallest of the 8 warps' values. Every warp holds at least q
+//     candidates at or above its own value, so at least 8q >= k reach the threshold, and every
+//     candidate of the top k is among them (a warp with fewer than q candidate lanes lowers the
+//     threshold to take every candidate);
+//   * those candidates -- a few dozen for real score distributions -- listed in shared memory
+//     by ballots and per-warp counts;
+//   * their exact ranks (score descending, block ascending) by comparing each candidate's
+//     packed key (score key above, inverted block index below: one 64-bit order) with every
+//     other, one thread per candidate over broadcast loads; each chosen block written at its
+//     rank, and then placed by counting the chosen blocks below it.
+// If more than kMaxList candidates reach the threshold (near-constant scores), or a candidate
+// score is not finite, a 4-pass radix select on order-preserving 32-bit keys takes over and
+// the output is assembled from per-block flags. Either way the result is exact and ties go to
+// the lower block index.
 template <int KPT>
 static __device__ void topk_select_impl(const float* S, int32_t* idx, int32_t* cnt_out, int topk, int max_ctx,
                                         int T, TopkShared& sh) {
@@ -108,112 +113,92 @@ static __device__ void topk_select_impl(const float* S, int32_t* idx, int32_t* c
   }
 
   if (k_eff > 0 && k_eff < n_cand) {
-    float lo = INFINITY, hi = -INFINITY;
+    // keys of the candidates, 0 for the others
+    uint32_t key[KPT];
+    uint32_t lane_max = 0u;
+    bool bad = false;
 #pragma unroll
-    for (int e = 0; e < KPT; ++e)
+    for (int e = 0; e < KPT; ++e) {
+      key[e] = 0u;
       if (isc[e]) {
-        lo = fminf(lo, v[e]);
-        hi = fmaxf(hi, v[e]);
+        bad |= !isfinite(v[e]);
+        key[e] = score_key(v[e]);
+        lane_max = max(lane_max, key[e]);
       }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
+    // the q-th largest lane maximum of this warp, the lanes counted with multiplicity
+    const int quota = (k_eff + kTopkWarps - 1) / kTopkWarps;
+    uint32_t th = 1u, cur = lane_max;
+    int got = 0;
+    for (int r = 0; r < quota; ++r) {             // warp-uniform: m and got are
+      const uint32_t m = __reduce_max_sync(0xffffffffu, cur);
+      if (m == 0u) {                              // fewer than quota candidate lanes: all
+        th = 1u;
+        break;
+      }
+      got += __popc(__ballot_sync(0xffffffffu, cur == m));
+      th = m;
+      if (got >= quota) break;
+      if (cur == m) cur = 0u;
+    }
+    const bool warp_bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      sh.red_lo[warp] = lo;
-      sh.red_hi[warp] = hi;
+      sh.warp_th[warp] = th;
+      sh.warp_bad[warp] = warp_bad ? 1 : 0;
     }
-    sh.hist[t] = 0u;
     topk_sync();
+    uint32_t theta = 0xffffffffu;
+    bool any_bad = false;
 #pragma unroll
     for (int w = 0; w < kTopkWarps; ++w) {
-      lo = fminf(lo, sh.red_lo[w]);
-      hi = fmaxf(hi, sh.red_hi[w]);
+      theta = min(theta, sh.warp_th[w]);
+      any_bad |= sh.warp_bad[w] != 0;
     }
-    const float scale = 256.f / (hi - lo);
-    bool fast = hi > lo && isfinite(lo) && isfinite(hi) && isfinite(scale);   // CTA-uniform
-    int bk[KPT];
-    if (fast) {
+    // list the candidates at or above the threshold, in (warp, e, lane) order: one ballot per
+    // register slot, per-warp totals exchanged once
+    unsigned bal[KPT];
+    int wcount = 0;
 #pragma unroll
-      for (int e = 0; e < KPT; ++e) {
-        bk[e] = isc[e] ? score_bucket(v[e], lo, scale) : -1;
-        if (isc[e]) atomicAdd(&sh.hist[bk[e]], 1u);
-      }
-      topk_sync();
-      const int hv = (int)sh.hist[255 - t];      // thread t looks at bucket 255 - t
-      int tot;
-      const int incl = topk_scan(hv, sh.warp_tot, &tot);
-      if (incl - hv < k_eff && incl >= k_eff) {
-        sh.bstar = 255 - t;
-        sh.n_ge = incl;
-      }
-      topk_sync();
-      fast = sh.n_ge <= kMaxList;
+    for (int e = 0; e < KPT; ++e) {
+      bal[e] = __ballot_sync(0xffffffffu, key[e] >= theta);
+      wcount += __popc(bal[e]);
     }
-    if (fast) {
-      const int bstar = sh.bstar;
-      // list the candidates at or above bucket bstar, in (warp, e, lane) order: one ballot
-      // per register slot, per-warp totals exchanged once
-      unsigned bal[KPT];
-      int wcount = 0;
+    if (lane == 0) sh.warp_tot[warp] = wcount;
+    topk_sync();
+    int p = 0, c = 0;
 #pragma unroll
-      for (int e = 0; e < KPT; ++e) {
-        bal[e] = __ballot_sync(0xffffffffu, bk[e] >= bstar);
-        wcount += __popc(bal[e]);
-      }
-      if (lane == 0) sh.warp_tot[warp] = wcount;
-      topk_sync();
-      int p = 0;
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w)
-        if (w < warp) p += sh.warp_tot[w];
+    for (int w = 0; w < kTopkWarps; ++w) {
+      const int x = sh.warp_tot[w];
+      if (w < warp) p += x;
+      c += x;
+    }
+    if (!any_bad && c <= kMaxList) {                // CTA-uniform
       const unsigned below = (1u << lane) - 1u;
 #pragma unroll
       for (int e = 0; e < KPT; ++e) {
-        if (bk[e] >= bstar) {
-          const int q = p + __popc(bal[e] & below);
-          sh.lv[q] = v[e];
-          sh.lj[q] = e * kTopkThreads + t;
+        if (key[e] >= theta) {
+          const uint32_t j = (uint32_t)(e * kTopkThreads + t);
+          sh.lp[p + __popc(bal[e] & below)] = ((uint64_t)key[e] << 32) | (uint64_t)(~j);
         }
         p += __popc(bal[e]);
       }
       topk_sync();
-      // exact rank of each listed candidate: `split` threads share one candidate, each
-      // scanning a slice of the list
-      const int c = sh.n_ge;
-      const int split = c <= 32 ? 8 : (c <= 64 ? 4 : (c <= 128 ? 2 : 1));
-      for (int i0 = 0; i0 < c * split; i0 += kTopkThreads) {
-        const int q = i0 + t;
-        const int i = q / split, part = q % split;
+      // exact rank of each listed candidate: the number of listed packed keys above its own
+      for (int i = t; i < c; i += kTopkThreads) {
+        const uint64_t mine = sh.lp[i];
         int rank = 0;
-        if (i < c) {
-          const float vi = sh.lv[i];
-          const int ji = sh.lj[i];
-          for (int m = part; m < c; m += split) {
-            const float vm = sh.lv[m];
-            rank += (vm > vi) || (vm == vi && sh.lj[m] < ji);
-          }
-        }
-        for (int o = 1; o < split; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        if (i < c && part == 0) sh.lr[i] = rank;
+#pragma unroll 8
+        for (int m = 0; m < c; ++m) rank += sh.lp[m] > mine ? 1 : 0;
+        if (rank < k_eff) sh.sel[rank] = (int)~(uint32_t)mine;
       }
       topk_sync();
       // output: block 0, the chosen blocks in ascending order, the tail block (tb >= 2 here)
-      for (int i0 = 0; i0 < c * split; i0 += kTopkThreads) {
-        const int q = i0 + t;
-        const int i = q / split, part = q % split;
+      if (t < k_eff) {
+        const int ji = sh.sel[t];
         int pos = 0;
-        bool chosen = false;
-        int ji = 0;
-        if (i < c) {
-          chosen = sh.lr[i] < k_eff;
-          ji = sh.lj[i];
-          if (chosen)
-            for (int m = part; m < c; m += split) pos += (sh.lr[m] < k_eff && sh.lj[m] < ji);
-        }
-        for (int o = 1; o < split; o <<= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
-        if (chosen && part == 0) idx[1 + pos] = ji;
+#pragma unroll 8
+        for (int m = 0; m < k_eff; ++m) pos += sh.sel[m] < ji ? 1 : 0;
+        idx[1 + pos] = ji;
       }
       if (t == 0) {
         idx[0] = 0;
@@ -235,7 +220,7 @@ static __device__ void topk_select_impl(const float* S, int32_t* idx, int32_t* c
   } else if (k_eff > 0) {
     uint32_t key[KPT];
 #pragma unroll
-    for (int e = 0; e < KPT; ++e) key[e] = isc[e] ? ordered_key(v[e]) : 0u;
+    for (int e = 0; e < KPT; ++e) key[e] = isc[e] ? score_key(v[e]) : 0u;
     uint32_t prefix = 0u, mask = 0u;
     int krem = k_eff;
     for (int shift = 24; shift >= 0; shift -= 8) {

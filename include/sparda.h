@@ -128,6 +128,14 @@ int32_t sparda_check_shape(const sparda_shape* shape);
  * sequences; 0 for an unsupported shape. */
 size_t sparda_workspace_bytes(const sparda_shape* shape, int32_t batch, int32_t kind);
 
+/* Byte offset, inside a SPARDA_WS_SELECT workspace, of its block scores: float32
+ * [max_batch * G][max_ctx / 64], row b*G + g holding S[j] of (b, g). sparda_forecast_select,
+ * sparda_forecast_score and sparda_attend_and_score leave the scores there, and
+ * sparda_decode_prologue's top-k reads them, so a caller may inspect them or write its own
+ * for the top-k to select from (entries j >= (T-1)/64 + 1 are not read for selection).
+ * 0 for an unsupported shape. */
+size_t sparda_block_scores_offset(const sparda_shape* shape);
+
 /* Reads the device error word (bits SPARDA_DEV_*) of the current device into *flags and,
  * if clear != 0, resets it. Synchronous: waits for all work on the device. */
 int32_t sparda_device_error(int32_t* flags, int32_t clear);

@@ -45,6 +45,10 @@ def test_workspace_sizes():
     assert sb.sparda_workspace_bytes(s, 0, sb.WS_SELECT) == 0
     assert sb.sparda_workspace_bytes(s, 17, sb.WS_SELECT) == 0
     assert sb.sparda_workspace_bytes(s, 4, 99) == 0
+    # the block scores fill the end of the selection workspace, after its counters
+    off = sb.sparda_block_scores_offset(s)
+    assert off % 16 == 0 and 16 * 2 * 4 <= off and off + 16 * 2 * nb * 4 <= sel
+    assert sb.sparda_block_scores_offset(sb.Shape(max_ctx=100)) == 0
     assert sb.sparda_prefetch_default_ctas(31) == 64 and sb.sparda_prefetch_default_ctas(32) == 152
 
 

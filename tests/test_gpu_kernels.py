@@ -399,6 +399,58 @@ def test_score_then_prologue_top_k_equals_select(sb, B):
     _no_device_error(sb)
 
 
+def _planted_scores(kind, nb, rng):
+    S = rng.standard_normal(nb).astype(np.float32)
+    if kind == "signed_zeros":          # -0 and +0 are equal scores: ties go to the lower block
+        S = np.where(rng.random(nb) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+        S[rng.choice(nb, 5, replace=False)] = 1.0
+        S[rng.choice(nb, 5, replace=False)] = -1.0
+    elif kind == "plateau":             # more equal maxima than the fast path lists
+        S -= 10.0
+        S[rng.choice(nb, nb * 3 // 4, replace=False)] = 3.0
+    elif kind == "few_distinct":        # heavy ties at every level
+        S = rng.integers(0, 4, nb).astype(np.float32)
+    elif kind == "one_warp_high":       # every high score in the lanes of one top-k warp
+        S[np.arange(nb) % 256 < 32] += 100.0
+    elif kind == "infinities":          # non-finite scores rank above / below every finite one
+        S[rng.choice(nb, 3, replace=False)] = np.inf
+        S[rng.choice(nb, 40, replace=False)] = -np.inf
+    return S
+
+
+@pytest.mark.parametrize("kind", ["normal", "signed_zeros", "plateau", "few_distinct", "one_warp_high",
+                                  "infinities"])
+@pytest.mark.parametrize("k,max_ctx", [(32, 131072), (62, 262144), (8, 8192)])
+def test_prologue_top_k_of_planted_scores(sb, kind, k, max_ctx):
+    # block scores written straight into the selection workspace: the prologue's top-k must
+    # give exactly the oracle's selection (block 0, the tail block and the k best others, ties
+    # to the lower block) for each (sequence, group) row, whatever the score distribution
+    nb = max_ctx // 64
+    T_list = [max_ctx, max_ctx - 100 * 64 + 5, 300 * 64 + 1 if max_ctx > 300 * 64 else 40 * 64, 3 * 64, 33 * 64 + 1]
+    B = len(T_list)
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    G = shape.n_groups
+    rng = np.random.default_rng([5, k, nb, len(kind)])
+    S = np.stack([_planted_scores(kind, nb, rng) for _ in range(B * G)])
+    ws = sb.workspace(shape, B, sb.WS_SELECT)
+    off = sb.sparda_block_scores_offset(shape)
+    ws[off:off + S.nbytes].view(torch.float32).view(B * G, nb).copy_(torch.from_numpy(S))
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    kn = torch.zeros((B, G, 128), dtype=torch.bfloat16, device="cuda")
+    idx = torch.full((B, G, k + 2), -9, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, G), -9, dtype=torch.int32, device="cuda")
+    sb.sparda_decode_prologue(shape, sb.LayerKV.empty(shape), kn, kn, seq, B, ws_scores=ws, idx=idx, cnt=cnt)
+    torch.cuda.synchronize()
+    idx, cnt = idx.cpu(), cnt.cpu()
+    for b, T in enumerate(T_list):
+        for g in range(G):
+            want = O.select_blocks(S[b * G + g].astype(np.float64), T, k)
+            got = idx[b, g].tolist()
+            assert cnt[b, g].item() == len(want), (kind, b, g)
+            assert got == want + [-1] * (k + 2 - len(want)), (kind, b, g)
+    _no_device_error(sb)
+
+
 def test_append_window_means_round_exactly(sb):
     # The window that token 31 completes, built so that the exact means hit the cases that a
     # slip in the append's exact summation and rounding would get wrong: halfway cases that
