@@ -11,14 +11,18 @@
 // Each alone is a launch of a few microseconds that leaves most of the GPU idle; together they
 // cost one launch. The grid is cut into role ranges: projection tiles (8 rows x kProjSeqs
 // sequences each), then one top-k CTA per (sequence, group), then append CTAs of four (sequence, group)
-// pairs each. The projection reads only the layer's hidden state and weights, which no
-// launch of the step writes, so its CTAs neither wait for the previous launch nor hold back
-// the next: the previous launch (attention beside the selection) lets this one begin while it
-// runs, and the projection tiles, first in the grid, start on the SMs its attention CTAs
-// release while its selection CTAs still stream. The top-k and append CTAs wait for the
-// previous launch to complete, and only then let the next launch begin (programmatic
-// dependent launch: its selection producers start streaming compressed keys during the top-k),
-// so the next launch never begins before the previous one has completed.
+// pairs each. Only the top-k reads what the previous launch (attention beside the selection)
+// writes: the layer's block scores. The projection reads the layer's hidden state and
+// weights, and the append writes the token's key/value and the window it completes, which
+// that launch does not read (it scores windows [0, num_windows(T-1)) of this layer, and the
+// token completes window num_windows(T-1)). So only the top-k CTAs wait for the previous
+// launch to complete; the others start as soon as SMs free up -- the previous launch lets
+// this one begin while it runs, and the projection tiles, first in the grid, take the SMs its
+// attention CTAs release while its selection CTAs still stream. The top-k CTAs let the next
+// launch begin only after their wait (programmatic dependent launch: its selection producers
+// start streaming compressed keys during the top-k), so the next launch never begins before
+// the previous one has completed. A launch without a top-k has its append CTAs wait instead,
+// so that it still completes after the previous launch.
 #include "append_body.cuh"
 #include "project_body.cuh"
 #include "topk.cuh"
@@ -43,10 +47,10 @@ __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const
     project_rows(a.pj, c % n_tiles, c / n_tiles, sh.pj, 1);
     return;
   }
-  grid_dep_wait();
-  grid_dep_launch();                   // only once the previous launch has completed
   c -= a.n_proj;
-  if (c < a.n_topk) {
+  if (c < a.n_topk) {                  // the scores are the previous launch's output
+    grid_dep_wait();
+    grid_dep_launch();                 // only once the previous launch has completed
     if (c < a.bg_count) {
       const int T = a.ap.seq_len[c / a.ap.G];
       topk_select(a.block_scores + (size_t)c * a.nb_cap, a.idx + (size_t)c * (a.topk + 2), a.cnt + c,
@@ -54,6 +58,8 @@ __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const
     }
     return;
   }
+  if (a.n_topk == 0) grid_dep_wait();
+  grid_dep_launch();
   c -= a.n_topk;
   const int bg = c * kAppendPerCta + (int)threadIdx.x / 64;
   if (bg < a.bg_count) append_token(a.ap, bg, threadIdx.x % 64);

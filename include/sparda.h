@@ -304,13 +304,15 @@ int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv
  *     sparda_forecast_project with rows = G*d (W_next: device bf16 [G*d, hidden] row-major,
  *     h: device bf16 [B, hidden], forecast_next: device bf16 [B, G, d]; hidden a multiple of
  *     32).
- * The three jobs read and write disjoint buffers. The top-k and the append wait for the
- * previous kernel in the stream to complete. The projection does not wait: when that kernel
- * is sparda_attend_and_score or sparda_attend_and_select (which let the next launch begin
- * once all their CTAs run), it runs on the SMs they release, beside their last CTAs. So
- * W_next and h must not be written, nor forecast_next read, by the kernel just before this
- * launch in the stream (no kernel of this library writes them). Errors: as the three
- * separate calls.
+ * The three jobs read and write disjoint buffers. Only the top-k waits for the previous
+ * kernel in the stream to complete (the append waits too when ws_scores is NULL). The
+ * projection and the append do not: when that kernel is sparda_attend_and_score or
+ * sparda_attend_and_select (which let the next launch begin once all their CTAs run), they
+ * run on the SMs it releases, beside its last CTAs. So the kernel just before this launch in
+ * the stream must not write W_next, h, k_new or v_new, nor read forecast_next, the layer's
+ * key/value at position T-1 or its compressed key of the window the token completes
+ * (sparda_attend_and_score of the layer before reads only the windows below it). Errors:
+ * as the three separate calls.
  */
 int32_t sparda_decode_prologue(const sparda_shape* shape, const sparda_layer_kv* layer,
                                const void* k_new, const void* v_new, const void* ws_scores,
