@@ -195,11 +195,19 @@ def kernel_times(stack, reps=4):
     import block_sparse_attention_forecast_gb300.binding as sb
     sh, B, n = stack.shape, stack.batch, stack.n_layers
     scores = (stack.ws_sel, stack.ws_sel2)
+    # Each attend-and-score / attend-and-select launch lets the next one begin while it runs,
+    # so consecutive launches must not share a selection workspace: they alternate by launch
+    # count, also across the captured repetitions (31 launches each).
+    launch = [0]
+
+    def next_scores():
+        launch[0] += 1
+        return scores[launch[0] % 2]
 
     def score_loop(s):
         for L in range(n - 1):
             sb.sparda_attend_and_score(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
-                                       stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], scores[(L + 1) % 2],
+                                       stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], next_scores(),
                                        stack.seq_len, B, l2_next=stack.W_next[L + 1] if L + 2 < n else None,
                                        stream=s)
 
@@ -216,7 +224,7 @@ def kernel_times(stack, reps=4):
         for L in range(n - 1):
             sb.sparda_attend_and_select(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
                                         stack.ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], stack.idx[L + 1],
-                                        stack.cnt[L + 1], scores[(L + 1) % 2], stack.seq_len, B, stream=s)
+                                        stack.cnt[L + 1], next_scores(), stack.seq_len, B, stream=s)
 
     def sel_loop(s):
         for L in range(1, n):

@@ -2,10 +2,13 @@
 // launch. Under lookahead the two are independent (layer L's forecast already exists when
 // layer L attends), and each alone is a persistent kernel that wants every SM, so launched
 // side by side they would only run one after the other. Here the grid is one CTA per SM,
-// split between the two jobs in proportion to the bytes each must stream: CTAs [0, n_attn)
-// run the attention work (attn_cta) over the attention units, the others the selection work
-// (sel_cta) over the selection units, so both jobs stream concurrently from HBM and finish
-// together, with one launch and one start-up per layer.
+// split between the two jobs in proportion to the bytes each must stream: the first CTAs run
+// the selection work (sel_cta) over the selection units, the last n_attn the attention work
+// (attn_cta) over the attention units, so both jobs stream concurrently from HBM and finish
+// together, with one launch and one start-up per layer. The selection CTAs come first because
+// the launch begins while the next layer's top-k CTAs of the launch before still hold SMs:
+// the selection, which does not depend on them, streams on the SMs free at the start, and
+// the attention CTAs, which need that top-k's blocks, take the SMs its CTAs release.
 #include "attn_body.cuh"
 #include "select_body.cuh"
 
@@ -24,12 +27,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap hk,
     const __grid_constant__ CUtensorMap hv) {
   grid_dep_launch();                   // the next prologue's projection may take freed SMs
-  if ((int)blockIdx.x < n_attn)
-    attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x, n_attn);
+  const int n_sel = (int)gridDim.x - n_attn;
+  if ((int)blockIdx.x >= n_sel)
+    attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x - n_sel, n_attn);
   else if (sa.queue)
-    sel_cta_dyn(sa, blockIdx.x - n_attn, gridDim.x - n_attn);
+    sel_cta_dyn(sa, blockIdx.x, n_sel);
   else
-    sel_cta(sa, blockIdx.x - n_attn, gridDim.x - n_attn);
+    sel_cta(sa, blockIdx.x, n_sel);
 }
 
 int sm_count();
