@@ -197,7 +197,9 @@ def kernel_times(stack, reps=4):
     scores = (stack.ws_sel, stack.ws_sel2)
     # Each attend-and-score / attend-and-select launch lets the next one begin while it runs,
     # so consecutive launches must not share a selection workspace: they alternate by launch
-    # count, also across the captured repetitions (31 launches each).
+    # count, also across the captured repetitions (31 launches each). Two suffice here: the
+    # grid holds one CTA on every SM, so a launch is fully resident, and the one after it can
+    # begin, only once the launch before it has exited.
     launch = [0]
 
     def next_scores():

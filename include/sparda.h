@@ -285,10 +285,11 @@ int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_k
  * into L2 after issuing their last load. It changes no result. Every CTA lets the next
  * launch in the stream begin as soon as it starts (programmatic dependent launch), so a
  * following sparda_decode_prologue's projection starts on the SMs that finished CTAs free.
- * Two of these calls (or of sparda_attend_and_select) directly after one another in a stream
- * therefore overlap, and their ws_scores must differ (the selection's work queue lives
- * there); with a sparda_decode_prologue between them, as in the decode step, the second
- * begins only after the first has completed.
+ * A run of these calls (or of sparda_attend_and_select) directly after one another in a
+ * stream therefore overlaps: as many as fit on the GPU may run at once, so give each call of
+ * such a run its own ws_scores (the selection's work queue lives there; ws_attn may be
+ * shared). With a sparda_decode_prologue between two calls, as in the decode step, the
+ * second begins only after the first has completed, and two workspaces alternating suffice.
  */
 int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv* layer,
                                 const void* staging_k, const void* staging_v, const void* q,

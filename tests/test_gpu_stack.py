@@ -171,6 +171,52 @@ def test_all_launch_modes_agree(sb, B):
     assert sb.sparda_device_error(clear=True) == 0
 
 
+@pytest.mark.parametrize("call", ["score", "select"])
+@pytest.mark.parametrize("B", [3, 18])
+def test_back_to_back_attend_calls(sb, call, B):
+    # Each attend-and-score / attend-and-select launch lets the next launch begin while it
+    # runs, so calls directly after one another on a stream overlap (at these small shapes
+    # the grids leave SMs free, so more than two may run at once). With a selection workspace
+    # of its own for each call (the rule the header states), the calls give exactly what the
+    # same calls give one at a time; in the attend-and-select chain each call's attention
+    # reads the blocks the call before selected. B = 3 hands the selection out from a queue,
+    # B = 18 in fixed ranges.
+    n_layers, T, topk, max_ctx, hidden = 5, 4097, 32, 8192, 256
+    shape, stack, _ = make_stack_case(sb, 37, n_layers, B, T, topk, max_ctx, hidden, 8)
+    stack.enqueue()                                  # idx, cnt and forecasts of every layer
+    torch.cuda.synchronize()
+    idx0, cnt0 = stack.idx.clone(), stack.cnt.clone()
+    off = sb.sparda_block_scores_offset(shape)
+    n_sc = B * shape.n_groups * (max_ctx // 64) * 4
+
+    def run(sync):
+        stack.idx.copy_(idx0)
+        stack.cnt.copy_(cnt0)
+        stack.out.zero_()
+        torch.cuda.synchronize()
+        ws = [sb.workspace(shape, B, sb.WS_SELECT) for _ in range(n_layers - 1)]
+        ws_attn = sb.workspace(shape, B, sb.WS_ATTN)
+        for L in range(n_layers - 1):
+            w = ws[L]
+            if call == "score":
+                sb.sparda_attend_and_score(shape, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L], stack.out[L],
+                                           ws_attn, stack.layers[L + 1].ck, stack.f[L + 1], w, stack.seq_len, B)
+            else:
+                sb.sparda_attend_and_select(shape, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L],
+                                            stack.out[L], ws_attn, stack.layers[L + 1].ck, stack.f[L + 1],
+                                            stack.idx[L + 1], stack.cnt[L + 1], w, stack.seq_len, B)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        scores = torch.stack([w[off:off + n_sc] for w in ws])
+        return stack.idx.clone(), stack.cnt.clone(), stack.out[:n_layers - 1].clone(), scores
+
+    ref, got = run(True), run(False)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    assert sb.sparda_device_error(clear=True) == 0
+
+
 @pytest.mark.parametrize("mode", ["pipelined", "fused"])
 def test_single_layer_stack(sb, mode):
     # one layer: layer 0's own selection, its prologue without a top-k or projection, its
