@@ -198,7 +198,7 @@ int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int3
  *   S[j] = max { s[i] : window i overlaps block j }   (windows 4j-1 .. 4j+3)
  *   chosen = the topk highest S[j] over 1 <= j < tb (ties -> lower j; -0 and +0 are equal
  *            scores; an infinity ranks above or below every finite score; a NaN score, which
- *            finite inputs cannot produce, has no defined rank)
+ *            only overflowing inputs can produce, has no defined rank)
  * Output idx: int32 [B, G, topk+2], the blocks {0, tb} U chosen sorted ascending, then -1
  * padding; cnt: int32 [B, G], the number of valid entries (min(topk, tb-1) + 2, or 1 when
  * tb = 0). forecast: device bf16 [B, G, d]. workspace: SPARDA_WS_SELECT.
