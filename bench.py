@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -106,7 +107,7 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % device_index)
+        self.path = os.path.join(tempfile.gettempdir(), "sparda_clocks_%d_%d.csv" % (os.getpid(), device_index))
 
     def start(self):
         try:
@@ -315,12 +316,13 @@ def graph_time(fn, reps=1):
 
 
 def run_offload(device, seed, steps, warmup):
-    """BASELINE config 4: batch 64, context 131072, 32 layers; layer 0 resident, layers 1-31
-    with their K/V in pinned host memory (gathered over the host link by the persistent UVA
-    kernel on a side stream), compressed keys and hot blocks in HBM, and a stand-in bf16 FFN
-    GEMM [64 x 4096] x [4096 x 14336] after every attention. The host holds 4 distinct K/V
-    pairs (8 GiB each) shared round-robin by layers 1-31: the GPU machine has about 200 GB of RAM,
-    and aliasing leaves the bytes gathered per step unchanged. Measured with the gather
+    """The offloaded decode step: batch 64, context 131072, 32 layers; layer 0 resident, layers
+    1-31 with their K/V in pinned host memory (gathered over the host link by the persistent
+    UVA kernel on a side stream), compressed keys and hot blocks in HBM, and a stand-in bf16
+    FFN GEMM [64 x 4096] x [4096 x 14336] after every attention. 31 layers of K/V at this size
+    would take ~266 GB of pinned host memory, more than a host with a few hundred GB can pin
+    beside everything else, so the host holds 4 distinct K/V pairs (8.6 GB each) shared
+    round-robin by layers 1-31; aliasing leaves the bytes gathered per step unchanged. Measured with the gather
     overlapped, with it waited on right after selection, and against the same step with
     every layer resident (4 distinct resident K/V pairs, same aliasing)."""
     import gc
@@ -449,7 +451,7 @@ def run_offload(device, seed, steps, warmup):
 
 # ---------------------------------------------------------------------- selector A/B
 def selector_ab(device, seed):
-    """BASELINE config 5: one layer's selection, the Forecast selector (one head per group, no
+    """The selector A/B: one layer's selection, the Forecast selector (one head per group, no
     softmax) against the baseline multi-head selector (16 query heads per group, softmax per
     head, sum, max-pool, top-32), for batch 1..128 at context 131072 and for context 32K..128K
     at batch 16. Compressed keys, forecasts and queries are seeded N(0,1) bf16 drawn on the

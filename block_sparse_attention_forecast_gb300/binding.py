@@ -20,7 +20,7 @@ __all__ = [
     "hot_slot", "fill_hot_from_host",
     "header_functions", "status_string", "num_windows", "c_shape", "c_layer_kv",
     "sparda_abi_version", "sparda_status_string", "sparda_check_shape", "sparda_workspace_bytes",
-    "sparda_block_scores_offset", "sparda_device_error",
+    "sparda_block_scores_offset", "sparda_device_error", "sparda_get_device_status",
     "sparda_prefetch_default_ctas", "sparda_append_kv", "sparda_compress_keys",
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
@@ -89,6 +89,7 @@ def _load():
         "sparda_workspace_bytes": (SZ, [SH, I32, I32]),
         "sparda_block_scores_offset": (SZ, [SH]),
         "sparda_device_error": (I32, [ctypes.POINTER(I32), I32]),
+        "sparda_get_device_status": (I32, [P, I32, P]),
         "sparda_prefetch_default_ctas": (I32, [I32]),
         "sparda_append_kv": (I32, [SH, LY, P, P, P, I32, P]),
         "sparda_compress_keys": (I32, [SH, LY, P, I32, P]),
@@ -260,6 +261,13 @@ def sparda_device_error(clear=True):
     flags = ctypes.c_int32(0)
     _check("sparda_device_error", lib.sparda_device_error(ctypes.byref(flags), 1 if clear else 0))
     return flags.value
+
+
+def sparda_get_device_status(dev_flag, clear=True, stream=None):
+    """Enqueue a stream-ordered copy of the device error word into dev_flag (an int32 tensor
+    of one element on the device, or pinned on the host), resetting the word if clear."""
+    _check("sparda_get_device_status", lib.sparda_get_device_status(_ptr(dev_flag), 1 if clear else 0,
+                                                                      _stream(stream)))
 
 
 def sparda_prefetch_default_ctas(batch):

@@ -11,6 +11,7 @@ using namespace sparda;
 
 namespace sparda {
 void launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s);   // copy.cu
+void launch_device_status(int* err, int32_t* out, bool clear, cudaStream_t s);  // copy.cu
 void launch_forecast_score(const SelectArgs& a, int bg_count, cudaStream_t s);  // select.cu
 void launch_select_topk(const SelectArgs& a, int bg_count, cudaStream_t s);     // select.cu
 }
@@ -222,6 +223,16 @@ int32_t sparda_device_error(int32_t* flags, int32_t clear) {
   SPARDA_TRY(cuda_status(cudaMemcpy(flags, p, sizeof(int), cudaMemcpyDeviceToHost)));
   if (clear) SPARDA_TRY(cuda_status(cudaMemset(p, 0, sizeof(int))));
   return SPARDA_OK;
+}
+
+int32_t sparda_get_device_status(int32_t* dev_flag, int32_t clear, void* stream) {
+  if (!dev_flag) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(dev_flag, 4)) return SPARDA_ERR_MISALIGNED;
+  SPARDA_TRY(device_addressable_status(dev_flag));
+  int* p = dev_error_ptr();
+  if (!p) return SPARDA_ERR_CUDA;
+  launch_device_status(p, dev_flag, clear != 0, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
 }
 
 int32_t sparda_prefetch_default_ctas(int32_t batch) { return batch < 32 ? 64 : 152; }

@@ -41,6 +41,17 @@ __global__ void __launch_bounds__(kCopyThreads) copy16_kernel(uint4* dst, const 
 
 int sm_count();
 
+// The stream-ordered read of the device error word: one thread copies it out and, when asked,
+// resets it in the same atomic step, so that a bit set by a kernel running elsewhere on the
+// device is either reported now or kept for the next read.
+__global__ void device_status_kernel(int* err, int32_t* out, int clear) {
+  *out = clear ? atomicExch(err, 0) : atomicOr(err, 0);
+}
+
+void launch_device_status(int* err, int32_t* out, bool clear, cudaStream_t s) {
+  device_status_kernel<<<1, 1, 0, s>>>(err, out, clear ? 1 : 0);
+}
+
 void launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t s) {
   const size_t n16 = bytes / 16;
   const size_t per_cta = (size_t)kCopyThreads * kCopyInFlight;

@@ -43,11 +43,15 @@ constexpr int kMaxList = 512;          // candidates ranked exactly by the fast 
 static_assert(kMaxTopk <= 64, "the chosen blocks fit TopkShared::sel");
 
 // Order-preserving 32-bit key of a block score, with -0 keyed as +0 so that equal scores get
-// equal keys (ties then go to the lower block, as for any other equal pair). Every finite
-// score's key is above 0, the key of a non-candidate.
+// equal keys (ties then go to the lower block, as for any other equal pair). Every NaN, of
+// either sign and any payload, is keyed as the largest key, above +inf: all NaNs rank alike,
+// above every number, and none can take key 0, the key of a non-candidate. Every other
+// score's key lies strictly between.
 __device__ __forceinline__ uint32_t score_key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return ordered_key(__uint_as_float(u == 0x80000000u ? 0u : u));
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  else if ((u & 0x7fffffffu) > 0x7f800000u) u = 0x7fffffffu;
+  return ordered_key(__uint_as_float(u));
 }
 
 struct TopkShared {

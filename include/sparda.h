@@ -40,6 +40,10 @@
  *     device memory, zero-filled before their first use (cudaMemset). Every call leaves
  *     the workspace's counters at zero again, so it can be reused without clearing.
  *     Two calls that may run at the same time must not share a workspace.
+ *   - The library looks up the device address of its own device variables (the error word,
+ *     the allocation-free entry's scratch) once per device and keeps it for the life of the
+ *     process. A cudaDeviceReset() unloads the library's device code, which may come back at
+ *     another address: do not call into the library after resetting a device it has used.
  */
 #ifndef SPARDA_H_
 #define SPARDA_H_
@@ -140,6 +144,17 @@ size_t sparda_block_scores_offset(const sparda_shape* shape);
  * if clear != 0, resets it. Synchronous: waits for all work on the device. */
 int32_t sparda_device_error(int32_t* flags, int32_t clear);
 
+/* The stream-ordered status read: enqueues on `stream` (a cudaStream_t as void*) a one-thread
+ * kernel that writes the device error word (bits SPARDA_DEV_*) into *dev_flag and, if
+ * clear != 0, resets the word in the same atomic step. dev_flag: 4-byte aligned device memory,
+ * or pinned host memory mapped into the device's address space (its device address equals
+ * its host address). Nothing waits on the host: the value covers every kernel ordered before
+ * this call in `stream` (and any other work the device had finished); read *dev_flag after
+ * synchronising with the stream or with an event recorded behind the call. The call may be
+ * captured into a CUDA graph. Errors: SPARDA_ERR_INVALID_ARG (null), SPARDA_ERR_MISALIGNED,
+ * SPARDA_ERR_NOT_MAPPED_HOST (memory the device cannot address as given). */
+int32_t sparda_get_device_status(int32_t* dev_flag, int32_t clear, void* stream);
+
 /* Copy-CTA count the gather uses by default for a batch: 64 below batch 32, 152 (one per
  * GB300 SM) from 32 on. The techwalker article (section 三) uses 16 / 32 copy CTAs on H100;
  * the same batch-adaptive rule was re-measured here for this library's copy CTAs, which are
@@ -156,8 +171,11 @@ int32_t sparda_prefetch_default_ctas(int32_t batch);
  *
  * k_new, v_new: device bf16 [B, G, d]. For every sequence b (T = seq_len[b]) the token is
  * written at position T-1. When T >= 32 and (T - 32) % 16 == 0 a window completes and
- * ck[b, g, (T-32)/16, :] = bf16(mean of keys T-32 .. T-1) is written; the mean is formed in
- * float64 (exact for bf16 keys of ordinary range) and rounded to nearest even.
+ * ck[b, g, (T-32)/16, :] = bf16(mean of keys T-32 .. T-1) is written: the exact mean rounded
+ * once to bf16, nearest even. Each dimension's window sum is formed exactly in a 64-bit
+ * fixed-point integer (47 fractional bits) when every key of the window is zero or of
+ * magnitude in [2^-40, 2^11); otherwise in float64, rounded to bf16 through a round-to-odd
+ * float32 so that no double rounding occurs. Both give the same bf16 code as the exact mean.
  * Offloaded layers: the token goes to the hot tail slot; when it fills its block (T % 64
  * == 0) that block is also written to the host cache, so that a later gather finds it.
  */
@@ -198,10 +216,18 @@ int32_t sparda_forecast_project(const void* W, const void* h, int32_t rows, int3
  *   S[j] = max { s[i] : window i overlaps block j }   (windows 4j-1 .. 4j+3)
  *   chosen = the topk highest S[j] over 1 <= j < tb (ties -> lower j; -0 and +0 are equal
  *            scores; an infinity ranks above or below every finite score; a NaN score, which
- *            only overflowing inputs can produce, has no defined rank)
+ *            only inputs whose float32 products or sums overflow can produce, ranks above
+ *            every number, all NaNs alike, and is still counted as a candidate)
  * Output idx: int32 [B, G, topk+2], the blocks {0, tb} U chosen sorted ascending, then -1
  * padding; cnt: int32 [B, G], the number of valid entries (min(topk, tb-1) + 2, or 1 when
  * tb = 0). forecast: device bf16 [B, G, d]. workspace: SPARDA_WS_SELECT.
+ * Ordering: the call begins while the kernel before it in the stream still runs
+ * (programmatic dependent launch). Its compressed-key loads do not wait for that kernel;
+ * everything else (the forecast, seq_len, the workspace, idx, cnt) does. So the kernel just
+ * before this call in the stream must not write the compressed keys it scores (the windows
+ * i < W of every sequence). sparda_append_kv of the same layer writes only the window the
+ * current token completes, which is not scored, and sparda_forecast_project writes only the
+ * forecast: both may come just before it.
  */
 int32_t sparda_forecast_select(const sparda_shape* shape, const void* ck, const void* forecast,
                                const int32_t* seq_len, int32_t batch, int32_t* idx,
@@ -212,7 +238,9 @@ int32_t sparda_forecast_select(const sparda_shape* shape, const void* ck, const 
  * sparda_forecast_score -- sparda_forecast_select without its top-k: the block scores S[j]
  * (float32, j < (T-1)/64 + 1) are left in the workspace (SPARDA_WS_SELECT), for
  * sparda_decode_prologue's top-k (its ws_scores) to select from, as sparda_attend_and_score
- * leaves them. All SMs stream the compressed keys. Errors: as sparda_forecast_select.
+ * leaves them. All SMs stream the compressed keys. Errors and the ordering rule (the
+ * kernel just before this call must not write the compressed keys it scores): as
+ * sparda_forecast_select.
  */
 int32_t sparda_forecast_score(const sparda_shape* shape, const void* ck, const void* forecast,
                               const int32_t* seq_len, int32_t batch, void* workspace,

@@ -251,6 +251,17 @@ def test_bad_seq_len_and_index_set_device_error(sb):
     ws = sb.workspace(shape, 2, sb.WS_SELECT)
     f = torch.zeros((2, 2, 128), dtype=torch.bfloat16, device="cuda")
     sb.sparda_forecast_select(shape, layer.ck, f, seq, 2, idx, cnt, ws)
+    # the stream-ordered read sees the bit and clears it; the blocking read then finds it clear
+    flag = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    sb.sparda_get_device_status(flag, clear=True)
+    torch.cuda.synchronize()
+    assert flag.item() & sb.DEV_BAD_SEQ_LEN
+    assert sb.sparda_device_error(clear=True) == 0
+    host_flag = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    sb.sparda_get_device_status(host_flag, clear=False)
+    torch.cuda.synchronize()
+    assert host_flag.item() == 0
+    sb.sparda_forecast_select(shape, layer.ck, f, seq, 2, idx, cnt, ws)
     assert sb.sparda_device_error(clear=True) & sb.DEV_BAD_SEQ_LEN
     assert cnt.abs().sum().item() == 0 and (idx == -1).all()
     # a block index beyond the sequence is skipped and reported, never dereferenced

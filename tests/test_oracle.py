@@ -168,6 +168,52 @@ def test_topk_picks_highest_scores_not_lowest():
     assert O.select_blocks(S, 4 * 64 + 1, 1) == [0, 2, 4]
 
 
+def test_topk_boundary_hand_cases():
+    # T in block 5 -> forced {0, 5}; candidates 1..4 score 5, 2, 1, 9. Block 0 (100) and the
+    # tail block 5 (50) are the two largest scores, and must not count as candidates.
+    S = np.array([100.0, 5, 2, 1, 9, 50])
+    T = 5 * 64 + 10
+    assert O.topk_boundary(S, T, 1) == (9.0, 5.0)
+    assert O.topk_boundary(S, T, 2) == (5.0, 2.0)
+    assert O.topk_boundary(S, T, 3) == (2.0, 1.0)
+    # k = number of candidates: a k-th but no (k+1)-th; k beyond it: neither
+    assert O.topk_boundary(S, T, 4) == (1.0, None)
+    assert O.topk_boundary(S, T, 5) == (None, None)
+    # ties: the k-th and (k+1)-th of equal candidates are equal
+    St = np.array([0.0, 3, 7, 3, 3, 0])
+    assert O.topk_boundary(St, T, 2) == (3.0, 3.0)
+    assert O.topk_boundary(St, T, 1) == (7.0, 3.0)
+    # no candidates at all (the context ends in block 0 or 1)
+    assert O.topk_boundary(S, 64, 1) == (None, None)
+    assert O.topk_boundary(S, 65, 1) == (None, None)
+    # blocks past the tail are not candidates even if their score is the largest
+    assert O.topk_boundary(np.array([0.0, 4, 1, 8, 99, 99]), 3 * 64 + 1, 1) == (4.0, 1.0)
+
+
+def test_topk_boundary_brackets_the_selection():
+    """The k-th value is the smallest chosen candidate score and the (k+1)-th the largest
+    unchosen one (by brute force over the selection), and the selection is unique exactly
+    when they differ."""
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        T = int(rng.integers(1, 64 * 30))
+        tb = (T - 1) // 64
+        S = rng.integers(-3, 4, tb + 3).astype(np.float64)
+        k = int(rng.integers(1, 10))
+        cand = [j for j in range(tb + 1) if j not in (0, tb)]
+        chosen = [j for j in _brute_select(S, T, k) if j not in (0, tb)]
+        left = [j for j in cand if j not in chosen]
+        kth, k1 = O.topk_boundary(S, T, k)
+        if k <= len(cand):
+            assert kth == min(S[j] for j in chosen)
+        else:
+            assert kth is None
+        if left and k < len(cand):
+            assert k1 == max(S[j] for j in left)
+        else:
+            assert k1 is None
+
+
 # ---------------------------------------------------------------- baseline selector
 def test_multihead_scores_closed_form():
     ck = np.array([[1.0, 0.0], [0.0, 0.0]])
