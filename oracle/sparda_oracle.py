@@ -1,4 +1,5 @@
-"""Plain, slow fp64 CPU oracle of the SparDA forecast-driven block-sparse decode step.
+"""Plain, slow fp64 CPU oracle of the SparDA forecast-driven block-sparse decode step and of
+its chunked prefill.
 
 TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline
 leg of ``bench.py`` may import this module. The product path (the CUDA library under
@@ -350,3 +351,128 @@ def decode_step(layers, W_self0, W_next, h, q, k_new, v_new, p, topk, heads_per_
                                                                    sel[L][b][g], T, block)
         out[L] = o
     return sel, out
+
+
+# --------------------------------------------------------------------------------------
+# Prefill: chunked queries
+# --------------------------------------------------------------------------------------
+# The pages measure prefill as well as decode ([thread] and the abstract: up to 1.25x faster
+# prefill; [techwalker] §五, the per-layer breakdown: in prefill the block-sparse attention
+# dominates, the block selection grows with the context and is close to it at 128K, and the
+# Forecast indexer cuts the selection cost by up to 2.5x while the attention is unchanged;
+# [10100]: in prefill all keys are already on the GPU, so the gain is the cheaper selection
+# alone). They do not spell the prefill selection out. The readings taken here:
+#
+#   * the prompt is processed in chunks of 64 query tokens (one KV block); chunk c holds the
+#     tokens [64c, 64c + 64) of the prompt, the last chunk possibly fewer;
+#   * the tokens of a chunk share one block selection, so that the block-sparse attention
+#     of the chunk reads each selected block once;
+#   * the selection of chunk c scores the compressed keys complete before the chunk starts
+#     (the windows within its first 64c tokens), as a decode step scores the windows complete
+#     before its current token; block 0 and the chunk's own block c are always kept, and the
+#     top-k of the blocks 1 .. c-1 is added;
+#   * the Forecast selector scores a window by the sum over the chunk's tokens of the decode
+#     score (each token's forecast vector dotted with the compressed key, no softmax, no
+#     scale); the baseline selector sums over the chunk's tokens what it sums over the
+#     group's heads in decode (each (token, head) query's softmax over the windows);
+#   * every query token attends the tokens of its chunk's selected blocks up to and including
+#     its own position (causal within the chunk's own block).
+def prefill_num_chunks(T, block=BLOCK):
+    """Chunks of a T-token prompt."""
+    return (T + block - 1) // block
+
+
+def prefill_chunk_windows(c, block=BLOCK, kernel=WIN_KERNEL, stride=WIN_STRIDE):
+    """Windows complete before chunk c starts: those within its first block*c tokens."""
+    return num_windows(block * c, kernel, stride)
+
+
+def prefill_forecast_scores(F_chunk, ck, c, block=BLOCK):
+    """Window scores of chunk c under the Forecast selector.
+
+    F_chunk: [n_tok, d], the forecast vectors of the chunk's tokens (one head of the group);
+    ck: the group's compressed keys. s[i] = sum over the chunk's tokens t of <f_t, ck[i]>,
+    for the windows i complete before the chunk.
+    """
+    W = prefill_chunk_windows(c, block)
+    per_token = np.asarray(F_chunk, dtype=np.float64) @ np.asarray(ck, dtype=np.float64)[:W].T   # [n_tok, W]
+    return per_token.sum(axis=0)
+
+
+def prefill_multihead_scores(Q_chunk, ck, c, scale=None, block=BLOCK):
+    """Window scores of chunk c under the baseline selector.
+
+    Q_chunk: [n_tok, H, d], the query heads of the group for each token of the chunk. Every
+    (token, head) query gets its own softmax over the windows complete before the chunk (its
+    logits scaled by 1/sqrt(d)), and the probabilities are summed over the chunk's tokens and
+    the group's heads.
+    """
+    Q_chunk = np.asarray(Q_chunk, dtype=np.float64)
+    W = prefill_chunk_windows(c, block)
+    if W == 0:
+        return np.zeros(0)
+    n_tok, H, d = Q_chunk.shape
+    total = np.zeros(W)
+    for t in range(n_tok):
+        total += multihead_scores(Q_chunk[t], np.asarray(ck)[:W], scale)
+    return total
+
+
+def prefill_select(S, c, k, block=BLOCK):
+    """Blocks of chunk c: {0, c} and the top-k of the blocks 1 .. c-1 by S (ties to the lower
+    block), ascending. The rule is the decode step's, for a context whose current token lies
+    in block c."""
+    return select_blocks(S, block * c + 1, k, block)
+
+
+def prefill_select_all(ck, per_chunk_queries, T, k, selector="forecast", block=BLOCK):
+    """Selections of every chunk of a T-token prompt for one (sequence, group).
+
+    per_chunk_queries(c) returns the chunk's forecast vectors [n_tok, d] ("forecast") or its
+    queries [n_tok, H, d] ("multihead"). Returns (sel, S): the block lists and the block
+    scores of each chunk.
+    """
+    sel, S = [], []
+    for c in range(prefill_num_chunks(T, block)):
+        if selector == "forecast":
+            s = prefill_forecast_scores(per_chunk_queries(c), ck, c, block)
+        else:
+            s = prefill_multihead_scores(per_chunk_queries(c), ck, c, block=block)
+        Sc = pool_to_blocks(s, c + 1, block)
+        S.append(Sc)
+        sel.append(prefill_select(Sc, c, k, block))
+    return sel, S
+
+
+def prefill_block_sparse_attention(Q, K, V, sel, T, block=BLOCK, scale=None):
+    """Causal block-sparse prefill attention of one (sequence, group).
+
+    Q: [T, H, d], the group's query heads for every prompt token; K, V: [>=T, d]; sel[c]: the
+    blocks of chunk c. Token t of chunk c = t // block attends, for every head, the tokens
+    t' <= t of its chunk's blocks. Returns [T, H, d].
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[2])
+    out = np.empty(Q.shape)
+    for t in range(T):
+        toks = selected_tokens(sel[t // block], t + 1, block)          # tokens <= t
+        z = (Q[t] @ K[toks].T) * scale                                 # [H, n]
+        z = z - z.max(axis=1, keepdims=True)
+        w = np.exp(z)
+        out[t] = (w @ V[toks]) / w.sum(axis=1, keepdims=True)
+    return out
+
+
+def dense_causal_prefill_attention(Q, K, V, T, scale=None):
+    """Dense causal prefill attention: token t attends every token t' <= t (written
+    separately from the block-sparse routine, per head as a log-sum-exp, to pin it)."""
+    Q = np.asarray(Q, dtype=np.float64)
+    if scale is None:
+        scale = 1.0 / math.sqrt(Q.shape[2])
+    out = np.empty(Q.shape)
+    for t in range(T):
+        out[t] = dense_causal_attention(Q[t], K, V, t + 1, scale)
+    return out

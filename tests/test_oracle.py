@@ -413,3 +413,121 @@ def test_decode_step_first_token_attends_itself():
             for g in range(G):
                 assert sel[L][b][g] == [0]
                 assert np.allclose(out[L][b, g * H:(g + 1) * H], vn[L][b, g], atol=1e-15)
+
+
+# ---------------------------------------------------------------- prefill (chunked queries)
+def _brute_attention(q_heads, K, V, toks, scale):
+    """Softmax attention of each head over an explicit token list, by a plain loop."""
+    out = np.zeros((q_heads.shape[0], V.shape[1]))
+    for h in range(q_heads.shape[0]):
+        logits = [float(q_heads[h] @ K[t]) * scale for t in toks]
+        m = max(logits)
+        w = [math.exp(x - m) for x in logits]
+        tot = sum(w)
+        for wi, t in zip(w, toks):
+            out[h] += wi / tot * V[t]
+    return out
+
+
+def test_prefill_chunk_windows_are_those_before_the_chunk():
+    for c in range(0, 40):
+        brute = sum(1 for i in range(0, 400) if 16 * i + 32 <= 64 * c)
+        assert O.prefill_chunk_windows(c) == brute
+    assert [O.prefill_chunk_windows(c) for c in range(4)] == [0, 3, 7, 11]
+    assert O.prefill_num_chunks(1) == 1 and O.prefill_num_chunks(64) == 1 and O.prefill_num_chunks(65) == 2
+
+
+def test_prefill_forecast_scores_small_integers():
+    rng = np.random.default_rng(21)
+    ck = rng.integers(-3, 4, (20, 4)).astype(np.float64)
+    F = rng.integers(-2, 3, (5, 4)).astype(np.float64)
+    c = 3                                                   # windows 0 .. 10 exist before chunk 3
+    s = O.prefill_forecast_scores(F, ck, c)
+    assert s.shape == (11,)
+    for i in range(11):
+        assert s[i] == sum(sum(F[t, e] * ck[i, e] for e in range(4)) for t in range(5))
+
+
+def test_prefill_window_touching_the_chunk_is_not_scored():
+    # a huge compressed key at the first window that overlaps chunk c's own tokens must not
+    # change chunk c's selection; one window earlier it must
+    rng = np.random.default_rng(22)
+    c, d = 6, 8
+    ck = rng.normal(size=(40, d))
+    f = rng.normal(size=(1, d))
+    base = O.prefill_select(O.pool_to_blocks(O.prefill_forecast_scores(f, ck, c), c + 1), c, 1)
+    W = O.prefill_chunk_windows(c)
+    hot = ck.copy()
+    hot[W] = 100 * f[0]
+    assert O.prefill_select(O.pool_to_blocks(O.prefill_forecast_scores(f, hot, c), c + 1), c, 1) == base
+    hot = ck.copy()
+    hot[W - 2] = 100 * f[0]                                 # window 4c-3 lies in block c-1 only
+    assert O.prefill_select(O.pool_to_blocks(O.prefill_forecast_scores(f, hot, c), c + 1), c, 1) == [0, c - 1, c]
+
+
+def test_prefill_constant_forecast_equals_the_decode_selection():
+    """A chunk whose tokens all carry the same forecast selects what a decode step with that
+    forecast selects when its current token is the first token of the chunk's block (the
+    decode step scores the windows before its current token, and its tail block is c)."""
+    rng = np.random.default_rng(23)
+    T, d, k = 64 * 9 + 17, 16, 3
+    K = rng.normal(size=(T, d))
+    ck = O.compress_keys(K, O.num_windows(T))
+    for c in range(O.prefill_num_chunks(T)):
+        f = rng.normal(size=d)
+        n_tok = min(64, T - 64 * c)
+        sc = O.prefill_forecast_scores(np.tile(f, (n_tok, 1)), ck, c)
+        got = O.prefill_select(O.pool_to_blocks(sc, c + 1), c, k)
+        assert got == O.forecast_select_one(K, f, 64 * c + 1, k)
+        # positive per-token weights sum to a positive multiple: the same selection
+        w = rng.uniform(0.5, 2.0, size=(n_tok, 1))
+        sw = O.prefill_forecast_scores(w * f, ck, c)
+        assert O.prefill_select(O.pool_to_blocks(sw, c + 1), c, k) == got
+    assert O.prefill_select(np.zeros(1), 0, 4) == [0]
+    assert O.prefill_select(np.zeros(2), 1, 4) == [0, 1]
+
+
+def test_prefill_multihead_with_identical_queries_equals_forecast():
+    rng = np.random.default_rng(24)
+    T, d, H, k = 64 * 7, 8, 4, 2
+    K = rng.normal(size=(T, d))
+    ck = O.compress_keys(K, O.num_windows(T))
+    for c in range(2, 7):
+        qv = rng.normal(size=d)
+        Qc = np.tile(qv, (64, H, 1))
+        mh = O.pool_to_blocks(O.prefill_multihead_scores(Qc, ck, c), c + 1)
+        fc = O.pool_to_blocks(O.prefill_forecast_scores(np.tile(qv, (64, 1)), ck, c), c + 1)
+        assert O.prefill_select(mh, c, k) == O.prefill_select(fc, c, k)
+        # the sum of 64 x H identical softmaxes is 64 H times one softmax
+        s1 = O.multihead_scores(qv[None, :], ck[:O.prefill_chunk_windows(c)])
+        assert np.allclose(O.prefill_multihead_scores(Qc, ck, c), 64 * H * s1, rtol=1e-12)
+
+
+def test_prefill_attention_with_all_blocks_equals_dense_causal():
+    rng = np.random.default_rng(25)
+    T, H, d = 64 * 3 + 21, 3, 8
+    Q, K, V = rng.normal(size=(T, H, d)), rng.normal(size=(T, d)), rng.normal(size=(T, d))
+    n = O.prefill_num_chunks(T)
+    sel = [O.prefill_select(rng.normal(size=c + 1), c, 99) for c in range(n)]
+    assert sel[-1] == list(range(n))
+    got = O.prefill_block_sparse_attention(Q, K, V, sel, T)
+    assert np.allclose(got, O.dense_causal_prefill_attention(Q, K, V, T), rtol=1e-12, atol=1e-12)
+    assert np.allclose(got[0], np.tile(V[0], (H, 1)))        # the first token attends itself only
+
+
+def test_prefill_attention_is_causal_within_the_selected_blocks():
+    rng = np.random.default_rng(26)
+    T, H, d = 64 * 5 + 9, 2, 8
+    Q, K, V = rng.normal(size=(T, H, d)), rng.normal(size=(T, d)), rng.normal(size=(T, d))
+    sel = [[0], [0, 1], [0, 2], [0, 1, 3], [0, 2, 4], [0, 3, 5]]
+    got = O.prefill_block_sparse_attention(Q, K, V, sel, T)
+    scale = 1 / math.sqrt(d)
+    for t in [0, 5, 63, 64, 100, 130, 191, 192, 250, 256, 300, T - 1]:
+        toks = [u for u in range(t + 1) if u // 64 in sel[t // 64]]
+        assert np.allclose(got[t], _brute_attention(Q[t], K, V, toks, scale), rtol=1e-12, atol=1e-12)
+    # a future token inside the chunk's own block changes nothing before it
+    V2 = V.copy()
+    V2[64 * 4 + 30] += 10.0
+    got2 = O.prefill_block_sparse_attention(Q, K, V2, sel, T)
+    assert np.array_equal(got2[:64 * 4 + 30], got[:64 * 4 + 30])
+    assert not np.allclose(got2[64 * 4 + 30], got[64 * 4 + 30])
