@@ -491,6 +491,68 @@ def selector_ab(device, seed):
     return out
 
 
+# ---------------------------------------------------------------------- chunked prefill A/B
+def prefill_attn_flops(idx, cnt, T):
+    """Algorithmic flops of the causal block-sparse prefill attention of one sequence-group:
+    QK^T and PV (2 x 2 flops per query head, key and dimension) over the keys each token
+    attends, from the chunk selections idx [n_chunks, k+2] / cnt [n_chunks] on the host."""
+    keys = 0
+    for c in range((T + 63) // 64):
+        n_tok = min(64, T - 64 * c)
+        full = int(cnt[c]) - 1                           # selected blocks before the chunk's own
+        keys += n_tok * 64 * full + n_tok * (n_tok + 1) // 2
+    return keys * H * D * 4
+
+
+def prefill_ab(device, seed, contexts=(32768, 65536, 131072)):
+    """One layer's prefill of a batch-1 prompt at each context: the Forecast chunk selector
+    against the baseline multi-head chunk selector, and the causal block-sparse prefill
+    attention over the forecast's selections (top-32 blocks plus block 0 and the chunk's own).
+    K, V, queries and per-token forecasts are seeded N(0,1) bf16 drawn on the device. Device
+    time per call from CUDA graph replays."""
+    import torch
+    import synth
+    import block_sparse_attention_forecast_gb300.binding as sb
+    peaks, _ = measured_peaks()
+    out = {}
+    for T in contexts:
+        shape = sb.Shape(n_groups=G, topk=TOPK, max_ctx=T, max_batch=1)
+        layer = sb.LayerKV.empty(shape, device=device)
+        layer.k.copy_(synth.normal_bf16_device(layer.k.shape, seed * 1000 + 950, device))
+        layer.v.copy_(synth.normal_bf16_device(layer.v.shape, seed * 1000 + 951, device))
+        q = synth.normal_bf16_device((1, T, G * H, D), seed * 1000 + 952, device)
+        f = synth.normal_bf16_device((1, T, G, D), seed * 1000 + 953, device)
+        seq = torch.full((1,), T, dtype=torch.int32, device=device)
+        sb.sparda_compress_keys(shape, layer, seq, 1)
+        nc = T // 64
+        idx = torch.zeros((1, G, nc, TOPK + 2), dtype=torch.int32, device=device)
+        cnt = torch.zeros((1, G, nc), dtype=torch.int32, device=device)
+        idx_m, cnt_m = torch.zeros_like(idx), torch.zeros_like(cnt)
+        ws = sb.workspace(shape, 1, sb.WS_PREFILL, device)
+        o = torch.empty_like(q)
+        t_f = graph_time(lambda s: sb.sparda_prefill_forecast_select(shape, layer.ck, f, seq, 1, idx, cnt, ws,
+                                                                     stream=s), 3)
+        t_m = graph_time(lambda s: sb.sparda_prefill_multihead_select(shape, layer.ck, q, seq, 1, idx_m, cnt_m, ws,
+                                                                      stream=s), 1)
+        t_a = graph_time(lambda s: sb.sparda_prefill_attn(shape, layer, q, idx, cnt, seq, 1, o, stream=s), 2)
+        ic, cc = idx.cpu().numpy(), cnt.cpu().numpy()
+        flops = sum(prefill_attn_flops(ic[0, g], cc[0, g], T) for g in range(G))
+        tf = flops / t_a / 1e12
+        out[str(T)] = {
+            "forecast_select_ms": t_f * 1e3, "multihead_select_ms": t_m * 1e3, "attn_ms": t_a * 1e3,
+            "selection_speedup": t_m / t_f,
+            "prefill_tok_s_forecast": T / (t_f + t_a), "prefill_tok_s_multihead": T / (t_m + t_a),
+            "prefill_speedup": (t_m + t_a) / (t_f + t_a),
+            "attn_tflops": tf, "attn_flops": flops, "attn_frac_of_bf16_peak": tf / float(peaks["bf16_tflops"]),
+        }
+        del layer, q, f, o, ws, idx, cnt, idx_m, cnt_m
+        torch.cuda.empty_cache()
+    out["device_error_flags"] = sb.sparda_device_error(clear=True)
+    out["workload"] = ("one 8B-shaped layer's prefill, batch 1, 64-token query chunks, top-32 blocks plus block 0 "
+                       "and the chunk's own; K/V/queries/forecasts seeded N(0,1) bf16")
+    return out
+
+
 # ---------------------------------------------------------------------- CPU oracle sample
 CPU_SAMPLE_SCRIPT = r"""
 import sys, time, json

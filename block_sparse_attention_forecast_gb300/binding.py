@@ -25,9 +25,10 @@ __all__ = [
     "sparda_forecast_project", "sparda_forecast_select", "sparda_sparse_decode_attn",
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
     "sparda_attend_and_score", "sparda_decode_prologue", "sparda_forecast_score", "sparda_copy",
+    "sparda_prefill_forecast_select", "sparda_prefill_multihead_select", "sparda_prefill_attn",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
-    "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
+    "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "WS_PREFILL", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,7 @@ DEV_BAD_INDEX = 4
 WS_SELECT = 1
 WS_ATTN = 2
 WS_MULTIHEAD = 3
+WS_PREFILL = 4
 
 BLOCK = 64
 WIN_KERNEL = 32
@@ -104,6 +106,9 @@ def _load():
         "sparda_decode_prologue": (I32, [SH, LY, P, P, P, SZ, P, P, P, P, I32, P, P, I32, P]),
         "sparda_copy": (I32, [P, P, SZ, P]),
         "sparda_forecast_score": (I32, [SH, P, P, P, I32, P, SZ, P]),
+        "sparda_prefill_forecast_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
+        "sparda_prefill_multihead_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
+        "sparda_prefill_attn": (I32, [SH, LY, P, P, P, P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -371,3 +376,29 @@ def sparda_forecast_select_static(shape, ck, forecast, seq_len, batch, idx, cnt,
     _check("sparda_forecast_select_static", lib.sparda_forecast_select_static(
         ctypes.byref(shape.c()), _ptr(ck), _ptr(forecast), _ptr(seq_len), int(batch), _ptr(idx),
         _ptr(cnt), _stream(stream)))
+
+
+# ------------------------------------------------------------------ chunked prefill
+def sparda_prefill_forecast_select(shape, ck, forecast, seq_len, batch, idx, cnt, ws, stream=None):
+    """Per-chunk selections of a prompt by the Forecast selector. forecast: bf16
+    [max_batch, max_ctx, G, d]; idx: int32 [B, G, max_ctx/64, topk+2]; cnt: int32
+    [B, G, max_ctx/64]; ws: a WS_PREFILL workspace."""
+    _check("sparda_prefill_forecast_select", lib.sparda_prefill_forecast_select(
+        ctypes.byref(shape.c()), _ptr(ck), _ptr(forecast), _ptr(seq_len), int(batch), _ptr(idx), _ptr(cnt),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def sparda_prefill_multihead_select(shape, ck, q, seq_len, batch, idx, cnt, ws, stream=None):
+    """Per-chunk selections of a prompt by the baseline multi-head selector. q: bf16
+    [max_batch, max_ctx, G*H, d]; outputs as sparda_prefill_forecast_select."""
+    _check("sparda_prefill_multihead_select", lib.sparda_prefill_multihead_select(
+        ctypes.byref(shape.c()), _ptr(ck), _ptr(q), _ptr(seq_len), int(batch), _ptr(idx), _ptr(cnt),
+        _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def sparda_prefill_attn(shape, layer, q, idx, cnt, seq_len, batch, out, stream=None):
+    """Causal block-sparse prefill attention of a resident layer over the per-chunk
+    selections. q, out: bf16 [max_batch, max_ctx, G*H, d]."""
+    _check("sparda_prefill_attn", lib.sparda_prefill_attn(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(q), _ptr(idx), _ptr(cnt), _ptr(seq_len),
+        int(batch), _ptr(out), _stream(stream)))

@@ -207,6 +207,7 @@ size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind
     case SPARDA_WS_SELECT: return kQueueBytes + counters_bytes(s) + select_data_bytes(s);
     case SPARDA_WS_ATTN: return counters_bytes(s) + attn_o_bytes(s) + attn_ml_bytes(s);
     case SPARDA_WS_MULTIHEAD: return mh_z_bytes(s) + mh_stats_bytes(s) + select_data_bytes(s);
+    case SPARDA_WS_PREFILL: return round256((size_t)s->max_batch * s->n_groups * nb_cap(s) * nb_cap(s) * sizeof(float));
     default: return 0;
   }
 }
@@ -528,6 +529,76 @@ int32_t sparda_multihead_select(const sparda_shape* s, const void* ck, const voi
                   reinterpret_cast<float*>(w + mh_z_bytes(s) + mh_stats_bytes(s)), err, s->n_groups, w_cap(s),
                   s->max_ctx, nb_cap(s), s->topk, multihead_tiles(w_cap(s))};
   launch_multihead_select(a, mck, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+
+// ------------------------------------------------------------------ chunked prefill
+}  // extern "C"
+
+namespace {
+
+int32_t prepare_prefill(const sparda_shape* s, const void* ck, const void* qf, const int32_t* seq_len, int32_t batch,
+                        int32_t* idx, int32_t* cnt, void* ws, size_t ws_bytes, PrefillArgs* a) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!ck || !qf || !seq_len || !idx || !cnt || !ws) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(ck, 16) || !aligned(qf, 16) || !aligned(ws, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
+      !aligned(seq_len, 4))
+    return SPARDA_ERR_MISALIGNED;
+  if (ws_bytes < sparda_workspace_bytes(s, batch, SPARDA_WS_PREFILL)) return SPARDA_ERR_WORKSPACE_TOO_SMALL;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  *a = PrefillArgs{static_cast<const __nv_bfloat16*>(ck), nullptr, nullptr, nullptr, seq_len, idx, cnt,
+                   static_cast<float*>(ws), err, s->n_groups, w_cap(s), s->max_ctx, nb_cap(s), s->topk};
+  return SPARDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sparda_prefill_forecast_select(const sparda_shape* s, const void* ck, const void* forecast,
+                                       const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  PrefillArgs a;
+  SPARDA_TRY(prepare_prefill(s, ck, forecast, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
+  a.f = static_cast<const __nv_bfloat16*>(forecast);
+  launch_prefill_forecast_select(a, batch, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_prefill_multihead_select(const sparda_shape* s, const void* ck, const void* q,
+                                        const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  PrefillArgs a;
+  SPARDA_TRY(prepare_prefill(s, ck, q, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  CUtensorMap mck;
+  SPARDA_TRY(make_kv_map(&mck, ck, (uint64_t)s->max_batch * s->n_groups * w_cap(s)));
+  launch_prefill_multihead_select(a, mck, batch, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_prefill_attn(const sparda_shape* s, const sparda_layer_kv* L, const void* q, const int32_t* idx,
+                            const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* out, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  SPARDA_TRY(layer_status(L, true));
+  if (L->on_host) return SPARDA_ERR_INVALID_ARG;              // prefill attends a resident layer
+  if (!q || !idx || !cnt || !seq_len || !out) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(seq_len, 4))
+    return SPARDA_ERR_MISALIGNED;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  const uint64_t rows = (uint64_t)s->max_batch * s->n_groups * s->max_ctx;
+  CUtensorMap mk, mv;
+  SPARDA_TRY(make_kv_map(&mk, L->k, rows));
+  SPARDA_TRY(make_kv_map(&mv, L->v, rows));
+  PrefillArgs a{nullptr, nullptr, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), seq_len,
+                const_cast<int32_t*>(idx), const_cast<int32_t*>(cnt), nullptr, err, s->n_groups, w_cap(s),
+                s->max_ctx, nb_cap(s), s->topk};
+  launch_prefill_attn(a, mk, mv, batch, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

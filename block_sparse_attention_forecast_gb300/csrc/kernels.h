@@ -131,6 +131,25 @@ struct PrologueArgs {
 };
 void launch_decode_prologue(const PrologueArgs& a, cudaStream_t s);
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);
+
+// Chunked prefill (prefill.cu): 64-token query chunks, chunk c of sequence-group bg at row
+// bg * nb_cap + c of idx [.., topk+2], cnt and the block scores [.., nb_cap].
+struct PrefillArgs {
+  const __nv_bfloat16* ck;       // [max_batch, G, W_cap, d]
+  const __nv_bfloat16* f;        // per-token forecasts [max_batch, max_ctx, G, d]
+  const __nv_bfloat16* q;        // per-token queries [max_batch, max_ctx, G*H, d]
+  __nv_bfloat16* out;            // attention output [max_batch, max_ctx, G*H, d]
+  const int32_t* seq_len;        // prompt lengths [B]
+  int32_t* idx;                  // [B*G, nb_cap, topk+2]
+  int32_t* cnt;                  // [B*G, nb_cap]
+  float* block_scores;           // workspace [B*G, nb_cap, nb_cap]
+  int* err;
+  int G, W_cap, max_ctx, nb_cap, topk;
+};
+void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s);
+void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mck, int batch, cudaStream_t s);
+void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, int batch,
+                         cudaStream_t s);
 int multihead_tiles(int w_cap);
 
 // Device address of the library's device error word on the current device (api.cu).

@@ -1,0 +1,607 @@
+// Chunked prefill: the Forecast selector and the baseline multi-head selector applied to
+// 64-token query chunks, and causal block-sparse prefill attention.
+//
+// The pages report prefill as well as decode figures (bittide thread and abstract: up to
+// 1.25x faster prefill; techwalker section 五: in prefill the block-sparse attention is the
+// main cost, the block selection grows with the context and nears it at 128K, and the
+// Forecast indexer cuts the selection cost by up to 2.5x). The prefill selection rule is a
+// reading: chunk c (tokens 64c .. 64c+63) shares one selection, scores the compressed keys
+// complete before it (windows i < W_c = num_windows(64c)), keeps blocks 0 and c and the
+// top-k of blocks 1 .. c-1. The Forecast score of a window sums the decode score over the
+// chunk's tokens, s_c[i] = sum_t f_t . ck_i = (sum_t f_t) . ck_i; the baseline sums each
+// (token, head) query's softmax over the windows. Every token attends its chunk's blocks up
+// to its own position.
+//
+// Kernels:
+//   prefill_forecast_score_kernel  per (sequence-group, 16-chunk tile): the chunks' summed
+//       forecasts (float32) against 64-window tiles of compressed keys staged in shared memory
+//       by cp.async (double buffered), float32 FMA on CUDA cores (128 FMAs per window and
+//       chunk, exact bf16 inputs), max-pooled onto blocks in shared memory; block scores to
+//       the workspace.
+//   prefill_topk_kernel            one top-k CTA per (sequence-group, chunk) (topk.cuh).
+//   prefill_multihead_kernel       the baseline: per (sequence-group, chunk), for each of
+//       8 slices of 8 tokens, two passes over TMA-staged 64-window tiles on bf16 mma.sync
+//       (a warp = one token's 16 heads): the per-row log-sum-exp, then the column sums of the
+//       normalised probabilities, added in a fixed order into the chunk's window sums in
+//       shared memory; then max-pool and the top-k in the same CTA.
+//   prefill_attn_kernel            per (sequence-group, chunk, 8-token slice): the chunk's
+//       selected K/V blocks through a TMA ring; each consumer warp runs one token's 16 heads
+//       over every block (QK^T and PV on bf16 mma.sync, float32 online softmax), causal in
+//       the chunk's own block.
+#include "common.cuh"
+#include "kernels.h"
+#include "topk.cuh"
+
+namespace sparda {
+
+namespace {
+
+// ------------------------------------------------------------------ shared helpers
+constexpr int kPfChunks = 16;                 // chunk rows per forecast-scoring CTA
+constexpr int kPfWin = 64;                    // windows per tile
+constexpr int kPfThreads = 256;
+constexpr int kCkStride = kHeadDim + 8;       // bf16 per padded shared row: 272 B, no conflicts
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  const int n = pred ? 16 : 0;                // 0: the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)), "l"(gmem), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ bool valid_len(int T, int max_ctx) { return T >= 1 && T <= max_ctx; }
+
+}  // namespace
+
+// ==================================================================== Forecast scoring
+__global__ void __launch_bounds__(kPfThreads) prefill_forecast_score_kernel(const PrefillArgs a) {
+  __shared__ __align__(16) float fs[kPfChunks][kHeadDim];            // summed forecasts
+  __shared__ __align__(16) __nv_bfloat16 ckt[2][kPfWin][kCkStride];  // window tiles
+  __shared__ float sw[kPfChunks][kPfWin + 1];                        // [.][0] = halo window
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
+  const int n_ct = (a.nb_cap + kPfChunks - 1) / kPfChunks;
+  const int c0 = (n_ct - 1 - (int)blockIdx.x) * kPfChunks;          // the longest rows first
+  const int T = a.seq_len[b];
+  if (!valid_len(T, a.max_ctx)) {
+    if (t == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nc = (T + kBlock - 1) / kBlock;
+  if (c0 >= nc) return;
+  const int c_last = min(c0 + kPfChunks, nc) - 1;
+
+  // ---- the chunks' summed forecasts: thread t sums 8 dims of chunk t/16 over its tokens
+  {
+    const int r = t >> 4, d8 = (t & 15) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int p0 = (c0 + r) * kBlock;
+    const int p1 = min(p0 + kBlock, T);
+    const size_t row_stride = (size_t)a.G * kHeadDim;
+    const __nv_bfloat16* fp = a.f + ((size_t)b * a.max_ctx * a.G + g) * kHeadDim + d8;
+#pragma unroll 8
+    for (int p = p0; p < p1; ++p) {
+      const uint4 v = *reinterpret_cast<const uint4*>(fp + (size_t)p * row_stride);
+      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+      acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+      acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fs[r][d8 + e] = acc[e];
+  }
+  if (t < kPfChunks) sw[t][0] = -INFINITY;                            // no window before tile 0
+
+  // ---- window tiles, double buffered
+  const int W_last = num_windows(kBlock * c_last);
+  const int n_wt = (W_last + kPfWin - 1) / kPfWin;
+  const __nv_bfloat16* ckg = a.ck + (size_t)bg * a.W_cap * kHeadDim;
+  auto load_tile = [&](int m, int buf) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int q = e * kPfThreads + t;                               // 16-byte chunk of the tile
+      const int r = q >> 4, c16 = q & 15;
+      const int i = m * kPfWin + r;
+      const bool in = i < W_last;
+      cp_async16(&ckt[buf][r][c16 * 8], ckg + (size_t)(in ? i : 0) * kHeadDim + c16 * 8, in);
+    }
+    cp_async_commit();
+  };
+  if (n_wt > 0) load_tile(0, 0);
+  const int r0 = warp, r1 = warp + 8;                                 // chunk rows of this thread
+  const int Wr0 = num_windows(kBlock * (c0 + r0)), Wr1 = num_windows(kBlock * (c0 + r1));
+  for (int m = 0; m < n_wt; ++m) {
+    const int buf = m & 1;
+    if (m + 1 < n_wt) {
+      load_tile(m + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();                                                  // tile m and fs visible
+    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;                 // [row][window]
+    const __nv_bfloat16* k0 = &ckt[buf][lane][0];
+    const __nv_bfloat16* k1 = &ckt[buf][lane + 32][0];
+#pragma unroll 4
+    for (int d = 0; d < kHeadDim; d += 8) {
+      const uint4 u0 = *reinterpret_cast<const uint4*>(k0 + d);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(k1 + d);
+      const float4 fa0 = *reinterpret_cast<const float4*>(&fs[r0][d]);
+      const float4 fb0 = *reinterpret_cast<const float4*>(&fs[r0][d + 4]);
+      const float4 fa1 = *reinterpret_cast<const float4*>(&fs[r1][d]);
+      const float4 fb1 = *reinterpret_cast<const float4*>(&fs[r1][d + 4]);
+      const float x0[8] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y),
+                           bf16_lo(u0.z), bf16_hi(u0.z), bf16_lo(u0.w), bf16_hi(u0.w)};
+      const float x1[8] = {bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
+                           bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
+      const float f0[8] = {fa0.x, fa0.y, fa0.z, fa0.w, fb0.x, fb0.y, fb0.z, fb0.w};
+      const float f1[8] = {fa1.x, fa1.y, fa1.z, fa1.w, fb1.x, fb1.y, fb1.z, fb1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s00 = fmaf(f0[e], x0[e], s00);
+        s01 = fmaf(f0[e], x1[e], s01);
+        s10 = fmaf(f1[e], x0[e], s10);
+        s11 = fmaf(f1[e], x1[e], s11);
+      }
+    }
+    const int i0 = m * kPfWin + lane, i1 = i0 + 32;
+    sw[r0][1 + lane] = i0 < Wr0 ? s00 : -INFINITY;
+    sw[r0][33 + lane] = i1 < Wr0 ? s01 : -INFINITY;
+    sw[r1][1 + lane] = i0 < Wr1 ? s10 : -INFINITY;
+    sw[r1][33 + lane] = i1 < Wr1 ? s11 : -INFINITY;
+    __syncthreads();
+    // max-pool: block j = 16m + jj takes windows 4j-1 .. 4j+3 (local 4jj .. 4jj+4 with the
+    // halo window in column 0); thread t: chunk row t/16, block t%16
+    {
+      const int r = t >> 4, jj = t & 15, j = m * 16 + jj;
+      float S = sw[r][4 * jj];
+#pragma unroll
+      for (int e = 1; e <= 4; ++e) S = fmaxf(S, sw[r][4 * jj + e]);
+      const int c = c0 + r;
+      if (c <= c_last && j < a.nb_cap && j <= c)
+        a.block_scores[((size_t)bg * a.nb_cap + c) * a.nb_cap + j] = S;
+    }
+    __syncthreads();                                                  // sw read before the halo moves
+    if (t < kPfChunks) sw[t][0] = sw[t][kPfWin];
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const PrefillArgs a) {
+  __shared__ TopkShared sh;
+  const int bg = blockIdx.y, b = bg / a.G, c = blockIdx.x;
+  const int T = a.seq_len[b];
+  const int kslots = a.topk + 2;
+  int32_t* idx = a.idx + ((size_t)bg * a.nb_cap + c) * kslots;
+  int32_t* cnt = a.cnt + (size_t)bg * a.nb_cap + c;
+  if (!valid_len(T, a.max_ctx) || c * kBlock >= T) {
+    // no such chunk: an empty selection
+    for (int s = threadIdx.x; s < kslots; s += blockDim.x) idx[s] = -1;
+    if (threadIdx.x == 0) *cnt = 0;
+    return;
+  }
+  // the decode rule for a context whose current token lies in block c: tail block c, windows
+  // before the chunk (the scores were written for exactly those)
+  topk_select(a.block_scores + ((size_t)bg * a.nb_cap + c) * a.nb_cap, idx, cnt, a.topk, a.max_ctx,
+              c * kBlock + 1, sh);
+}
+
+// ==================================================================== tensor-core helpers
+namespace {
+
+constexpr int kPaConsumerWarps = 8;
+constexpr int kPaThreads = (kPaConsumerWarps + 1) * 32;     // 8 consumer warps + producer
+constexpr int kPaStages = 4;
+constexpr int kPaSlotBytes = 2 * kBlockBytes;                // K + V of one block
+constexpr int kPaSmem = 1024 + 1024 + kPaStages * kPaSlotBytes;
+constexpr int kMhStages = 6;
+constexpr int kMhTileBytes = kBlockBytes;                    // 64 windows x 128 dims bf16
+// [align slack][barriers][ring][per-warp column sums, 2 buffers][top-k scratch][window sums]
+constexpr int kMhFixedSmem = 1024 + 1024 + kMhStages * kMhTileBytes + 2 * kPaConsumerWarps * 64 * 4 +
+                             ((int)sizeof(TopkShared) + 15) / 16 * 16;
+__host__ __device__ constexpr int mh_smem_bytes(int w_cap) { return kMhFixedSmem + 4 * w_cap; }
+static_assert(mh_smem_bytes(kMaxCtx / kWinStride) <= 227 * 1024, "the baseline prefill selector fits shared memory");
+constexpr int kSlices = 8;                                   // 8-token slices of a chunk
+
+// Shared address of 16-byte chunk `chunk` (0..15 over the 128 dims) of row r of a 64-row
+// tile staged by TMA as two 64-column halves with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz_addr(const uint8_t* tile, int r, int chunk) {
+  return smem_addr(tile + (chunk >> 3) * (kBlockBytes / 2) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kPaConsumerWarps * 32) : "memory");
+}
+
+// The A fragments of one token's 16 query heads (rows = heads, k = dims), from global memory.
+__device__ __forceinline__ void load_q_frags(const __nv_bfloat16* q16, int lane, uint32_t (&qf)[8][4]) {
+  const int g = lane >> 2, cq = lane & 3;
+  const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q16 + (size_t)g * kHeadDim);
+  const uint32_t* q1 = q0 + 8 * (kHeadDim / 2);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    qf[ks][0] = q0[8 * ks + cq];
+    qf[ks][1] = q1[8 * ks + cq];
+    qf[ks][2] = q0[8 * ks + 4 + cq];
+    qf[ks][3] = q1[8 * ks + 4 + cq];
+  }
+}
+
+// S[16 heads x 64 rows of the tile] = Q . tile^T; sc[n] is n-tile n (rows 8n .. 8n+7 of the
+// tile) in the m16n8 accumulator layout.
+__device__ __forceinline__ void qk_tile(const uint32_t (&qf)[8][4], const uint8_t* tile, int lane, float (&sc)[8][4]) {
+#pragma unroll
+  for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+  const int hi = (lane >> 3) & 1;
+#pragma unroll
+  for (int wq = 0; wq < 4; ++wq) {
+    const int r = 16 * wq + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(swz_addr(tile, r, 2 * ks + hi), b0, b1, b2, b3);
+      mma_16816(sc[2 * wq], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+      mma_16816(sc[2 * wq + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+    }
+  }
+}
+
+}  // namespace
+
+// ==================================================================== block-sparse attention
+__global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_kernel(const PrefillArgs a,
+                                                                     const __grid_constant__ CUtensorMap mk,
+                                                                     const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kPaStages;
+  int* stage_j = reinterpret_cast<int*>(empty + kPaStages);
+  uint8_t* ring = smem + 1024;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
+  const int c = blockIdx.x / kSlices, sl = blockIdx.x % kSlices;
+  const int T = a.seq_len[b];
+  if (!valid_len(T, a.max_ctx)) {
+    if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int tok0 = c * kBlock + sl * kPaConsumerWarps;
+  if (tok0 >= T) return;                                     // CTA-uniform
+  const int kslots = a.topk + 2;
+  const size_t row = (size_t)bg * a.nb_cap + c;
+  const int n_sel = min(max(a.cnt[row], 0), kslots);
+
+  if (tid == 0) {
+    for (int i = 0; i < kPaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kPaConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kPaConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    prefetch_tensormap(&mk);
+    prefetch_tensormap(&mv);
+    for (int s = 0; s < n_sel; ++s) {
+      int j = a.idx[row * kslots + s];
+      if (j < 0 || j > c) {                                   // only blocks up to the chunk's own
+        atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
+        j = 0;
+      }
+      const int stage = s % kPaStages;
+      if (s >= kPaStages && !mbar_wait(&empty[stage], ((s / kPaStages) & 1) ^ 1, a.err)) return;
+      uint8_t* dst = ring + stage * kPaSlotBytes;
+      stage_j[stage] = j;
+      const int rr = bg * a.max_ctx + j * kBlock;
+      mbar_arrive_expect_tx(&full[stage], kPaSlotBytes);
+      tma_load_2d(dst, &mk, 0, rr, &full[stage]);
+      tma_load_2d(dst + kBlockBytes / 2, &mk, 64, rr, &full[stage]);
+      tma_load_2d(dst + kBlockBytes, &mv, 0, rr, &full[stage]);
+      tma_load_2d(dst + kBlockBytes + kBlockBytes / 2, &mv, 64, rr, &full[stage]);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers: one token each
+  const int tok = tok0 + warp;
+  const bool active = tok < T;
+  const int g8 = lane >> 2, cq = lane & 3;
+  const float sl2 = 1.4426950408889634f * 0.08838834764831845f;     // log2(e) / sqrt(128)
+  const __nv_bfloat16* q16 = a.q + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim;
+  uint32_t qf[8][4];
+  if (active) load_q_frags(q16, lane, qf);
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  bool ok = true;
+  for (int s = 0; s < n_sel; ++s) {
+    const int stage = s % kPaStages;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (s / kPaStages) & 1, a.err));
+    if (ok && active) {
+      const int j = stage_j[stage];
+      const uint8_t* Kt = ring + stage * kPaSlotBytes;
+      const uint8_t* Vt = Kt + kBlockBytes;
+      float sc[8][4];
+      qk_tile(qf, Kt, lane, sc);
+      // causal: keys after the token (only in the chunk's own block) are masked
+      const int kbase = j * kBlock + 2 * cq;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pos = kbase + 8 * n + (e & 1);
+          sc[n][e] = pos <= tok ? sc[n][e] * sl2 : -INFINITY;
+          if (e < 2) mx0 = fmaxf(mx0, sc[n][e]);
+          else mx1 = fmaxf(mx1, sc[n][e]);
+        }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        sc[n][0] = exp2f(sc[n][0] - base0);
+        sc[n][1] = exp2f(sc[n][1] - base0);
+        sc[n][2] = exp2f(sc[n][2] - base1);
+        sc[n][3] = exp2f(sc[n][3] - base1);
+        ps0 += sc[n][0] + sc[n][1];
+        ps1 += sc[n][2] + sc[n][3];
+      }
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= al0;
+        o[n][1] *= al0;
+        o[n][2] *= al1;
+        o[n][3] *= al1;
+      }
+      // O += P V, the keys of the block as 4 k-steps of 16
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t pa0 = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+        const uint32_t pa1 = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+        const uint32_t pa2 = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+        const uint32_t pa3 = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+        const int r = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int hi = lane >> 4;
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(swz_addr(Vt, r, 2 * np + hi), b0, b1, b2, b3);
+          mma_16816(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+          mma_16816(o[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) bar_arrive(&empty[stage]);
+  }
+  if (!active || !ok) return;
+  // out[tok, g*16 + h, :] = O / l (rows g8 and g8+8 of the accumulators)
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  __nv_bfloat16* o16 = a.out + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim;
+  uint32_t* r0p = reinterpret_cast<uint32_t*>(o16 + (size_t)g8 * kHeadDim);
+  uint32_t* r1p = reinterpret_cast<uint32_t*>(o16 + (size_t)(g8 + 8) * kHeadDim);
+#pragma unroll
+  for (int n = 0; n < 16; ++n) {
+    r0p[4 * n + cq] = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
+    r1p[4 * n + cq] = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+  }
+}
+
+// ==================================================================== baseline multi-head
+__global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const PrefillArgs a,
+                                                                          const __grid_constant__ CUtensorMap mck) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMhStages;
+  uint8_t* ring = smem + 1024;
+  float* part = reinterpret_cast<float*>(ring + kMhStages * kMhTileBytes);    // [2][8 warps][64]
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(part + 2 * kPaConsumerWarps * 64);
+  float* win_sum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sh) +
+                                            ((int)sizeof(TopkShared) + 15) / 16 * 16);   // [W_cap]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
+  const int c = a.nb_cap - 1 - (int)blockIdx.x;                // the longest chunks first
+  const int T = a.seq_len[b];
+  const int kslots = a.topk + 2;
+  const size_t row = (size_t)bg * a.nb_cap + c;
+  if (!valid_len(T, a.max_ctx) || c * kBlock >= T) {
+    if (!valid_len(T, a.max_ctx) && tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    for (int s = tid; s < kslots; s += blockDim.x) a.idx[row * kslots + s] = -1;
+    if (tid == 0) a.cnt[row] = 0;
+    return;
+  }
+  const int Wc = num_windows(c * kBlock);
+  const int n_wt = (Wc + 63) / 64;
+  const int n_tok = min(kBlock, T - c * kBlock);
+  const int n_sl = (n_tok + kPaConsumerWarps - 1) / kPaConsumerWarps;
+  const int n_loads = n_sl * 2 * n_wt;                           // slices x passes x tiles
+
+  if (tid == 0) {
+    for (int i = 0; i < kMhStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kPaConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid; i < Wc; i += blockDim.x) win_sum[i] = 0.f;
+  __syncthreads();
+
+  if (warp == kPaConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mck);
+      for (int it = 0; it < n_loads; ++it) {
+        const int m = it % n_wt;
+        const int stage = it % kMhStages;
+        if (it >= kMhStages && !mbar_wait(&empty[stage], ((it / kMhStages) & 1) ^ 1, a.err)) break;
+        uint8_t* dst = ring + stage * kMhTileBytes;
+        const int rr = bg * a.W_cap + m * 64;
+        mbar_arrive_expect_tx(&full[stage], kMhTileBytes);
+        tma_load_2d(dst, &mck, 0, rr, &full[stage]);
+        tma_load_2d(dst + kBlockBytes / 2, &mck, 64, rr, &full[stage]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cq = lane & 3;
+    const float zl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    bool ok = true;
+    int it = 0, tile_no = 0;
+    for (int s = 0; s < n_sl; ++s) {
+      const int tok = c * kBlock + s * kPaConsumerWarps + warp;
+      const bool active = tok < T;
+      uint32_t qf[8][4];
+      if (active) {
+        load_q_frags(a.q + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim, lane, qf);
+      }
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        for (int m = 0; m < n_wt; ++m, ++it) {
+          const int stage = it % kMhStages;
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kMhStages) & 1, a.err));
+          float sc[8][4];
+          if (ok && active) {
+            qk_tile(qf, ring + stage * kMhTileBytes, lane, sc);
+            const int ibase = m * 64 + 2 * cq;
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                sc[n][e] = (ibase + 8 * n + (e & 1)) < Wc ? sc[n][e] * zl2 : -INFINITY;
+          }
+          __syncwarp();
+          if (lane == 0) bar_arrive(&empty[stage]);
+          if (pass == 0) {
+            if (ok && active) {
+              float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+              for (int n = 0; n < 8; ++n) {
+                mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+                mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+              }
+              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+              const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+              const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+              const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+              float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+              for (int n = 0; n < 8; ++n) {
+                ps0 += exp2f(sc[n][0] - base0) + exp2f(sc[n][1] - base0);
+                ps1 += exp2f(sc[n][2] - base1) + exp2f(sc[n][3] - base1);
+              }
+              ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+              ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+              ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+              ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+              l0 = l0 * exp2f(m0 - base0) + ps0;
+              l1 = l1 * exp2f(m1 - base1) + ps1;
+              m0 = mn0;
+              m1 = mn1;
+            }
+          } else {
+            // normalised probabilities summed over this token's 16 heads, per window
+            float cs[8][2];
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+              cs[n][0] = cs[n][1] = 0.f;
+              if (ok && active) {
+                const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
+                cs[n][0] = exp2f(sc[n][0] - b0) * inv0 + exp2f(sc[n][2] - b1) * inv1;
+                cs[n][1] = exp2f(sc[n][1] - b0) * inv0 + exp2f(sc[n][3] - b1) * inv1;
+              }
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 4);
+                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 8);
+                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 16);
+              }
+            }
+            float* pw = part + ((tile_no & 1) * kPaConsumerWarps + warp) * 64;
+            if (lane < 4) {
+#pragma unroll
+              for (int n = 0; n < 8; ++n) {
+                pw[8 * n + 2 * lane] = cs[n][0];
+                pw[8 * n + 2 * lane + 1] = cs[n][1];
+              }
+            }
+            consumers_sync();
+            // the eight tokens' sums, added in warp order into the chunk's window sums
+            if (tid < 64) {
+              const float* pb = part + (tile_no & 1) * kPaConsumerWarps * 64;
+              float acc = 0.f;
+#pragma unroll
+              for (int w = 0; w < kPaConsumerWarps; ++w) acc += pb[w * 64 + tid];
+              const int i = m * 64 + tid;
+              if (i < Wc) win_sum[i] += acc;
+            }
+            ++tile_no;
+          }
+        }
+      }
+    }
+    consumers_sync();
+    // max-pool onto blocks j <= c (windows 4j-1 .. 4j+3 below Wc), then the top-k
+    float* S = a.block_scores + row * a.nb_cap;
+    for (int j = tid; j <= c; j += kPaConsumerWarps * 32) {
+      float v = -INFINITY;
+      for (int i = max(0, 4 * j - 1); i <= min(Wc - 1, 4 * j + 3); ++i) v = fmaxf(v, win_sum[i]);
+      S[j] = v;
+    }
+    __threadfence_block();
+    consumers_sync();
+    topk_select(S, a.idx + row * kslots, a.cnt + row, a.topk, a.max_ctx, c * kBlock + 1, sh);
+  }
+}
+
+// ==================================================================== launches
+void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s) {
+  const int n_ct = (a.nb_cap + kPfChunks - 1) / kPfChunks;
+  prefill_forecast_score_kernel<<<dim3(n_ct, batch * a.G), kPfThreads, 0, s>>>(a);
+  prefill_topk_kernel<<<dim3(a.nb_cap, batch * a.G), kTopkThreads, 0, s>>>(a);
+}
+
+void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mck, int batch, cudaStream_t s) {
+  const int smem = mh_smem_bytes(a.W_cap);
+  cudaFuncSetAttribute(prefill_multihead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  prefill_multihead_kernel<<<dim3(a.nb_cap, batch * a.G), kPaThreads, smem, s>>>(a, mck);
+}
+
+void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, int batch,
+                         cudaStream_t s) {
+  cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPaSmem);
+  prefill_attn_kernel<<<dim3(a.nb_cap * kSlices, batch * a.G), kPaThreads, kPaSmem, s>>>(a, mk, mv);
+}
+
+}  // namespace sparda

@@ -74,6 +74,7 @@ extern "C" {
 #define SPARDA_WS_SELECT      1
 #define SPARDA_WS_ATTN        2
 #define SPARDA_WS_MULTIHEAD   3
+#define SPARDA_WS_PREFILL     4
 
 /* ---------------------------------------------------------------- shapes */
 /*
@@ -424,6 +425,68 @@ int32_t sparda_multihead_select(const sparda_shape* shape, const void* ck, const
 int32_t sparda_forecast_select_static(const sparda_shape* shape, const void* ck,
                                       const void* forecast, const int32_t* seq_len,
                                       int32_t batch, int32_t* idx, int32_t* cnt, void* stream);
+
+/* ---------------------------------------------------------------- chunked prefill */
+/*
+ * Prefill processes a whole prompt. The pages give its figures (bittide thread and abstract:
+ * up to 1.25x faster prefill than the sparse offload baseline; techwalker section 五: in
+ * prefill the block-sparse attention dominates, the block selection grows with the context
+ * and nears it at 128K, and the Forecast indexer cuts the selection cost by up to 2.5x while
+ * the attention is unchanged; 10100 "SparDA 的解法": in prefill all keys are already on the
+ * GPU, so only the cheaper selection helps) but not the prefill selection itself. This
+ * library takes these readings:
+ *   - the prompt is split into chunks of 64 query tokens; chunk c = tokens 64c .. 64c+63
+ *     (the last chunk of a sequence may be shorter), n_chunks = ceil(T / 64);
+ *   - the tokens of a chunk share one selection: block 0, the chunk's own block c, and the
+ *     topk best of blocks 1 .. c-1, ties to the lower block, ascending, -1 padded, scored
+ *     over the compressed keys complete before the chunk (windows i < (64c - 32) / 16 + 1);
+ *   - every token attends its chunk's blocks up to its own position (causal in block c).
+ * Per-chunk outputs: idx int32 [B, G, max_ctx/64, topk+2] and cnt int32 [B, G, max_ctx/64]
+ * (row c of (b, g) for chunk c; chunks past the prompt get cnt 0 and idx -1). seq_len[b] is
+ * the prompt length T (1 <= T <= max_ctx). The compressed keys must hold every window of the
+ * prompt (sparda_compress_keys with seq_len = T). workspace: SPARDA_WS_PREFILL (float32
+ * block scores [max_batch * G, max_ctx/64, max_ctx/64]: 16 MiB per sequence-group at
+ * max_ctx 131072; no zero-fill needed). The calls wait for the kernel before them in the
+ * stream to finish (no programmatic overlap).
+ */
+
+/*
+ * sparda_prefill_forecast_select -- the Forecast selector on prefill chunks: window i of
+ * chunk c scores sum over the chunk's tokens t of f_t . ck_i (the decode score summed over
+ * the chunk, no softmax, no scale), max-pooled onto blocks as in decode. forecast: device
+ * bf16 [max_batch, max_ctx, G, d], the per-token forecast vectors (the fourth projection of
+ * the prompt's hidden states, one head per group). The chunk's forecasts are summed in
+ * float32 and the dot products run in float32.
+ */
+int32_t sparda_prefill_forecast_select(const sparda_shape* shape, const void* ck, const void* forecast,
+                                       const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sparda_prefill_multihead_select -- the baseline query-driven selector on prefill chunks:
+ * every (token, head) query of the chunk gets its own softmax over the windows before the
+ * chunk (logits scaled by 1/sqrt(d)), and the probabilities are summed over the chunk's
+ * tokens and the group's heads; then the same max-pool and top-k. q: device bf16
+ * [max_batch, max_ctx, G*H, d]. The logits run on tensor cores (bf16 operands, float32
+ * accumulation); the softmax and the sums are float32.
+ */
+int32_t sparda_prefill_multihead_select(const sparda_shape* shape, const void* ck, const void* q,
+                                        const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sparda_prefill_attn -- causal block-sparse prefill attention of a resident layer: for
+ * every token t of chunk c and query head h of group g,
+ *   out[b, t, g*H + h, :] = sum_u softmax_u(q[b, t, g*H + h] . k_u / sqrt(d)) v_u
+ * over the tokens u <= t of the blocks idx[b, g, c, 0 .. cnt[b, g, c]-1] (as the prefill
+ * selectors write them; a block index outside 0 .. c sets SPARDA_DEV_BAD_INDEX and reads
+ * block 0 instead). q, out: device bf16 [max_batch, max_ctx, G*H, d]; the layer's k, v hold
+ * the prompt's keys and values. QK^T and PV on tensor cores (bf16 operands, float32
+ * accumulation), float32 softmax. SPARDA_ERR_INVALID_ARG for an offloaded layer.
+ */
+int32_t sparda_prefill_attn(const sparda_shape* shape, const sparda_layer_kv* layer, const void* q,
+                            const int32_t* idx, const int32_t* cnt, const int32_t* seq_len, int32_t batch,
+                            void* out, void* stream);
 
 #ifdef __cplusplus
 }
