@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--no-offload", action="store_true", help="skip the batch-64 offload measurement")
     p.add_argument("--offload-steps", type=int, default=20)
     p.add_argument("--no-selector-ab", action="store_true", help="skip the selector A/B sweep")
+    p.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill A/B")
     p.add_argument("--layout", default="pipelined", choices=["pipelined", "fused"],
                    help="launch layout of the resident step (the same arithmetic in each)")
     p.add_argument("--layers", type=int, default=N_LAYERS,
@@ -367,25 +368,33 @@ def run_offload(device, seed, steps, warmup):
     def ffn(L):
         torch.mm(x, Wffn[L % OFF_DISTINCT], out=y)
 
-    def make(lays, overlap):
+    def make(lays, overlap, block_cache=None):
         st = DecodeStack(shape, lays, W_self0, W_next, B, device=device, overlap=overlap, advance=True,
-                         after_attention=ffn)
+                         after_attention=ffn, block_cache=block_cache)
         st.h.copy_(synth.normal_bf16_device(st.h.shape, seed * 1000 + 820, device))
         st.q.copy_(synth.normal_bf16_device(st.q.shape, seed * 1000 + 821, device))
         st.k_new.copy_(synth.normal_bf16_device(st.k_new.shape, seed * 1000 + 822, device))
         st.v_new.copy_(synth.normal_bf16_device(st.v_new.shape, seed * 1000 + 823, device))
         return st
 
-    def time_stack(st):
+    def time_stack(st, h_bank=None):
+        """Mean step time; with h_bank, every step first takes the next hidden states of the bank
+        (a device copy on the same stream), so that consecutive steps select different blocks."""
         st.seq_len.fill_(T0)
         st.capture()
-        for _ in range(warmup):
+        for i in range(warmup):
+            if h_bank is not None:
+                st.h.copy_(h_bank[i % len(h_bank)])
             st.run()
         torch.cuda.synchronize()
+        if st.cache_stats is not None:
+            st.cache_stats.zero_()
         s = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        for _ in range(steps):
+        for i in range(steps):
+            if h_bank is not None:
+                st.h.copy_(h_bank[(warmup + i) % len(h_bank)])
             st.run()
         e1.record(s)
         torch.cuda.synchronize()
@@ -400,6 +409,32 @@ def run_offload(device, seed, steps, warmup):
     del st_pg
     t_no = time_stack(make(layers, False))
     t_res = time_stack(make(resident, True))
+    # the cross-step block cache (an extension beyond the pages): each offloaded layer keeps
+    # topk + 2 gathered blocks per (sequence, group) in HBM and gathers only the ones it lacks.
+    # Measured with the hidden states constant across steps (consecutive steps select nearly
+    # the same blocks: the best case) and with new hidden states every step (independent
+    # selections: the worst case); real decoding lies between.
+    cache_res = {}
+    h_bank = [synth.normal_bf16_device((N_LAYERS, B, HIDDEN), seed * 1000 + 830 + i, device) for i in range(4)]
+    for name, bank in (("same_hidden_every_step", None), ("new_hidden_every_step", h_bank)):
+        st_bc = make(layers, True, block_cache=TOPK + 2)
+        t_bc = time_stack(st_bc, bank)
+        hits, misses = st_bc.cache_stats.cpu().tolist()
+        cache_res[name] = {"tok_s": B / t_bc, "ms_per_step": t_bc * 1e3, "hit_rate": hits / max(1, hits + misses),
+                           "blocks_gathered_per_step": misses / steps,
+                           "offload_vs_resident_time": t_bc / t_res}
+        del st_bc
+        gc.collect()
+        torch.cuda.empty_cache()
+    del h_bank
+    cache_res["slots_per_group"] = TOPK + 2
+    # without the cache, at new hidden states every step (the comparison for the worst case)
+    h_bank = [synth.normal_bf16_device((N_LAYERS, B, HIDDEN), seed * 1000 + 830 + i, device) for i in range(4)]
+    st_nb = make(layers, True)
+    cache_res["no_cache_new_hidden_every_step_tok_s"] = B / time_stack(st_nb, h_bank)
+    del st_nb, h_bank
+    gc.collect()
+    torch.cuda.empty_cache()
     # the gather alone: the step's own 31 gathers (last step's selections), per launch
     gbytes = B * G * TOPK * 2 * 64 * D * 2
 
@@ -414,6 +449,27 @@ def run_offload(device, seed, steps, warmup):
     for n in (8, 16, 32, 64, 152):
         sweep[str(n)] = gbytes / gathers(n) / 1e9
     t_g = gathers(0)
+    # the copy-engine alternative for one layer's gather: the selection read back to the host,
+    # then one cudaMemcpyAsync per run of consecutive selected blocks (K and V); wall time from
+    # the selection on the device to the copies done, and the copies' own device time
+    L1 = 1
+    ce_times, ce_dev, n_copies = [], [], 0
+    for rep in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ih, ch, sh = st_ov.idx[L1].cpu(), st_ov.cnt[L1].cpu(), st_ov.seq_len.cpu()     # each waits on the device
+        s_ce = torch.cuda.current_stream()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(s_ce)
+        n_copies = sb.sparda_prefetch_blocks_copy_engine(shape, st_ov.layers[L1], ih, ch, sh, B, st_ov.stage_k[0],
+                                                         st_ov.stage_v[0], stream=s_ce)
+        a1.record(s_ce)
+        torch.cuda.synchronize()
+        ce_times.append(time.perf_counter() - t0)
+        ce_dev.append(a0.elapsed_time(a1) * 1e-3)
+    ce = {"copies_per_layer": n_copies, "wall_ms_per_layer": min(ce_times) * 1e3,
+          "device_ms_per_layer": min(ce_dev) * 1e3, "gbs_wall": gbytes / min(ce_times) / 1e9,
+          "vs_sm_gather_time": min(ce_times) / t_g}
     # host link: one pinned 1 GiB host-to-device copy
     hb = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
     db = torch.empty(1 << 30, dtype=torch.uint8, device=device)
@@ -440,7 +496,9 @@ def run_offload(device, seed, steps, warmup):
         "gather_gbs_while_overlapping": (N_LAYERS - 1) * gbytes / t_ov / 1e9,
         "gather_link_frac_while_overlapping": (N_LAYERS - 1) * gbytes / t_ov / 1e9 / link,
         "link_peak_gbs": link,
-        "host_buffers": "4 distinct 8 GiB K/V pairs aliased over layers 1-31 (bytes gathered per step unchanged)",
+        "host_buffers": "4 distinct 8.6 GB K/V pairs aliased over layers 1-31 (bytes gathered per step unchanged)",
+        "block_cache": cache_res,
+        "copy_engine_gather": ce,
         "device_error_flags": sb.sparda_device_error(clear=True),
     })
     del st_ov, layers, resident, devK, devV, hostK, hostV, cks, hb, db
@@ -456,7 +514,8 @@ def selector_ab(device, seed):
     head, sum, max-pool, top-32), for batch 1..128 at context 131072 and for context 32K..128K
     at batch 16. Compressed keys, forecasts and queries are seeded N(0,1) bf16 drawn on the
     device (selection time does not depend on their values). Device time per call from CUDA
-    graph replays; GB/s counts the compressed keys and forecast/query bytes each call reads."""
+    graph replays; GB/s counts every byte each call moves (compressed keys, forecast or
+    queries, block scores written and read back, selection)."""
     import torch
     import synth
     import block_sparse_attention_forecast_gb300.binding as sb
@@ -476,8 +535,12 @@ def selector_ab(device, seed):
         W = num_windows(T - 1)
         t_f = graph_time(lambda s: sb.sparda_forecast_select(shape, ck, f, seq, B, idx, cnt, ws, stream=s), 8)
         t_m = graph_time(lambda s: sb.sparda_multihead_select(shape, ck, q, seq, B, idx, cnt, wm, stream=s), 8)
-        bytes_f = B * G * (W * D * 2 + D * 2)
-        bytes_m = B * G * (W * D * 2 + H * D * 2)
+        # every byte each call moves: the compressed keys, the forecast (or the 16 queries), the
+        # float32 block scores written and read back by the top-k, and the selection written
+        nb = (T - 1) // 64 + 1
+        tail = nb * 4 * 2 + (TOPK + 2) * 4 + 4
+        bytes_f = B * G * (W * D * 2 + D * 2 + tail)
+        bytes_m = B * G * (W * D * 2 + H * D * 2 + tail)
         del ck, ws, wm
         torch.cuda.empty_cache()
         return {"forecast_us": t_f * 1e6, "multihead_us": t_m * 1e6, "speedup": t_m / t_f,
@@ -701,6 +764,9 @@ def run_ours(args):
     ab = None
     if world == 1 and not args.no_selector_ab:
         ab = selector_ab(device, args.seed)
+    pf = None
+    if world == 1 and not args.no_prefill:
+        pf = prefill_ab(device, args.seed)
     elapsed, e2e_elapsed = replica_max([elapsed, e2e_elapsed], dist, device)
     if rank != 0:
         dist.destroy_process_group()
@@ -748,6 +814,8 @@ def run_ours(args):
         line["offload"] = offload
     if ab is not None:
         line["selector_ab"] = ab
+    if pf is not None:
+        line["prefill"] = pf
     if cpu is not None:
         per_step, cores, desc = cpu
         line["cpu_baseline"] = {"value": BATCH / per_step, "unit": "tok/s", "cores": cores, "kind": "oracle",

@@ -26,6 +26,8 @@ __all__ = [
     "sparda_prefetch_blocks", "sparda_multihead_select", "sparda_forecast_select_static", "sparda_attend_and_select",
     "sparda_attend_and_score", "sparda_decode_prologue", "sparda_forecast_score", "sparda_copy",
     "sparda_prefill_forecast_select", "sparda_prefill_multihead_select", "sparda_prefill_attn",
+    "sparda_prefetch_blocks_cached", "sparda_sparse_decode_attn_cached", "BlockCache",
+    "sparda_prefetch_blocks_copy_engine",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED_SHAPE", "ERR_MISALIGNED", "ERR_NOT_MAPPED_HOST",
     "ERR_WORKSPACE_TOO_SMALL", "ERR_CUDA", "ERR_STATIC_SCRATCH_LIMIT", "DEV_WAIT_TIMEOUT", "DEV_BAD_SEQ_LEN", "DEV_BAD_INDEX",
     "WS_SELECT", "WS_ATTN", "WS_MULTIHEAD", "WS_PREFILL", "BLOCK", "WIN_KERNEL", "WIN_STRIDE",
@@ -109,6 +111,9 @@ def _load():
         "sparda_prefill_forecast_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
         "sparda_prefill_multihead_select": (I32, [SH, P, P, P, I32, P, P, P, SZ, P]),
         "sparda_prefill_attn": (I32, [SH, LY, P, P, P, P, I32, P, P]),
+        "sparda_prefetch_blocks_cached": (I32, [SH, LY, P, P, P, I32, P, P, P, I32, P, P, P, I32, P]),
+        "sparda_prefetch_blocks_copy_engine": (I32, [SH, LY, P, P, P, I32, P, P, P, P]),
+        "sparda_sparse_decode_attn_cached": (I32, [SH, LY, P, P, I32, P, P, P, P, P, I32, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -402,3 +407,57 @@ def sparda_prefill_attn(shape, layer, q, idx, cnt, seq_len, batch, out, stream=N
     _check("sparda_prefill_attn", lib.sparda_prefill_attn(
         ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(q), _ptr(idx), _ptr(cnt), _ptr(seq_len),
         int(batch), _ptr(out), _stream(stream)))
+
+
+# ------------------------------------------------------------------ cross-step block cache
+class BlockCache:
+    """The block cache of one offloaded layer (include/sparda.h): n_cache HBM slots per
+    (sequence, group) holding blocks gathered at earlier steps, the block each slot holds
+    (-1: none), the slot of each idx entry, and the gather's scratch."""
+
+    def __init__(self, shape, n_cache=None, device="cuda"):
+        n = shape.kslots if n_cache is None else int(n_cache)
+        B, G = shape.max_batch, shape.n_groups
+        self.n_cache = n
+        self.k = torch.zeros((B, G, n, shape.block, shape.head_dim), dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.blocks = torch.full((B, G, n), -1, dtype=torch.int32, device=device)
+        self.slot = torch.full((B, G, shape.kslots), -1, dtype=torch.int32, device=device)
+        self.fetch = torch.full((B, G, n), -1, dtype=torch.int32, device=device)
+
+    def reset(self):
+        self.blocks.fill_(-1)
+
+
+def sparda_prefetch_blocks_cached(shape, layer, idx, cnt, seq_len, batch, cache, stats=None, n_ctas=0,
+                                  stream=None):
+    """Gather of the selected blocks not yet in `cache` (a BlockCache); stats: optional int64
+    tensor [2] on the device accumulating hits and misses."""
+    _check("sparda_prefetch_blocks_cached", lib.sparda_prefetch_blocks_cached(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(idx), _ptr(cnt), _ptr(seq_len), int(batch),
+        _ptr(cache.k), _ptr(cache.v), _ptr(cache.blocks), int(cache.n_cache), _ptr(cache.slot), _ptr(cache.fetch),
+        _ptr(stats), int(n_ctas), _stream(stream)))
+
+
+def sparda_sparse_decode_attn_cached(shape, layer, cache, q, idx, cnt, seq_len, batch, out, ws, stream=None):
+    """Attention of an offloaded layer over its selected blocks, read from `cache`."""
+    _check("sparda_sparse_decode_attn_cached", lib.sparda_sparse_decode_attn_cached(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), _ptr(cache.k), _ptr(cache.v), int(cache.n_cache),
+        _ptr(cache.slot), _ptr(q), _ptr(idx), _ptr(cnt), _ptr(seq_len), int(batch), _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def sparda_prefetch_blocks_copy_engine(shape, layer, idx_host, cnt_host, seq_len_host, batch, staging_k, staging_v,
+                                       stream=None):
+    """The gather by one cudaMemcpyAsync per run of consecutive selected blocks; the selection
+    (idx_host, cnt_host, seq_len_host) must be int32 CPU tensors. Returns the number of copies
+    issued."""
+    for t in (idx_host, cnt_host, seq_len_host):
+        if t.device.type != "cpu" or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("the copy-engine gather takes the selection as contiguous int32 CPU tensors")
+    n = ctypes.c_int32(0)
+    _check("sparda_prefetch_blocks_copy_engine", lib.sparda_prefetch_blocks_copy_engine(
+        ctypes.byref(shape.c()), ctypes.byref(layer.c()), ctypes.c_void_p(idx_host.data_ptr()),
+        ctypes.c_void_p(cnt_host.data_ptr()), ctypes.c_void_p(seq_len_host.data_ptr()), int(batch),
+        _ptr(staging_k), _ptr(staging_v), ctypes.byref(n), _stream(stream)))
+    return n.value

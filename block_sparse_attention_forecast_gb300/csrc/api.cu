@@ -82,12 +82,6 @@ size_t attn_ml_bytes(const sparda_shape* s) {
   return round256((size_t)s->max_batch * s->n_groups * attn_splits(s) * 2 * kHeads * sizeof(float));
 }
 
-size_t mh_z_bytes(const sparda_shape* s) {
-  return round256((size_t)s->max_batch * s->n_groups * kHeads * w_cap(s) * sizeof(float));
-}
-size_t mh_stats_bytes(const sparda_shape* s) {
-  return round256((size_t)s->max_batch * s->n_groups * multihead_tiles(w_cap(s)) * kHeads * sizeof(float2));
-}
 
 int32_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return SPARDA_OK;
@@ -206,7 +200,7 @@ size_t sparda_workspace_bytes(const sparda_shape* s, int32_t batch, int32_t kind
   switch (kind) {
     case SPARDA_WS_SELECT: return kQueueBytes + counters_bytes(s) + select_data_bytes(s);
     case SPARDA_WS_ATTN: return counters_bytes(s) + attn_o_bytes(s) + attn_ml_bytes(s);
-    case SPARDA_WS_MULTIHEAD: return mh_z_bytes(s) + mh_stats_bytes(s) + select_data_bytes(s);
+    case SPARDA_WS_MULTIHEAD: return select_data_bytes(s);
     case SPARDA_WS_PREFILL: return round256((size_t)s->max_batch * s->n_groups * nb_cap(s) * nb_cap(s) * sizeof(float));
     default: return 0;
   }
@@ -328,7 +322,8 @@ int32_t prepare_select(const sparda_shape* s, const void* ck, const void* foreca
 int32_t prepare_attn(const sparda_shape* s, const sparda_layer_kv* L, const void* staging_k,
                      const void* staging_v, const void* q, const int32_t* idx, const int32_t* cnt,
                      const int32_t* seq_len, int32_t batch, void* out, void* ws, size_t ws_bytes,
-                     AttnArgs* args, CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* hk, CUtensorMap* hv) {
+                     AttnArgs* args, CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* hk, CUtensorMap* hv,
+                     int staging_slots = 0) {
   SPARDA_TRY(shape_status(s));
   SPARDA_TRY(batch_status(s, batch));
   if (!L || !q || !idx || !cnt || !seq_len || !out || !ws) return SPARDA_ERR_INVALID_ARG;
@@ -340,8 +335,9 @@ int32_t prepare_attn(const sparda_shape* s, const sparda_layer_kv* L, const void
     if (!staging_k || !staging_v || !L->hot_k || !L->hot_v) return SPARDA_ERR_INVALID_ARG;
     if (!aligned(staging_k, 16) || !aligned(staging_v, 16) || !aligned(L->hot_k, 16) || !aligned(L->hot_v, 16))
       return SPARDA_ERR_MISALIGNED;
-    SPARDA_TRY(make_kv_map(mk, staging_k, bgcap * kslots(s) * kBlock));
-    SPARDA_TRY(make_kv_map(mv, staging_v, bgcap * kslots(s) * kBlock));
+    const uint64_t per_bg = (uint64_t)(staging_slots > 0 ? staging_slots : kslots(s));
+    SPARDA_TRY(make_kv_map(mk, staging_k, bgcap * per_bg * kBlock));
+    SPARDA_TRY(make_kv_map(mv, staging_v, bgcap * per_bg * kBlock));
     SPARDA_TRY(make_kv_map(hk, L->hot_k, bgcap * kHotSlots * kBlock));
     SPARDA_TRY(make_kv_map(hv, L->hot_v, bgcap * kHotSlots * kBlock));
   } else {
@@ -523,11 +519,10 @@ int32_t sparda_multihead_select(const sparda_shape* s, const void* ck, const voi
   SPARDA_TRY(make_kv_map(&mck, ck, (uint64_t)s->max_batch * s->n_groups * w_cap(s)));
   int* err = dev_error_ptr();
   if (!err) return SPARDA_ERR_CUDA;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  MultiheadArgs a{static_cast<const __nv_bfloat16*>(q), seq_len, idx, cnt, reinterpret_cast<float*>(w),
-                  reinterpret_cast<float2*>(w + mh_z_bytes(s)),
-                  reinterpret_cast<float*>(w + mh_z_bytes(s) + mh_stats_bytes(s)), err, s->n_groups, w_cap(s),
-                  s->max_ctx, nb_cap(s), s->topk, multihead_tiles(w_cap(s))};
+  const int n_tiles = multihead_tiles(w_cap(s));
+  const int ncl = multihead_cluster_size(n_tiles, batch * s->n_groups);
+  MultiheadArgs a{static_cast<const __nv_bfloat16*>(q), seq_len, idx, cnt, static_cast<float*>(ws), err,
+                  s->n_groups, w_cap(s), s->max_ctx, nb_cap(s), s->topk, ncl, (n_tiles + ncl - 1) / ncl};
   launch_multihead_select(a, mck, batch * s->n_groups, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
@@ -600,6 +595,95 @@ int32_t sparda_prefill_attn(const sparda_shape* s, const sparda_layer_kv* L, con
                 s->max_ctx, nb_cap(s), s->topk};
   launch_prefill_attn(a, mk, mv, batch, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
+}
+
+
+// ------------------------------------------------------------------ cross-step block cache
+int32_t sparda_prefetch_blocks_cached(const sparda_shape* s, const sparda_layer_kv* L, const int32_t* idx,
+                                      const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* cache_k,
+                                      void* cache_v, int32_t* cache_blocks, int32_t n_cache, int32_t* slot,
+                                      int32_t* fetch, unsigned long long* stats, int32_t n_ctas, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!L || !L->on_host) return SPARDA_ERR_INVALID_ARG;
+  SPARDA_TRY(layer_status(L, true));
+  if (!idx || !cnt || !seq_len || !cache_k || !cache_v || !cache_blocks || !slot || !fetch || n_ctas < 0 ||
+      n_ctas > 4096)
+    return SPARDA_ERR_INVALID_ARG;
+  if (n_cache < kslots(s) || n_cache > 128) return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(cache_k, 16) || !aligned(cache_v, 16) || !aligned(cache_blocks, 4) || !aligned(slot, 4) ||
+      !aligned(fetch, 4) || !aligned(stats, 8))
+    return SPARDA_ERR_MISALIGNED;
+  int* err = dev_error_ptr();
+  if (!err) return SPARDA_ERR_CUDA;
+  CacheArgs a{static_cast<const __nv_bfloat16*>(L->k), static_cast<const __nv_bfloat16*>(L->v), idx, cnt, seq_len,
+              cache_blocks, slot, fetch, stats, static_cast<__nv_bfloat16*>(cache_k),
+              static_cast<__nv_bfloat16*>(cache_v), err, batch, s->n_groups, s->max_ctx, kslots(s), n_cache};
+  launch_cache_gather(a, n_ctas ? n_ctas : sparda_prefetch_default_ctas(batch), static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+int32_t sparda_sparse_decode_attn_cached(const sparda_shape* s, const sparda_layer_kv* L, const void* cache_k,
+                                         const void* cache_v, int32_t n_cache, const int32_t* slot, const void* q,
+                                         const int32_t* idx, const int32_t* cnt, const int32_t* seq_len,
+                                         int32_t batch, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!L || !L->on_host || !slot) return SPARDA_ERR_INVALID_ARG;
+  if (n_cache < kslots(s) || n_cache > 128) return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(slot, 4)) return SPARDA_ERR_MISALIGNED;
+  AttnArgs a;
+  CUtensorMap mk, mv, hk, hv;
+  SPARDA_TRY(prepare_attn(s, L, cache_k, cache_v, q, idx, cnt, seq_len, batch, out, ws, ws_bytes, &a, &mk, &mv,
+                          &hk, &hv, n_cache));
+  a.stage_slot = slot;
+  a.stage_slots = n_cache;
+  launch_sparse_attn(a, mk, mv, hk, hv, batch * s->n_groups, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+
+// ------------------------------------------------------------------ copy-engine gather
+int32_t sparda_prefetch_blocks_copy_engine(const sparda_shape* s, const sparda_layer_kv* L, const int32_t* idx_host,
+                                           const int32_t* cnt_host, const int32_t* seq_len_host, int32_t batch,
+                                           void* staging_k, void* staging_v, int32_t* n_copies, void* stream) {
+  SPARDA_TRY(shape_status(s));
+  SPARDA_TRY(batch_status(s, batch));
+  if (!L || !L->on_host) return SPARDA_ERR_INVALID_ARG;
+  SPARDA_TRY(layer_status(L, true));
+  if (!idx_host || !cnt_host || !seq_len_host || !staging_k || !staging_v) return SPARDA_ERR_INVALID_ARG;
+  if (!aligned(staging_k, 16) || !aligned(staging_v, 16)) return SPARDA_ERR_MISALIGNED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ks = kslots(s);
+  const size_t blk = (size_t)kBlock * kHeadDim * 2;                 // bytes of one block of K (or V)
+  int copies = 0;
+  for (int bg = 0; bg < batch * s->n_groups; ++bg) {
+    const int T = seq_len_host[bg / s->n_groups];
+    if (T < 1 || T > s->max_ctx) return SPARDA_ERR_INVALID_ARG;
+    const int tb = (T - 1) / kBlock;
+    const int n = cnt_host[bg] < 0 ? 0 : (cnt_host[bg] > ks ? ks : cnt_host[bg]);
+    const int32_t* row = idx_host + (size_t)bg * ks;
+    for (int sl = 0; sl < n;) {
+      const int j = row[sl];
+      if (j == 0 || j == tb) {
+        ++sl;
+        continue;
+      }
+      if (j < 0 || j > tb) return SPARDA_ERR_INVALID_ARG;
+      // a run of consecutive blocks in consecutive slots is one contiguous range on both sides
+      int e = sl + 1;
+      while (e < n && row[e] == row[e - 1] + 1 && row[e] != tb) ++e;
+      const size_t src = ((size_t)bg * s->max_ctx + (size_t)j * kBlock) * kHeadDim * 2;
+      const size_t dst = ((size_t)bg * ks + sl) * blk;
+      const size_t bytes = (size_t)(e - sl) * blk;
+      SPARDA_TRY(cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(staging_k) + dst,
+                                             static_cast<const uint8_t*>(L->k) + src, bytes, cudaMemcpyDefault, st)));
+      SPARDA_TRY(cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(staging_v) + dst,
+                                             static_cast<const uint8_t*>(L->v) + src, bytes, cudaMemcpyDefault, st)));
+      copies += 2;
+      sl = e;
+    }
+  }
+  if (n_copies) *n_copies = copies;
+  return SPARDA_OK;
 }
 
 }  // extern "C"

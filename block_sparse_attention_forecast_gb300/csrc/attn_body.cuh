@@ -144,6 +144,13 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
           } else if (j == 0 || j == gi.tb) {
             hot = 1;
             row = (bg * kHotSlots + hot_slot(j)) * kBlock;
+          } else if (a.stage_slot) {
+            int cs = a.stage_slot[u];             // its block-cache slot
+            if (cs < 0 || cs >= a.stage_slots) {
+              atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
+              cs = 0;
+            }
+            row = (bg * a.stage_slots + cs) * kBlock;
           } else {
             row = u * kBlock;                   // staging slot (bg, s) = unit u
           }

@@ -80,6 +80,10 @@ struct AttnArgs {
   // > 0: the grid is seg_per_group CTAs per (sequence, group), each taking an equal share of
   // that group's slots (no CTA spans two groups); 0: contiguous balanced unit ranges
   int seg_per_group = 0;
+  // offload with the block cache: idx entry u's staged block is in row block
+  // (bg * stage_slots + stage_slot[u]) of the staging map; nullptr: row block u
+  const int32_t* stage_slot = nullptr;
+  int stage_slots = 0;
 };
 
 struct MultiheadArgs {
@@ -87,11 +91,11 @@ struct MultiheadArgs {
   const int32_t* seq_len;
   int32_t* idx;                  // [B, G, topk+2]
   int32_t* cnt;                  // [B, G]
-  float* z;                      // workspace [B*G, H, W_cap] head scores (exp2 domain)
-  float2* stats;                 // workspace [B*G, n_tiles, H] per-tile (max, sum exp2)
   float* block_scores;           // workspace [B*G, nb_cap]
   int* err;
-  int G, W_cap, max_ctx, nb_cap, topk, n_tiles;
+  int G, W_cap, max_ctx, nb_cap, topk;
+  int cluster;                   // CTAs per (sequence, group): one thread-block cluster
+  int tiles_per_cta;             // 64-window tiles a CTA holds at most (shared-memory sizing)
 };
 
 struct PrefetchArgs {
@@ -105,6 +109,24 @@ struct PrefetchArgs {
   int* err;
   int B, G, max_ctx, kslots;
 };
+
+// The cross-step block cache of an offloaded layer (prefetch.cu).
+struct CacheArgs {
+  const __nv_bfloat16* hk;       // host cache (UVA) [B, G, max_ctx, d]
+  const __nv_bfloat16* hv;
+  const int32_t* idx;            // [B, G, kslots]
+  const int32_t* cnt;            // [B, G]
+  const int32_t* seq_len;
+  int32_t* cache_blocks;         // [max_batch*G, n_cache], persistent: block held per slot, -1 none
+  int32_t* slot;                 // [B, G, kslots] out: cache slot of each idx entry (-1: hot / none)
+  int32_t* fetch;                // [max_batch*G, n_cache] scratch: block to fetch per slot, -1 none
+  unsigned long long* stats;     // optional [2]: hits, misses (accumulated)
+  __nv_bfloat16* ck_cache;       // [max_batch, G, n_cache, 64, d]
+  __nv_bfloat16* cv_cache;
+  int* err;
+  int B, G, max_ctx, kslots, n_cache;
+};
+void launch_cache_gather(const CacheArgs& a, int n_ctas, cudaStream_t s);
 
 void launch_append_kv(const AppendArgs& a, int bg_count, cudaStream_t s);
 void launch_compress_keys(const CompressArgs& a, int bg_count, cudaStream_t s);
@@ -151,6 +173,7 @@ void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mc
 void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, int batch,
                          cudaStream_t s);
 int multihead_tiles(int w_cap);
+int multihead_cluster_size(int n_tiles_cap, int bg_count);
 
 // Device address of the library's device error word on the current device (api.cu).
 int* dev_error_word();

@@ -2,196 +2,344 @@
 // the standard selector; 10100 "先把痛点讲透"): every query head of a GQA group scores every
 // compressed key, each head's scores go through a softmax over the windows, the per-head
 // probabilities are summed over the group, and the sums are max-pooled onto blocks for the
-// same top-k as the Forecast selector. Built as the comparison point for the selector A/B.
+// same top-k as the Forecast selector. Built as the comparison point for the selector A/B,
+// engineered like the Forecast selector: the compressed keys are read from HBM once, and no
+// per-head score leaves the chip.
 //
-// Kernel 1, grid (64-window tiles, sequence-groups), 4 warps: the tile of compressed keys is
-// one 64 x 128 bf16 box pair loaded by TMA with the 128-byte swizzle (the layout of a K block
-// in the attention kernel); z = Q ck^T for the group's 16 heads runs on m16n8k16 bf16 MMAs,
-// in the exp2 domain (scale log2(e)/sqrt(d)). It stores z and, per head, the tile's maximum
-// and sum of exp2(z - max).
-// Kernel 2, one CTA of 256 threads per sequence-group: combines the tile statistics into each
-// head's softmax normaliser, forms s[i] = sum_h exp2(z[h][i] - M_h) / L_h in shared memory,
-// max-pools the windows 4j-1 .. 4j+3 onto block j, and runs the exact top-k.
+// One thread-block cluster of NC CTAs per sequence-group (NC = 1 .. 8, chosen so that the
+// clusters fill the GPU and each CTA's share of the windows fits in shared memory). CTA r of
+// the cluster owns a contiguous range of 64-window tiles:
+//   * a producer warp streams its tiles by TMA (one 64 x 128 bf16 box pair, 128-byte
+//     swizzle) into a ring of full/empty mbarriers;
+//   * two groups of four consumer warps take alternate tiles; warp w of a group computes the
+//     logits of windows 16w .. 16w+15 for the group's 16 heads on m16n8k16 bf16 MMAs
+//     (exp2 domain, scale log2(e)/sqrt(d)), keeps them in shared memory (float32, 16 heads x
+//     the CTA's windows) and folds them into a running per-head (max, sum of exp2);
+//   * the CTAs exchange their per-head (max, sum) through distributed shared memory, so every
+//     CTA holds each head's softmax normaliser over all windows;
+//   * each CTA forms s[i] = sum_h exp2(z[h][i] - M_h) / L_h for its windows, takes the score of
+//     the window just before its range from the previous CTA (distributed shared memory),
+//     max-pools windows 4j-1 .. 4j+3 onto its blocks and writes them to the workspace;
+//   * after a cluster barrier (release / acquire), CTA 0 runs the exact top-k (topk.cuh).
+// The bytes moved per sequence-group are the compressed keys once, the queries, the block
+// scores and the selection: those of the Forecast selector plus the 16 query heads.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
 
 namespace sparda {
 
-constexpr int kMhTile = 64;
-constexpr int kMhThreads = 128;
+constexpr int kMhTile = 64;                                   // windows per tile
+constexpr int kMhGroupWarps = 4;
+constexpr int kMhConsumerWarps = 2 * kMhGroupWarps;
+constexpr int kMhThreads = (kMhConsumerWarps + 1) * 32;       // + producer warp
+constexpr int kMhStages = 4;                                  // even: one consumer group per stage
+static_assert(kMhStages % 2 == 0, "each ring stage must belong to one consumer group");
+constexpr int kMhMaxCluster = 8;
+constexpr int kMhMaxTilesPerCta = 32;                         // 2048 windows of logits per CTA
 
 int multihead_tiles(int w_cap) { return (w_cap + kMhTile - 1) / kMhTile; }
+
+namespace {
 
 __device__ __forceinline__ uint32_t mh_swz(const uint8_t* tile, int r, int chunk) {
   return smem_addr(tile + (chunk >> 3) * (kBlockBytes / 2) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kMhThreads) multihead_scores_kernel(
-    const MultiheadArgs a, const __grid_constant__ CUtensorMap mck) {
-  __shared__ __align__(1024) uint8_t tile[kBlockBytes];
-  __shared__ uint64_t bar;
-  __shared__ float red_m[4][kHeads], red_l[4][kHeads];
-  const int bg = blockIdx.y, tl = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, cq = lane & 3;
-  const int T = a.seq_len[bg / a.G];
-  const bool valid = T >= 1 && T <= a.max_ctx;
-  const int W = valid ? num_windows(T - 1) : 0;
-  const int i0 = tl * kMhTile;
-  float2* st = a.stats + ((size_t)bg * a.n_tiles + tl) * kHeads;
-  if (i0 >= W) {
-    if (tid < kHeads) st[tid] = make_float2(-INFINITY, 0.f);
-    return;
-  }
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, kBlockBytes);
-    const int row = bg * a.W_cap + i0;
-    tma_load_2d(tile, &mck, 0, row, &bar);
-    tma_load_2d(tile + kBlockBytes / 2, &mck, 64, row, &bar);
-  }
-  uint32_t qf[8][4];
-  {
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)bg * kHeads + g) * kHeadDim);
-    const uint32_t* q1 = q0 + 8 * (kHeadDim / 2);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qf[ks][0] = q0[8 * ks + cq];
-      qf[ks][1] = q1[8 * ks + cq];
-      qf[ks][2] = q0[8 * ks + 4 + cq];
-      qf[ks][3] = q1[8 * ks + 4 + cq];
-    }
-  }
-  __syncthreads();
-  const bool ok = __syncthreads_and(mbar_wait(&bar, 0, a.err));
-  float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  if (ok) {
-    const int r = 16 * warp + (lane & 7) + ((lane >> 4) << 3);
-    const int hi = (lane >> 3) & 1;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(mh_swz(tile, r, 2 * ks + hi), b0, b1, b2, b3);
-      mma_16816(sc[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-      mma_16816(sc[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-    }
-  }
-  const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-  float* z = a.z + (size_t)bg * kHeads * a.W_cap;
-  float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = i0 + 16 * warp + 8 * nt + 2 * cq + (e & 1);
-      const int h = (e < 2) ? g : g + 8;
-      const float v = (i < W && ok) ? sc[nt][e] * sl2 : -INFINITY;
-      sc[nt][e] = v;
-      if (i < W) z[(size_t)h * a.W_cap + i] = v;
-      if (e < 2) m0 = fmaxf(m0, v); else m1 = fmaxf(m1, v);
-    }
-  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-  const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
-  float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    l0 += exp2f(sc[nt][0] - b0) + exp2f(sc[nt][1] - b0);
-    l1 += exp2f(sc[nt][2] - b1) + exp2f(sc[nt][3] - b1);
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (cq == 0) {
-    red_m[warp][g] = m0;
-    red_l[warp][g] = l0;
-    red_m[warp][g + 8] = m1;
-    red_l[warp][g + 8] = l1;
-  }
-  __syncthreads();
-  if (tid < kHeads) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w][tid]);
-    const float base = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) L += exp2f(red_m[w][tid] - base) * red_l[w][tid];
-    st[tid] = make_float2(M, L);
-  }
+__device__ __forceinline__ void mh_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// (m1, l1) + (m2, l2) of the same head: one softmax normaliser over both parts.
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kMhConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster; release / acquire at cluster scope, so that the
+// shared- and global-memory writes before it are visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory word of CTA `rank` of the cluster at the same offset as the local `p`.
+__device__ __forceinline__ float2 ld_cluster_f2(const void* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f(const void* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// (m1, l1) + (m2, l2) of the same head: one softmax normaliser (sum of exp2(x - m)) over both.
 __device__ __forceinline__ float2 lse_combine(float2 x, float2 y) {
   const float M = fmaxf(x.x, y.x);
   if (M == -INFINITY) return make_float2(-INFINITY, 0.f);
   return make_float2(M, x.y * exp2f(x.x - M) + y.y * exp2f(y.x - M));
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1) multihead_pool_topk_kernel(const MultiheadArgs a) {
-  extern __shared__ float s_win[];                 // [W_cap] summed probabilities
-  __shared__ TopkShared sh;
-  __shared__ float s_M[kHeads], s_invL[kHeads];
-  const int bg = blockIdx.x;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int T = a.seq_len[bg / a.G];
-  const bool valid = T >= 1 && T <= a.max_ctx;
-  if (!valid && t == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
-  const int W = valid ? num_windows(T - 1) : 0;
-  const int nb = valid ? (T - 1) / kBlock + 1 : 0;
-  const int n_used = (W + kMhTile - 1) / kMhTile;
-  // each warp owns heads 2w and 2w+1: fold the tile statistics
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = 2 * warp + hh;
-    float2 acc = make_float2(-INFINITY, 0.f);
-    for (int tl = lane; tl < n_used; tl += 32) acc = lse_combine(acc, a.stats[((size_t)bg * a.n_tiles + tl) * kHeads + h]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float2 other;
-      other.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
-      other.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
-      acc = lse_combine(acc, other);
-    }
-    if (lane == 0) {
-      s_M[h] = acc.x;
-      s_invL[h] = acc.y > 0.f ? 1.f / acc.y : 0.f;
-    }
-  }
-  __syncthreads();
-  const float* z = a.z + (size_t)bg * kHeads * a.W_cap;
-  for (int i = t; i < W; i += kTopkThreads) {
-    float s = 0.f;
-#pragma unroll
-    for (int h = 0; h < kHeads; ++h) s += exp2f(z[(size_t)h * a.W_cap + i] - s_M[h]) * s_invL[h];
-    s_win[i] = s;
-  }
-  __syncthreads();
-  float* S = a.block_scores + (size_t)bg * a.nb_cap;
-  for (int j = t; j < nb; j += kTopkThreads) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int d = -1; d <= 3; ++d) {
-      const int w = kWinPerBlock * j + d;
-      if (w >= 0 && w < W) m = fmaxf(m, s_win[w]);
-    }
-    S[j] = m;
-  }
-  __syncthreads();
-  topk_select(S, a.idx + (size_t)bg * (a.topk + 2), a.cnt + bg, a.topk, a.max_ctx, T, sh);
+struct MhLayout {
+  int zstride;                   // floats per head row of logits (tiles x 64 + 8)
+  size_t ring, z, s, stat, red, misc, topk, total;
+};
+
+__host__ __device__ inline MhLayout mh_layout(int tiles_per_cta) {
+  MhLayout L;
+  L.zstride = tiles_per_cta * kMhTile + 8;   // = 8 (mod 32): conflict-free float2 stores
+  L.ring = 1024;
+  L.z = L.ring + (size_t)kMhStages * kBlockBytes;
+  L.s = L.z + (size_t)kHeads * L.zstride * 4;
+  L.stat = L.s + ((size_t)tiles_per_cta * kMhTile + 4) * 4;
+  L.stat = (L.stat + 15) & ~(size_t)15;
+  L.red = L.stat + kHeads * 8;
+  L.misc = L.red + (size_t)kMhConsumerWarps * kHeads * 8;
+  L.topk = L.misc + 256;                          // misc: 1 + 16 + 16 floats
+  L.total = L.topk + sizeof(TopkShared) + 1024;   // + alignment slack of the dynamic base
+  return L;
 }
 
+}  // namespace
+
+__global__ void __launch_bounds__(kMhThreads, 1) multihead_select_kernel(const MultiheadArgs a,
+                                                                        const __grid_constant__ CUtensorMap mck) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const MhLayout Ly = mh_layout(a.tiles_per_cta);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMhStages;
+  uint8_t* ring = smem + Ly.ring;
+  float* z = reinterpret_cast<float*>(smem + Ly.z);                 // [16][zstride]
+  float* s = reinterpret_cast<float*>(smem + Ly.s);                 // [1 + windows]: s[0] halo
+  float2* stat = reinterpret_cast<float2*>(smem + Ly.stat);         // this CTA's (max, sum) per head
+  float2* red = reinterpret_cast<float2*>(smem + Ly.red);           // [8 warps][16 heads]
+  float* misc = reinterpret_cast<float*>(smem + Ly.misc);           // [0]: last window score; [1..16]: M; [17..32]: 1/L
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(smem + Ly.topk);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const int ncl = a.cluster;
+  const int bg = blockIdx.x / ncl;
+  const int T = a.seq_len[bg / a.G];
+  const bool valid = T >= 1 && T <= a.max_ctx;
+  if (!valid && rank == 0 && tid == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+  const int W = valid ? num_windows(T - 1) : 0;
+  const int nb = valid ? (T - 1) / kBlock + 1 : 0;
+  const int n_used = (W + kMhTile - 1) / kMhTile;                   // tiles with a window
+  const int tpr = (n_used + ncl - 1) / ncl;
+  const int tl0 = min((int)rank * tpr, n_used), tl1 = min(tl0 + tpr, n_used);
+  const int n_my = tl1 - tl0;
+  const int w0 = tl0 * kMhTile;                                     // first window of this CTA
+
+  if (tid == 0) {
+    for (int i = 0; i < kMhStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMhGroupWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kMhConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mck);
+      for (int it = 0; it < n_my; ++it) {
+        const int stage = it % kMhStages;
+        if (it >= kMhStages && !mbar_wait(&empty[stage], ((it / kMhStages) & 1) ^ 1, a.err)) break;
+        const int row = bg * a.W_cap + (tl0 + it) * kMhTile;
+        uint8_t* dst = ring + stage * kBlockBytes;
+        mbar_arrive_expect_tx(&full[stage], kBlockBytes);
+        tma_load_2d(dst, &mck, 0, row, &full[stage]);
+        tma_load_2d(dst + kBlockBytes / 2, &mck, 64, row, &full[stage]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int grp = warp / kMhGroupWarps, wq = warp % kMhGroupWarps;
+    const int g = lane >> 2, cq = lane & 3;
+    uint32_t qf[8][4];
+    {
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)bg * kHeads + g) * kHeadDim);
+      const uint32_t* q1 = q0 + 8 * (kHeadDim / 2);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[ks][0] = q0[8 * ks + cq];
+        qf[ks][1] = q1[8 * ks + cq];
+        qf[ks][2] = q0[8 * ks + 4 + cq];
+        qf[ks][3] = q1[8 * ks + 4 + cq];
+      }
+    }
+    const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    float2 st0 = make_float2(-INFINITY, 0.f), st1 = make_float2(-INFINITY, 0.f);   // heads g, g+8
+    bool ok = true;
+    for (int it = 0; it < n_my; ++it) {
+      if ((it & 1) != grp) continue;
+      const int stage = it % kMhStages;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kMhStages) & 1, a.err));
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (ok) {
+        const uint8_t* tile = ring + stage * kBlockBytes;
+        const int r = 16 * wq + (lane & 7) + ((lane >> 4) << 3);
+        const int hi = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(mh_swz(tile, r, 2 * ks + hi), b0, b1, b2, b3);
+          mma_16816(sc[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+          mma_16816(sc[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mh_arrive(&empty[stage]);
+      // logits of windows il .. il+1 (local), heads g and g+8; windows past W are -inf
+      float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int il = it * kMhTile + 16 * wq + 8 * nt + 2 * cq;
+        const int ig = w0 + il;
+        const float v0 = (ok && ig < W) ? sc[nt][0] * sl2 : -INFINITY;
+        const float v1 = (ok && ig + 1 < W) ? sc[nt][1] * sl2 : -INFINITY;
+        const float v2 = (ok && ig < W) ? sc[nt][2] * sl2 : -INFINITY;
+        const float v3 = (ok && ig + 1 < W) ? sc[nt][3] * sl2 : -INFINITY;
+        *reinterpret_cast<float2*>(z + (size_t)g * Ly.zstride + il) = make_float2(v0, v1);
+        *reinterpret_cast<float2*>(z + (size_t)(g + 8) * Ly.zstride + il) = make_float2(v2, v3);
+        sc[nt][0] = v0; sc[nt][1] = v1; sc[nt][2] = v2; sc[nt][3] = v3;
+        m0 = fmaxf(m0, fmaxf(v0, v1));
+        m1 = fmaxf(m1, fmaxf(v2, v3));
+      }
+      const float b0 = m0 == -INFINITY ? 0.f : m0, b1 = m1 == -INFINITY ? 0.f : m1;
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        l0 += exp2f(sc[nt][0] - b0) + exp2f(sc[nt][1] - b0);
+        l1 += exp2f(sc[nt][2] - b1) + exp2f(sc[nt][3] - b1);
+      }
+      st0 = lse_combine(st0, make_float2(m0, l0));
+      st1 = lse_combine(st1, make_float2(m1, l1));
+    }
+    // this CTA's per-head (max, sum): over the 4 lanes of a row, then over the 8 warps
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      st0 = lse_combine(st0, make_float2(__shfl_xor_sync(0xffffffffu, st0.x, o), __shfl_xor_sync(0xffffffffu, st0.y, o)));
+      st1 = lse_combine(st1, make_float2(__shfl_xor_sync(0xffffffffu, st1.x, o), __shfl_xor_sync(0xffffffffu, st1.y, o)));
+    }
+    if (cq == 0) {
+      red[warp * kHeads + g] = st0;
+      red[warp * kHeads + g + 8] = st1;
+    }
+    consumers_sync();
+    if (tid < kHeads) {
+      float2 acc = make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int w = 0; w < kMhConsumerWarps; ++w) acc = lse_combine(acc, red[w * kHeads + tid]);
+      stat[tid] = acc;
+    }
+  }
+  cluster_sync();                                               // #1: every CTA's stat is set
+
+  // every head's normaliser over the whole cluster
+  if (tid < kHeads) {
+    float2 acc = make_float2(-INFINITY, 0.f);
+    for (int r = 0; r < ncl; ++r) acc = lse_combine(acc, ld_cluster_f2(&stat[tid], (uint32_t)r));
+    misc[1 + tid] = acc.x == -INFINITY ? 0.f : acc.x;
+    misc[17 + tid] = acc.y > 0.f ? 1.f / acc.y : 0.f;
+  }
+  __syncthreads();
+  // s[i] = sum_h exp2(z[h][i] - M_h) / L_h over this CTA's windows (-inf past W, for the pool)
+  const int nw = n_my * kMhTile;
+  for (int il = tid; il < nw; il += kMhThreads) {
+    float v = -INFINITY;
+    if (w0 + il < W) {
+      v = 0.f;
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) v += exp2f(z[(size_t)h * Ly.zstride + il] - misc[1 + h]) * misc[17 + h];
+    }
+    s[1 + il] = v;
+  }
+  __syncthreads();
+  if (tid == 0) misc[0] = nw > 0 ? s[nw] : -INFINITY;          // the last window, for the next CTA
+  cluster_sync();                                               // #2: every CTA's last window is set
+
+  // max-pool: this CTA's blocks are those whose first full window (4j) lies in its range; the
+  // CTA with the last used tile also takes the blocks past it (no window: -inf, or the forced
+  // tail). Window 4j-1 of its first block comes from the previous CTA.
+  if (tid == 0) s[0] = (rank > 0 && n_my > 0) ? ld_cluster_f(&misc[0], rank - 1) : -INFINITY;
+  __syncthreads();
+  {
+    const int j0 = w0 / kWinPerBlock;
+    const bool last = (n_my > 0 && tl1 == n_used) || (n_used == 0 && rank == 0);
+    const int j1 = last ? nb : min(nb, (w0 + nw) / kWinPerBlock);
+    float* S = a.block_scores + (size_t)bg * a.nb_cap;
+    for (int j = j0 + tid; j < j1; j += kMhThreads) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int d = -1; d <= 3; ++d) {
+        const int il = kWinPerBlock * j + d - w0;               // local window, -1 = the halo
+        if (il >= -1 && il < nw) m = fmaxf(m, s[1 + il]);
+      }
+      S[j] = m;
+    }
+  }
+  cluster_sync();                                               // #3: every block score is written
+  if (rank == 0 && warp < kMhConsumerWarps)
+    topk_select(a.block_scores + (size_t)bg * a.nb_cap, a.idx + (size_t)bg * (a.topk + 2), a.cnt + bg, a.topk,
+                a.max_ctx, T, sh);
+}
+
+namespace {
+int mh_sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 152;
+  }
+  return n[dev];
+}
+}  // namespace
+
+// Cluster size for a launch: the fewest CTAs whose shared memory holds a (sequence, group)'s
+// logits, raised (in powers of two, up to 8) while the clusters of all groups still fit the
+// GPU in one wave.
+int multihead_cluster_size(int n_tiles_cap, int bg_count) {
+  int nc = 1;
+  while (nc < kMhMaxCluster && (n_tiles_cap + nc - 1) / nc > kMhMaxTilesPerCta) nc *= 2;
+  while (nc < kMhMaxCluster && 2 * nc * bg_count <= mh_sm_count()) nc *= 2;
+  return nc;
+}
+
+size_t multihead_smem_bytes(int tiles_per_cta) { return mh_layout(tiles_per_cta).total; }
+
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s) {
-  dim3 g1(a.n_tiles, bg_count);
-  multihead_scores_kernel<<<g1, kMhThreads, 0, s>>>(a, mck);
-  const int smem = a.W_cap * (int)sizeof(float);
-  cudaFuncSetAttribute(multihead_pool_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  multihead_pool_topk_kernel<<<bg_count, kTopkThreads, smem, s>>>(a);
+  const size_t smem = multihead_smem_bytes(a.tiles_per_cta);
+  cudaFuncSetAttribute(multihead_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.cluster * bg_count);
+  cfg.blockDim = dim3(kMhThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, multihead_select_kernel, a, mck);
 }
 
 }  // namespace sparda

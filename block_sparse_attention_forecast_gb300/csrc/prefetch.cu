@@ -31,6 +31,32 @@ __device__ __forceinline__ uint4 ld_host(const uint4* p) {
   return r;
 }
 
+// Copies one 64-token block of K and V (16 KiB each) from host memory to device memory, by
+// the 128 threads of a copy CTA: kPasses rounds of kInFlight 16-byte loads per tensor and
+// thread, all issued before their stores.
+__device__ __forceinline__ void copy_block(const __nv_bfloat16* hk, const __nv_bfloat16* hv, size_t src,
+                                           __nv_bfloat16* dk_base, __nv_bfloat16* dv_base, size_t dst, int t) {
+  const uint4* sk = reinterpret_cast<const uint4*>(hk + src);
+  const uint4* sv = reinterpret_cast<const uint4*>(hv + src);
+  uint4* dk = reinterpret_cast<uint4*>(dk_base + dst);
+  uint4* dv = reinterpret_cast<uint4*>(dv_base + dst);
+#pragma unroll
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int base = pass * kGatherThreads * kInFlight + t;
+    uint4 rk[kInFlight], rv[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      rk[u] = ld_host(sk + base + u * kGatherThreads);
+      rv[u] = ld_host(sv + base + u * kGatherThreads);
+    }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      dk[base + u * kGatherThreads] = rk[u];
+      dv[base + u * kGatherThreads] = rv[u];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kGatherThreads) prefetch_kernel(const PrefetchArgs a) {
   const int n_items = a.B * a.G * a.kslots;
   const int t = threadIdx.x;
@@ -50,32 +76,150 @@ __global__ void __launch_bounds__(kGatherThreads) prefetch_kernel(const Prefetch
       if (t == 0) atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
       continue;
     }
-    const size_t src = ((size_t)bg * a.max_ctx + (size_t)j * kBlock) * kHeadDim;
-    const size_t dst = ((size_t)bg * a.kslots + s) * kBlock * kHeadDim;
-    const uint4* sk = reinterpret_cast<const uint4*>(a.hk + src);
-    const uint4* sv = reinterpret_cast<const uint4*>(a.hv + src);
-    uint4* dk = reinterpret_cast<uint4*>(a.sk + dst);
-    uint4* dv = reinterpret_cast<uint4*>(a.sv + dst);
-#pragma unroll
-    for (int pass = 0; pass < kPasses; ++pass) {
-      const int base = pass * kGatherThreads * kInFlight + t;
-      uint4 rk[kInFlight], rv[kInFlight];
-#pragma unroll
-      for (int u = 0; u < kInFlight; ++u) {
-        rk[u] = ld_host(sk + base + u * kGatherThreads);
-        rv[u] = ld_host(sv + base + u * kGatherThreads);
-      }
-#pragma unroll
-      for (int u = 0; u < kInFlight; ++u) {
-        dk[base + u * kGatherThreads] = rk[u];
-        dv[base + u * kGatherThreads] = rv[u];
-      }
-    }
+    copy_block(a.hk, a.hv, ((size_t)bg * a.max_ctx + (size_t)j * kBlock) * kHeadDim, a.sk, a.sv,
+               ((size_t)bg * a.kslots + s) * kBlock * kHeadDim, t);
   }
 }
 
 void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s) {
   prefetch_kernel<<<n_ctas, kGatherThreads, 0, s>>>(a);
+}
+
+// ------------------------------------------------------------------ cross-step block cache
+// An extension beyond the pages: each (sequence, group) of an offloaded layer keeps the blocks
+// it gathered at earlier steps in n_cache slots of HBM, and only blocks that are not there
+// yet cross the host link. cache_blocks[bg][c] names the block held in slot c (-1: none).
+//
+// cache_assign_kernel: one warp per (sequence, group). A selected block (not block 0 or the
+// tail block, which the hot ring supplies) already held in a slot keeps it (a hit). Every
+// other selected block (a miss) takes, in order of its position in idx, the lowest slot whose
+// block is not selected at this step; fetch[bg][c] = the block slot c must receive (-1:
+// none), slot[bg][s] = the cache slot of idx entry s (-1 for block 0, the tail block and
+// padding). cache_fetch_kernel then copies the fetched blocks on the copy CTAs.
+constexpr int kCacheMaxSlots = 128;                 // 4 words of 32 lanes
+constexpr int kAssignWarps = 4;
+
+__global__ void __launch_bounds__(kAssignWarps * 32) cache_assign_kernel(const CacheArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int bg = blockIdx.x * kAssignWarps + (threadIdx.x >> 5);
+  if (bg >= a.B * a.G) return;
+  const int T = a.seq_len[bg / a.G];
+  const bool valid = T >= 1 && T <= a.max_ctx;
+  if (!valid && lane == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+  const int tb = valid ? (T - 1) / kBlock : -1;
+  const int n = valid ? min(max(a.cnt[bg], 0), a.kslots) : 0;
+  int32_t* cb = a.cache_blocks + (size_t)bg * a.n_cache;
+  // the blocks held in this lane's slots (c = lane + 32m)
+  int held[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int c = lane + 32 * m;
+    held[m] = c < a.n_cache ? cb[c] : -2;
+  }
+  // the selected blocks that need a slot (idx entries s = lane, lane + 32)
+  int js[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    int j = -1;
+    if (s < n) {
+      j = a.idx[(size_t)bg * a.kslots + s];
+      if (j < 0 || j > tb) {
+        atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
+        j = -1;
+      } else if (j == 0 || j == tb) {
+        j = -1;                                     // the hot ring holds it
+      }
+    }
+    js[h] = j;
+  }
+  // hits: the slot already holding each selected block; keep[m] bit lane: slot selected
+  unsigned keep[4] = {0u, 0u, 0u, 0u};
+  int myslot[2] = {-1, -1};
+  int n_miss_before = 0, my_miss_rank[2] = {-1, -1};
+  for (int s = 0; s < a.kslots; ++s) {               // warp-uniform loop over idx entries
+    const int j = __shfl_sync(0xffffffffu, js[s >> 5], s & 31);
+    if (j < 0) continue;
+    int slot = -1;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const unsigned b = __ballot_sync(0xffffffffu, held[m] == j);
+      if (b && slot < 0) {
+        slot = 32 * m + __ffs(b) - 1;
+        keep[m] |= 1u << (__ffs(b) - 1);
+      }
+    }
+    if ((s & 31) == lane) {
+      if (slot >= 0) myslot[s >> 5] = slot;
+      else my_miss_rank[s >> 5] = n_miss_before;
+    }
+    if (slot < 0) ++n_miss_before;
+  }
+  // the r-th miss takes the r-th slot not kept (slots past n_cache are never free)
+  unsigned freem[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int lim = a.n_cache - 32 * m;
+    const unsigned in = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : ((1u << lim) - 1u));
+    freem[m] = in & ~keep[m];
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (my_miss_rank[h] >= 0) {
+      int r = my_miss_rank[h], slot = -1;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int pc = __popc(freem[m]);
+        if (slot < 0 && r < pc) {
+          unsigned x = freem[m];
+          for (int q = 0; q < r; ++q) x &= x - 1;  // drop the r lowest free slots
+          slot = 32 * m + __ffs(x) - 1;
+        } else if (slot < 0) {
+          r -= pc;
+        }
+      }
+      myslot[h] = slot;                             // n_cache >= topk: a free slot exists
+    }
+  }
+  __syncwarp();
+  // outputs: fetch list cleared, then the misses' slots; the slot of every idx entry
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int c = lane + 32 * m;
+    if (c < a.n_cache) a.fetch[(size_t)bg * a.n_cache + c] = -1;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = lane + 32 * h;
+    if (s < a.kslots) a.slot[(size_t)bg * a.kslots + s] = js[h] >= 0 ? myslot[h] : -1;
+    if (js[h] >= 0 && my_miss_rank[h] >= 0 && myslot[h] >= 0) {
+      a.fetch[(size_t)bg * a.n_cache + myslot[h]] = js[h];
+      cb[myslot[h]] = js[h];
+    }
+  }
+  if (a.stats && lane == 0) {
+    atomicAdd(a.stats, (unsigned long long)(__popc(keep[0]) + __popc(keep[1]) + __popc(keep[2]) + __popc(keep[3])));
+    atomicAdd(a.stats + 1, (unsigned long long)n_miss_before);
+  }
+}
+
+__global__ void __launch_bounds__(kGatherThreads) cache_fetch_kernel(const CacheArgs a) {
+  const int n_items = a.B * a.G * a.n_cache;
+  const int t = threadIdx.x;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int j = a.fetch[item];
+    if (j < 0) continue;
+    const int bg = item / a.n_cache;
+    copy_block(a.hk, a.hv, ((size_t)bg * a.max_ctx + (size_t)j * kBlock) * kHeadDim, a.ck_cache, a.cv_cache,
+               (size_t)item * kBlock * kHeadDim, t);
+  }
+}
+
+void launch_cache_gather(const CacheArgs& a, int n_ctas, cudaStream_t s) {
+  const int bgc = a.B * a.G;
+  cache_assign_kernel<<<(bgc + kAssignWarps - 1) / kAssignWarps, kAssignWarps * 32, 0, s>>>(a);
+  cache_fetch_kernel<<<n_ctas, kGatherThreads, 0, s>>>(a);
 }
 
 }  // namespace sparda

@@ -17,7 +17,9 @@ and selects its own blocks with a same-layer forecast), three ways to launch the
       (join before layer L+1)
     Offloaded layers add a third stream that gathers layer L+1's selected blocks from pinned
     host memory as soon as they are known, into one of two staging buffers; layer L+1's
-    attention waits for that gather.
+    attention waits for that gather. With block_cache, each offloaded layer instead keeps its
+    gathered blocks in an HBM cache of its own across steps, and the gather copies only the
+    selected blocks the cache lacks (an extension beyond the pages).
 
 Every mode computes the same results bit for bit. Everything here is host-side orchestration
 of libsparda calls (no arithmetic); the whole step can be captured once into a CUDA graph and
@@ -44,7 +46,7 @@ class DecodeStack:
     MODES = ("pipelined", "fused", "streams")
 
     def __init__(self, shape, layers, W_self0, W_next, batch, device="cuda", gather_ctas=0,
-                 overlap=True, advance=False, after_attention=None, mode="pipelined"):
+                 overlap=True, advance=False, after_attention=None, mode="pipelined", block_cache=None):
         self.shape = shape
         self.layers = layers
         self.n_layers = len(layers)
@@ -90,7 +92,15 @@ class DecodeStack:
         self.ws_sel = sb.workspace(shape, B, sb.WS_SELECT, device)
         self.ws_attn = sb.workspace(shape, B, sb.WS_ATTN, device)
         self.ws_sel2 = sb.workspace(shape, B, sb.WS_SELECT, device) if self.mode != "streams" else None
-        if self.any_offload:
+        # block_cache = n_cache slots per (sequence, group): every offloaded layer keeps the
+        # blocks it gathered in HBM across steps and gathers only the ones it lacks (an
+        # extension beyond the pages); None: two staging buffers shared by all layers
+        self.caches = None
+        self.cache_stats = None
+        if self.any_offload and block_cache:
+            self.caches = {L: sb.BlockCache(shape, block_cache, device) for L, l in enumerate(layers) if l.on_host}
+            self.cache_stats = torch.zeros(2, dtype=torch.int64, device=device)   # hits, misses
+        elif self.any_offload:
             st = (shape.max_batch, G, shape.kslots, shape.block, d)
             self.stage_k = [torch.zeros(st, **bf) for _ in range(2)]
             self.stage_v = [torch.zeros(st, **bf) for _ in range(2)]
@@ -272,7 +282,17 @@ class DecodeStack:
                                           self.cnt[L + 1], self.ws_sel, stream=side)
                 sel_done = ev()
                 sel_done.record(side)
-                if nxt.on_host:
+                if nxt.on_host and self.caches is not None:
+                    # the layer's own cache: last read by its attention of the previous step
+                    self.gather.wait_event(sel_done)
+                    sb.sparda_prefetch_blocks_cached(sh, nxt, self.idx[L + 1], self.cnt[L + 1], self.seq_len, B,
+                                                     self.caches[L + 1], self.cache_stats, self.gather_ctas,
+                                                     stream=self.gather)
+                    gather_done[L + 1] = ev()
+                    gather_done[L + 1].record(self.gather)
+                    if not self.overlap:
+                        main.wait_event(gather_done[L + 1])
+                elif nxt.on_host:
                     slot = (L + 1) % 2
                     self.gather.wait_event(sel_done)
                     if L - 1 >= 0 and attn_done[L - 1] is not None:
@@ -285,7 +305,11 @@ class DecodeStack:
                     if not self.overlap:
                         main.wait_event(gather_done[L + 1])
             sb.sparda_append_kv(sh, layer, self.k_new[L], self.v_new[L], self.seq_len, B, stream=main)
-            if layer.on_host:
+            if layer.on_host and self.caches is not None:
+                main.wait_event(gather_done[L])
+                sb.sparda_sparse_decode_attn_cached(sh, layer, self.caches[L], self.q[L], self.idx[L], self.cnt[L],
+                                                    self.seq_len, B, self.out[L], self.ws_attn, stream=main)
+            elif layer.on_host:
                 main.wait_event(gather_done[L])
                 slot = L % 2
                 sb.sparda_sparse_decode_attn(sh, layer, self.q[L], self.idx[L], self.cnt[L], self.seq_len, B,
@@ -405,5 +429,5 @@ class DecodeStack:
             return 2 + n + (n - 1) + 1
         if self.mode == "fused":
             return 2 + n + 2 * (n - 1) + 1
-        gathers = sum(1 for l in self.layers[1:] if l.on_host)
+        gathers = sum(1 for l in self.layers[1:] if l.on_host) * (2 if self.caches is not None else 1)
         return 2 + n * 2 + (n - 1) * 2 + gathers

@@ -426,6 +426,68 @@ int32_t sparda_forecast_select_static(const sparda_shape* shape, const void* ck,
                                       const void* forecast, const int32_t* seq_len,
                                       int32_t batch, int32_t* idx, int32_t* cnt, void* stream);
 
+/*
+ * sparda_prefetch_blocks_copy_engine -- the gather of sparda_prefetch_blocks done by the
+ * copy engines instead of copy CTAs, for comparison: one cudaMemcpyAsync on `stream` per run
+ * of consecutive selected blocks (K and V separately), into the same staging layout. The
+ * selection must be on the HOST (idx_host int32 [B, G, topk+2], cnt_host int32 [B, G],
+ * seq_len_host int32 [B]): the caller reads it back from the device and waits for it first,
+ * which is the host-side indexing step the pages contrast SparDA with (techwalker section 五,
+ * the InfiniGen paragraph); the GPU-side gather needs no such round trip. *n_copies (optional)
+ * receives the number of copies issued. Host-synchronous argument checks; the copies are
+ * asynchronous. Errors: as sparda_prefetch_blocks, plus SPARDA_ERR_INVALID_ARG for a host
+ * seq_len or block index out of range (checked before each copy is issued) and
+ * SPARDA_ERR_CUDA if a copy cannot be enqueued.
+ */
+int32_t sparda_prefetch_blocks_copy_engine(const sparda_shape* shape, const sparda_layer_kv* host_layer,
+                                           const int32_t* idx_host, const int32_t* cnt_host,
+                                           const int32_t* seq_len_host, int32_t batch, void* staging_k,
+                                           void* staging_v, int32_t* n_copies, void* stream);
+
+/* ---------------------------------------------------------------- cross-step block cache */
+/*
+ * An extension beyond the pages, for offloaded layers: consecutive decode steps often select
+ * many of the same blocks, so each (b, g) of an offloaded layer keeps the blocks it gathered
+ * in n_cache slots of HBM (topk + 2 <= n_cache <= 128), and only the selected blocks not held
+ * there yet are read over the host link. The caller owns, per offloaded layer:
+ *   cache_k, cache_v  device bf16 [max_batch, G, n_cache, 64, d] (the cached blocks);
+ *   cache_blocks      device int32 [max_batch, G, n_cache]: the block each slot holds, -1 for
+ *                     none. Fill with -1 before the first call (or after the layer's cache
+ *                     content stops being valid, e.g. a new prompt in that sequence slot);
+ *   slot              device int32 [B, G, topk+2]: written by the gather, read by the attention;
+ *   fetch             device int32 [max_batch, G, n_cache]: scratch of the gather.
+ */
+
+/*
+ * sparda_prefetch_blocks_cached -- sparda_prefetch_blocks with the block cache. For every
+ * (b, g), a selected block (other than block 0 and the tail block, which the hot buffers
+ * hold) already held in a slot keeps it; each other selected block, in idx order, takes the
+ * lowest slot whose block is not selected now, and is copied there from the host cache by the
+ * copy CTAs. slot[b, g, s] receives the cache slot of idx entry s (-1 for block 0, the tail
+ * block and padding). stats (optional, NULL for none; device uint64 [2], 8-byte aligned)
+ * accumulates the hits and the misses (blocks copied). n_ctas as sparda_prefetch_blocks.
+ * Errors: as sparda_prefetch_blocks; SPARDA_ERR_UNSUPPORTED_SHAPE for n_cache out of range.
+ */
+int32_t sparda_prefetch_blocks_cached(const sparda_shape* shape, const sparda_layer_kv* host_layer,
+                                      const int32_t* idx, const int32_t* cnt, const int32_t* seq_len,
+                                      int32_t batch, void* cache_k, void* cache_v, int32_t* cache_blocks,
+                                      int32_t n_cache, int32_t* slot, int32_t* fetch, unsigned long long* stats,
+                                      int32_t n_ctas, void* stream);
+
+/*
+ * sparda_sparse_decode_attn_cached -- sparda_sparse_decode_attn of an offloaded layer whose
+ * selected blocks sit in the block cache: the block of idx entry s is read from slot
+ * slot[b, g, s] of cache_k / cache_v (as sparda_prefetch_blocks_cached left them), block 0
+ * and the tail block from the hot buffers. Results are those of sparda_sparse_decode_attn on
+ * the same blocks, bit for bit. A slot outside 0 .. n_cache-1 sets SPARDA_DEV_BAD_INDEX and
+ * reads slot 0.
+ */
+int32_t sparda_sparse_decode_attn_cached(const sparda_shape* shape, const sparda_layer_kv* layer,
+                                         const void* cache_k, const void* cache_v, int32_t n_cache,
+                                         const int32_t* slot, const void* q, const int32_t* idx,
+                                         const int32_t* cnt, const int32_t* seq_len, int32_t batch, void* out,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- chunked prefill */
 /*
  * Prefill processes a whole prompt. The pages give its figures (bittide thread and abstract:

@@ -22,7 +22,7 @@ def sb(cuda_ok):
 
 
 def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, offload=(), overlap=True,
-                    mode="pipelined"):
+                    mode="pipelined", block_cache=None):
     """Seeded caches holding tokens 0..T-2, the step's inputs, and forecast heads; planted
     blocks of each layer are shifted along the forecast (computed by the oracle) that selects
     that layer's blocks."""
@@ -59,7 +59,7 @@ def make_stack_case(sb, seed, n_layers, B, T, topk, max_ctx, hidden, n_planted, 
         Vs.append(V)
         layers.append(layer)
     stack = DecodeStack(shape, layers, W_self0.cuda(), [w.cuda() for w in W_next], B, overlap=overlap,
-                        mode=mode)
+                        mode=mode, block_cache=block_cache)
     stack.h.copy_(h.cuda())
     stack.q.copy_(q.cuda())
     stack.k_new.copy_(kn.cuda())
