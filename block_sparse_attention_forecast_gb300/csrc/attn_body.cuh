@@ -69,12 +69,14 @@ struct GroupInfo {
   int T, tb, n_sel;
 };
 
+// Both loads are issued before either is looked at (one memory round trip, not two).
 __device__ __forceinline__ GroupInfo group_info(const AttnArgs& a, int bg) {
   GroupInfo gi;
   gi.T = a.seq_len[bg / a.G];
+  const int cnt = a.cnt[bg];
   const bool valid = gi.T >= 1 && gi.T <= a.max_ctx;
   gi.tb = valid ? (gi.T - 1) / kBlock : 0;
-  gi.n_sel = valid ? min(max(a.cnt[bg], 0), a.kslots) : 0;
+  gi.n_sel = valid ? min(max(cnt, 0), a.kslots) : 0;
   return gi;
 }
 
@@ -131,10 +133,11 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
       int j = 0, row = 0, hot = 0;
       if (u < u1) {
         const int bg = u / a.kslots;
+        const int j_raw = a.idx[u];              // in bounds for every unit: loaded with the two below
         const GroupInfo gi = group_info(a, bg);
         if (u - bg * a.kslots < gi.n_sel) {
           v = true;
-          j = a.idx[u];
+          j = j_raw;
           if (j < 0 || j > gi.tb) {
             atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
             j = 0;
