@@ -109,13 +109,13 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-// A [rows, 128] bf16 matrix read in boxes of 64 rows x 64 columns, 128-byte swizzle.
-int32_t make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
+// A [rows, 128] bf16 matrix read in boxes of box_rows rows x 64 columns, 128-byte swizzle.
+int32_t make_kv_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows = 64) {
   EncodeTiledFn enc = encoder();
   if (!enc) return SPARDA_ERR_CUDA;
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
-  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -587,13 +587,16 @@ int32_t sparda_prefill_attn(const sparda_shape* s, const sparda_layer_kv* L, con
   int* err = dev_error_ptr();
   if (!err) return SPARDA_ERR_CUDA;
   const uint64_t rows = (uint64_t)s->max_batch * s->n_groups * s->max_ctx;
-  CUtensorMap mk, mv;
+  // every query row must fit a signed 32-bit TMA coordinate
+  if (rows * kHeads >= ((uint64_t)1 << 31)) return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap mk, mv, mq;
   SPARDA_TRY(make_kv_map(&mk, L->k, rows));
   SPARDA_TRY(make_kv_map(&mv, L->v, rows));
+  SPARDA_TRY(make_kv_map(&mq, q, rows * kHeads, 16));
   PrefillArgs a{nullptr, nullptr, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), seq_len,
                 const_cast<int32_t*>(idx), const_cast<int32_t*>(cnt), nullptr, err, s->n_groups, w_cap(s),
                 s->max_ctx, nb_cap(s), s->topk};
-  launch_prefill_attn(a, mk, mv, batch, static_cast<cudaStream_t>(stream));
+  launch_prefill_attn_tc(a, mq, mk, mv, batch, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

@@ -30,6 +30,7 @@
 //       the chunk's own block.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc05.cuh"
 #include "topk.cuh"
 
 namespace sparda {
@@ -585,6 +586,289 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
   }
 }
 
+// ==================================================================== block-sparse attention, tcgen05
+// The same work as prefill_attn_kernel on the fifth-generation tensor cores: a CTA holds the
+// 128 query rows of 8 tokens x 16 heads (row 16i + h) as one M = 128 tile.
+//   warp 0, one thread: TMA loads of the Q tile (once) and of the chunk's K/V blocks into a
+//       ring of full / empty mbarriers;
+//   warp 1: allocates 256 tensor-memory columns (S double buffer: columns 0-63 and 64-127;
+//       O: 128-255) and, from one thread, issues S_j = Q K_j^T (M 128, N 64, 8 K steps) and
+//       O += P_j V_j (M 128, N 128, 4 K steps; V read M/N-major), each completion signalled
+//       by tcgen05.commit on an mbarrier; S_{j+1} is issued before O += P_j V_j, so the
+//       tensor cores compute the next scores while the softmax runs;
+//   warps 2-5, one thread per row (tensor-memory lane): load S_j, mask the keys after the
+//       token (the chunk's own block), an online softmax in the exp2 domain whose running
+//       maximum is only moved (and O rescaled in tensor memory) when it grows by more than
+//       2^8, P_j written to shared memory as bf16 in the 128-byte-swizzled K-major layout;
+//       at the end O / l to the output.
+namespace {
+constexpr int kTcStages = 3;
+constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB: 128 rows x 128 dims bf16
+constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB: 128 rows x 64 keys bf16
+constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcQBytes + kTcStages * kPaSlotBytes + 2 * kTcPBytes;
+constexpr int kTcThreads = 6 * 32;
+constexpr uint32_t kTcCols = 256;
+constexpr float kRescaleLog2 = 8.f;                         // move the running max past 2^8 growth
+
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait(bar, parity, err);
+}
+}  // namespace
+
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const PrefillArgs a,
+                                                                       const __grid_constant__ CUtensorMap mq,
+                                                                       const __grid_constant__ CUtensorMap mk,
+                                                                       const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* kv_full = q_full + 1;
+  uint64_t* kv_empty = kv_full + kTcStages;
+  uint64_t* s_full = kv_empty + kTcStages;                  // [2]
+  uint64_t* s_free = s_full + 2;                            // [2]
+  uint64_t* p_full = s_free + 2;                            // [2]
+  uint64_t* p_free = p_full + 2;                            // [2]
+  uint64_t* o_done = p_free + 2;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(o_done + 1);
+  uint8_t* qs = smem + 1024;
+  uint8_t* ring = qs + kTcQBytes;
+  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
+  const int c = blockIdx.x / kSlices, sl = blockIdx.x % kSlices;
+  const int T = a.seq_len[b];
+  if (!valid_len(T, a.max_ctx)) {
+    if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int tok0 = c * kBlock + sl * 8;
+  if (tok0 >= T) return;                                     // CTA-uniform
+  const int kslots = a.topk + 2;
+  const size_t row = (size_t)bg * a.nb_cap + c;
+  const int n_sel = min(max(a.cnt[row], 0), kslots);
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_free[i], 1);
+    }
+    mbar_init(o_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc05::alloc(tmem_base_sh, kTcCols);
+    tc05::relinquish();
+  }
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+  const uint32_t t_s[2] = {tmem, tmem + 64};
+  const uint32_t t_o = tmem + 128;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      mbar_arrive_expect_tx(q_full, kTcQBytes);
+      const int qrow0 = (((b * a.max_ctx) + tok0) * a.G + g) * kHeads;
+      const int tok_stride = a.G * kHeads;
+      for (int i = 0; i < 8; ++i) {
+        const int qr = qrow0 + i * tok_stride;
+        tma_load_2d(qs + i * 16 * 128, &mq, 0, qr, q_full);
+        tma_load_2d(qs + kTcQBytes / 2 + i * 16 * 128, &mq, 64, qr, q_full);
+      }
+      for (int s = 0; s < n_sel && ok; ++s) {
+        int j = a.idx[row * kslots + s];
+        if (j < 0 || j > c) {
+          atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
+          j = 0;
+        }
+        const int stage = s % kTcStages;
+        if (s >= kTcStages) ok = tc_wait(&kv_empty[stage], ((s / kTcStages) & 1) ^ 1, a.err);
+        if (!ok) break;
+        uint8_t* dst = ring + stage * kPaSlotBytes;
+        const int rr = bg * a.max_ctx + j * kBlock;
+        mbar_arrive_expect_tx(&kv_full[stage], kPaSlotBytes);
+        tma_load_2d(dst, &mk, 0, rr, &kv_full[stage]);
+        tma_load_2d(dst + kBlockBytes / 2, &mk, 64, rr, &kv_full[stage]);
+        tma_load_2d(dst + kBlockBytes, &mv, 0, rr, &kv_full[stage]);
+        tma_load_2d(dst + kBlockBytes + kBlockBytes / 2, &mv, 64, rr, &kv_full[stage]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
+      const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring), p_addr = smem_addr(pbuf);
+      ok = tc_wait(q_full, 0, a.err);
+      auto issue_pv = [&](int jp) {
+        // O += P_jp V_jp once the softmax has written P_jp
+        if (ok) ok = tc_wait(&p_full[jp & 1], (jp >> 1) & 1, a.err);
+        if (!ok) return;
+        tc05::fence_after();
+        const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
+        const uint32_t pb = p_addr + (jp & 1) * kTcPBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
+          const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
+          tc05::mma_bf16_ss(t_o, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc05::commit(o_done);
+        tc05::commit(&kv_empty[jp % kTcStages]);
+        tc05::commit(&p_free[jp & 1]);
+      };
+      for (int j = 0; j < n_sel && ok; ++j) {
+        const int stage = j % kTcStages;
+        ok = tc_wait(&kv_full[stage], (j / kTcStages) & 1, a.err);
+        if (ok && j >= 2) ok = tc_wait(&s_free[j & 1], ((j - 2) >> 1) & 1, a.err);
+        if (!ok) break;
+        tc05::fence_after();
+        const uint32_t kb = ring_addr + stage * kPaSlotBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
+          const uint64_t da = tc05::smem_desc(q_addr + half * (kTcQBytes / 2) + off, 16, 1024);
+          const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
+          tc05::mma_bf16_ss(t_s[j & 1], da, db, id_qk, kk > 0 ? 1u : 0u);
+        }
+        tc05::commit(&s_full[j & 1]);
+        if (j >= 1) issue_pv(j - 1);
+      }
+      if (ok && n_sel > 0) issue_pv(n_sel - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax, one row per thread
+    const int quarter = warp & 3;                            // tensor-memory lanes 32q .. 32q+31
+    const int r = quarter * 32 + lane;                       // query row: token r/16, head r%16
+    const int tok = tok0 + (r >> 4);
+    const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_sel; ++j) {
+      if (ok) ok = __all_sync(0xffffffffu, tc_wait(&s_full[j & 1], (j >> 1) & 1, a.err));
+      float sv[64];
+      if (ok) {
+        tc05::fence_after();
+        float x0[32], x1[32];
+        tc05::ld32(t_s[j & 1] + lane_off, x0);
+        tc05::ld32(t_s[j & 1] + lane_off + 32, x1);
+        tc05::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = x0[e];
+          sv[32 + e] = x1[e];
+        }
+      }
+      tc05::fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&s_free[j & 1]);
+      if (!ok) {
+        if (lane == 0) bar_arrive(&p_full[j & 1]);
+        continue;
+      }
+      int jb = a.idx[row * kslots + j];                      // the block of S_j (as the producer read it)
+      if (jb < 0 || jb > c) jb = 0;
+      const int kbase = jb * kBlock;
+      float mb = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        sv[e] = (kbase + e <= tok) ? sv[e] * sl2 : -INFINITY;
+        mb = fmaxf(mb, sv[e]);
+      }
+      // move the running max only when it grows by more than 2^8 (or on the first block)
+      const bool first = (m_used == -INFINITY);
+      const bool grow = !first && mb > m_used + kRescaleLog2;
+      if (__any_sync(0xffffffffu, grow)) {
+        // O in tensor memory holds P_0..P_{j-1} V: rescale it once O += P_{j-1} V_{j-1} is done
+        const float mn = fmaxf(m_used, mb);
+        const float alpha = exp2f(m_used - mn);
+        ok = __all_sync(0xffffffffu, tc_wait(o_done, (j - 1) & 1, a.err));
+        if (ok) {
+          tc05::fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float o[32];
+            tc05::ld32(t_o + lane_off + 32 * q4, o);
+            tc05::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tc05::st32(t_o + lane_off + 32 * q4, o);
+          }
+          tc05::wait_st();
+        }
+        l *= alpha;
+        m_used = mn;
+      } else if (first) {
+        m_used = mb;
+      }
+      float ps = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = exp2f(sv[2 * e] - m_used), p1 = exp2f(sv[2 * e + 1] - m_used);
+        ps += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+      l += ps;
+      // P_j into its buffer once O += P_{j-2} V_{j-2} has read it
+      if (j >= 2) ok = __all_sync(0xffffffffu, tc_wait(&p_free[j & 1], ((j - 2) >> 1) & 1, a.err));
+      if (ok) {
+        uint8_t* prow = pbuf + (j & 1) * kTcPBytes + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_shared();
+      tc05::fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&p_full[j & 1]);
+    }
+    // ---- epilogue: O / l of this row (token tok, head r % 16)
+    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, tc_wait(o_done, (n_sel - 1) & 1, a.err));
+    if (ok && n_sel > 0) {
+      tc05::fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(a.out + ((((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads + (r & 15)) * kHeadDim);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float o[32];
+        tc05::ld32(t_o + lane_off + 32 * q4, o);
+        tc05::wait_ld();
+        if (tok < T) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[4 * q4 + e] = make_uint4(pack_bf16(o[8 * e] * inv, o[8 * e + 1] * inv),
+                                         pack_bf16(o[8 * e + 2] * inv, o[8 * e + 3] * inv),
+                                         pack_bf16(o[8 * e + 4] * inv, o[8 * e + 5] * inv),
+                                         pack_bf16(o[8 * e + 6] * inv, o[8 * e + 7] * inv));
+        }
+      }
+    }
+  }
+  // every tensor-memory access of this CTA is done before the allocating warp frees it
+  tc05::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc05::fence_after();
+    tc05::dealloc(tmem, kTcCols);
+  }
+}
+
 // ==================================================================== launches
 void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s) {
   const int n_ct = (a.nb_cap + kPfChunks - 1) / kPfChunks;
@@ -602,6 +886,12 @@ void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUte
                          cudaStream_t s) {
   cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPaSmem);
   prefill_attn_kernel<<<dim3(a.nb_cap * kSlices, batch * a.G), kPaThreads, kPaSmem, s>>>(a, mk, mv);
+}
+
+void launch_prefill_attn_tc(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, int batch, cudaStream_t s) {
+  cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  prefill_attn_tc_kernel<<<dim3(a.nb_cap * kSlices, batch * a.G), kTcThreads, kTcSmem, s>>>(a, mq, mk, mv);
 }
 
 }  // namespace sparda
