@@ -587,32 +587,35 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 }
 
 // ==================================================================== block-sparse attention, tcgen05
-// The same work as prefill_attn_kernel on the fifth-generation tensor cores: a CTA holds the
-// 128 query rows of 8 tokens x 16 heads (row 16i + h) as one M = 128 tile.
-//   warp 0, one thread: TMA loads of the Q tile (once) and of the chunk's K/V blocks into a
-//       ring of full / empty mbarriers;
-//   warp 1: allocates 256 tensor-memory columns (S double buffer: columns 0-63 and 64-127;
-//       O: 128-255) and, from one thread, issues S_j = Q K_j^T (M 128, N 64, 8 K steps) and
-//       O += P_j V_j (M 128, N 128, 4 K steps; V read M/N-major), each completion signalled
-//       by tcgen05.commit on an mbarrier; S_{j+1} is issued before O += P_j V_j, so the
-//       tensor cores compute the next scores while the softmax runs;
-//   warps 2-5, one thread per row (tensor-memory lane): load S_j, mask the keys after the
-//       token (the chunk's own block), an online softmax in the exp2 domain whose running
-//       maximum is only moved (and O rescaled in tensor memory) when it grows by more than
-//       2^8, P_j written to shared memory as bf16 in the 128-byte-swizzled K-major layout;
-//       at the end O / l to the output.
+// The same work as prefill_attn_kernel on the fifth-generation tensor cores. A CTA holds two
+// query tiles of 128 rows (8 tokens x 16 heads each, row 16i + h), 16 tokens of one chunk,
+// which share every K/V block it loads:
+//   warp 0, one thread: TMA loads of the two Q tiles (once) and of the chunk's K/V blocks into
+//       a ring of full / empty mbarriers;
+//   warp 1: allocates the 512 tensor-memory columns (per tile an S double buffer of 2 x 64
+//       columns and an O of 128 columns) and, from one thread, issues per block j and tile t
+//       S_t,j = Q_t K_j^T (M 128, N 64, 8 K steps of 16) and O_t += P_t,j V_j (M 128, N 128,
+//       4 K steps; V read M/N-major), each completion signalled by tcgen05.commit on an
+//       mbarrier; both tiles' S_j+1 are issued before their O += P_j V_j, so the tensor cores
+//       work on one tile while the other tile's softmax runs;
+//   warps 2-5 (tile 0) and 6-9 (tile 1), one thread per row (tensor-memory lane): load S_t,j,
+//       mask the keys after the token (the chunk's own block), an online softmax in the exp2
+//       domain whose running maximum is only moved (and O rescaled in tensor memory) when it
+//       grows by more than 2^8, P_t,j written to shared memory as bf16 in the 128-byte-swizzled
+//       K-major layout; at the end O / l to the output.
 namespace {
+constexpr int kTcTiles = 2;
+constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
+constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
 constexpr int kTcStages = 3;
-constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB: 128 rows x 128 dims bf16
-constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB: 128 rows x 64 keys bf16
-constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcQBytes + kTcStages * kPaSlotBytes + 2 * kTcPBytes;
-constexpr int kTcThreads = 6 * 32;
-constexpr uint32_t kTcCols = 256;
+constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB per tile: 128 rows x 128 dims
+constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB per tile and buffer: 128 x 64 keys
+constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcTiles * kTcQBytes + kTcStages * kPaSlotBytes +
+                        kTcTiles * 2 * kTcPBytes;
+static_assert(kTcSmem <= 227 * 1024, "the tcgen05 prefill attention fits shared memory");
+constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
+constexpr uint32_t kTcCols = 512;
 constexpr float kRescaleLog2 = 8.f;                         // move the running max past 2^8 growth
-
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* err) {
-  return mbar_wait(bar, parity, err);
-}
 }  // namespace
 
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const PrefillArgs a,
@@ -622,27 +625,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* q_full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* kv_full = q_full + 1;
-  uint64_t* kv_empty = kv_full + kTcStages;
-  uint64_t* s_full = kv_empty + kTcStages;                  // [2]
-  uint64_t* s_free = s_full + 2;                            // [2]
-  uint64_t* p_full = s_free + 2;                            // [2]
-  uint64_t* p_free = p_full + 2;                            // [2]
-  uint64_t* o_done = p_free + 2;
-  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(o_done + 1);
-  uint8_t* qs = smem + 1024;
-  uint8_t* ring = qs + kTcQBytes;
-  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;
+  uint64_t* kv_full = q_full + 1;                           // [stages]
+  uint64_t* kv_empty = kv_full + kTcStages;                 // [stages]
+  uint64_t* s_full = kv_empty + kTcStages;                  // [tile][2]
+  uint64_t* s_free = s_full + 2 * kTcTiles;                 // [tile][2]
+  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile][2]
+  uint64_t* p_free = p_full + 2 * kTcTiles;                 // [tile][2]
+  uint64_t* o_done = p_free + 2 * kTcTiles;                 // [tile]
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(o_done + kTcTiles);
+  uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
+  uint8_t* ring = qs + kTcTiles * kTcQBytes;
+  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile][2] 16 KiB
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
-  const int c = blockIdx.x / kSlices, sl = blockIdx.x % kSlices;
+  const int c = blockIdx.x / kTcSlices, sl = blockIdx.x % kTcSlices;
   const int T = a.seq_len[b];
   if (!valid_len(T, a.max_ctx)) {
     if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
     return;
   }
-  const int tok0 = c * kBlock + sl * 8;
+  const int tok0 = c * kBlock + sl * kTcTokens;
   if (tok0 >= T) return;                                     // CTA-uniform
   const int kslots = a.topk + 2;
   const size_t row = (size_t)bg * a.nb_cap + c;
@@ -654,13 +657,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2 * kTcTiles; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&p_free[i], 1);
     }
-    mbar_init(o_done, 1);
+    for (int t = 0; t < kTcTiles; ++t) mbar_init(&o_done[t], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -671,8 +674,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   __syncthreads();
   tc05::fence_after();
   const uint32_t tmem = *tmem_base_sh;
-  const uint32_t t_s[2] = {tmem, tmem + 64};
-  const uint32_t t_o = tmem + 128;
   bool ok = true;
 
   if (warp == 0) {
@@ -681,13 +682,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
-      mbar_arrive_expect_tx(q_full, kTcQBytes);
+      mbar_arrive_expect_tx(q_full, kTcTiles * kTcQBytes);
       const int qrow0 = (((b * a.max_ctx) + tok0) * a.G + g) * kHeads;
       const int tok_stride = a.G * kHeads;
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kTcTokens; ++i) {
         const int qr = qrow0 + i * tok_stride;
-        tma_load_2d(qs + i * 16 * 128, &mq, 0, qr, q_full);
-        tma_load_2d(qs + kTcQBytes / 2 + i * 16 * 128, &mq, 64, qr, q_full);
+        uint8_t* qt = qs + (i >> 3) * kTcQBytes + (i & 7) * 16 * 128;
+        tma_load_2d(qt, &mq, 0, qr, q_full);
+        tma_load_2d(qt + kTcQBytes / 2, &mq, 64, qr, q_full);
       }
       for (int s = 0; s < n_sel && ok; ++s) {
         int j = a.idx[row * kslots + s];
@@ -696,7 +698,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
           j = 0;
         }
         const int stage = s % kTcStages;
-        if (s >= kTcStages) ok = tc_wait(&kv_empty[stage], ((s / kTcStages) & 1) ^ 1, a.err);
+        if (s >= kTcStages) ok = mbar_wait(&kv_empty[stage], ((s / kTcStages) & 1) ^ 1, a.err);
         if (!ok) break;
         uint8_t* dst = ring + stage * kPaSlotBytes;
         const int rr = bg * a.max_ctx + j * kBlock;
@@ -713,59 +715,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
       const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring), p_addr = smem_addr(pbuf);
-      ok = tc_wait(q_full, 0, a.err);
+      ok = mbar_wait(q_full, 0, a.err);
       auto issue_pv = [&](int jp) {
-        // O += P_jp V_jp once the softmax has written P_jp
-        if (ok) ok = tc_wait(&p_full[jp & 1], (jp >> 1) & 1, a.err);
-        if (!ok) return;
-        tc05::fence_after();
+        // O_t += P_t,jp V_jp for both tiles, each once its softmax has written P_t,jp
         const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
-        const uint32_t pb = p_addr + (jp & 1) * kTcPBytes;
+        for (int t = 0; t < kTcTiles && ok; ++t) {
+          ok = mbar_wait(&p_full[2 * t + (jp & 1)], (jp >> 1) & 1, a.err);
+          if (!ok) break;
+          tc05::fence_after();
+          const uint32_t pb = p_addr + (2 * t + (jp & 1)) * kTcPBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
-          const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
-          tc05::mma_bf16_ss(t_o, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
+            const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
+            tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc05::commit(&o_done[t]);
+          tc05::commit(&p_free[2 * t + (jp & 1)]);
         }
-        tc05::commit(o_done);
-        tc05::commit(&kv_empty[jp % kTcStages]);
-        tc05::commit(&p_free[jp & 1]);
+        if (ok) tc05::commit(&kv_empty[jp % kTcStages]);
       };
       for (int j = 0; j < n_sel && ok; ++j) {
         const int stage = j % kTcStages;
-        ok = tc_wait(&kv_full[stage], (j / kTcStages) & 1, a.err);
-        if (ok && j >= 2) ok = tc_wait(&s_free[j & 1], ((j - 2) >> 1) & 1, a.err);
-        if (!ok) break;
-        tc05::fence_after();
+        ok = mbar_wait(&kv_full[stage], (j / kTcStages) & 1, a.err);
         const uint32_t kb = ring_addr + stage * kPaSlotBytes;
+        for (int t = 0; t < kTcTiles && ok; ++t) {
+          if (j >= 2) ok = mbar_wait(&s_free[2 * t + (j & 1)], ((j - 2) >> 1) & 1, a.err);
+          if (!ok) break;
+          tc05::fence_after();
+          const uint32_t qa = q_addr + t * kTcQBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
-          const uint64_t da = tc05::smem_desc(q_addr + half * (kTcQBytes / 2) + off, 16, 1024);
-          const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
-          tc05::mma_bf16_ss(t_s[j & 1], da, db, id_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
+            const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
+            const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
+            tc05::mma_bf16_ss(tmem + (2 * t + (j & 1)) * 64, da, db, id_qk, kk > 0 ? 1u : 0u);
+          }
+          tc05::commit(&s_full[2 * t + (j & 1)]);
         }
-        tc05::commit(&s_full[j & 1]);
-        if (j >= 1) issue_pv(j - 1);
+        if (ok && j >= 1) issue_pv(j - 1);
       }
       if (ok && n_sel > 0) issue_pv(n_sel - 1);
     }
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
+    const int t = (warp - 2) >> 2;                           // query tile
     const int quarter = warp & 3;                            // tensor-memory lanes 32q .. 32q+31
-    const int r = quarter * 32 + lane;                       // query row: token r/16, head r%16
-    const int tok = tok0 + (r >> 4);
+    const int r = quarter * 32 + lane;                       // row: token r/16 of the tile, head r%16
+    const int tok = tok0 + 8 * t + (r >> 4);
     const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n_sel; ++j) {
-      if (ok) ok = __all_sync(0xffffffffu, tc_wait(&s_full[j & 1], (j >> 1) & 1, a.err));
+      const int sb = 2 * t + (j & 1);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, a.err));
       float sv[64];
       if (ok) {
         tc05::fence_after();
         float x0[32], x1[32];
-        tc05::ld32(t_s[j & 1] + lane_off, x0);
-        tc05::ld32(t_s[j & 1] + lane_off + 32, x1);
+        tc05::ld32(tmem + sb * 64 + lane_off, x0);
+        tc05::ld32(tmem + sb * 64 + lane_off + 32, x1);
         tc05::wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -775,38 +785,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       }
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&s_free[j & 1]);
+      if (lane == 0) bar_arrive(&s_free[sb]);
       if (!ok) {
-        if (lane == 0) bar_arrive(&p_full[j & 1]);
+        if (lane == 0) bar_arrive(&p_full[sb]);
         continue;
       }
       int jb = a.idx[row * kslots + j];                      // the block of S_j (as the producer read it)
       if (jb < 0 || jb > c) jb = 0;
-      const int kbase = jb * kBlock;
+      // raw logits; the scale log2(e)/sqrt(d) > 0 is folded into the exponent below. Only the
+      // chunk's own block has keys after some of the tile's tokens.
+      if (jb == c) {
+        const int kbase = jb * kBlock;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = (kbase + e <= tok) ? sv[e] : -INFINITY;
+      }
       float mb = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        sv[e] = (kbase + e <= tok) ? sv[e] * sl2 : -INFINITY;
-        mb = fmaxf(mb, sv[e]);
-      }
+      for (int e = 0; e < 64; ++e) mb = fmaxf(mb, sv[e]);
+      mb *= sl2;
       // move the running max only when it grows by more than 2^8 (or on the first block)
       const bool first = (m_used == -INFINITY);
       const bool grow = !first && mb > m_used + kRescaleLog2;
       if (__any_sync(0xffffffffu, grow)) {
         // O in tensor memory holds P_0..P_{j-1} V: rescale it once O += P_{j-1} V_{j-1} is done
+        // (O += P_{j-2} V_{j-2} was issued before S_j and is complete, so this parity wait is
+        // one phase ahead)
         const float mn = fmaxf(m_used, mb);
         const float alpha = exp2f(m_used - mn);
-        ok = __all_sync(0xffffffffu, tc_wait(o_done, (j - 1) & 1, a.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1, a.err));
         if (ok) {
           tc05::fence_after();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             float o[32];
-            tc05::ld32(t_o + lane_off + 32 * q4, o);
+            tc05::ld32(t_o + 32 * q4, o);
             tc05::wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tc05::st32(t_o + lane_off + 32 * q4, o);
+            tc05::st32(t_o + 32 * q4, o);
           }
           tc05::wait_st();
         }
@@ -819,15 +835,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = exp2f(sv[2 * e] - m_used), p1 = exp2f(sv[2 * e + 1] - m_used);
+        const float p0 = exp2f(fmaf(sv[2 * e], sl2, -m_used)), p1 = exp2f(fmaf(sv[2 * e + 1], sl2, -m_used));
         ps += p0 + p1;
         pk[e] = pack_bf16(p0, p1);
       }
       l += ps;
-      // P_j into its buffer once O += P_{j-2} V_{j-2} has read it
-      if (j >= 2) ok = __all_sync(0xffffffffu, tc_wait(&p_free[j & 1], ((j - 2) >> 1) & 1, a.err));
+      // P_t,j into its buffer once O_t += P_t,j-2 V_j-2 has read it
+      if (j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&p_free[sb], ((j - 2) >> 1) & 1, a.err));
       if (ok) {
-        uint8_t* prow = pbuf + (j & 1) * kTcPBytes + r * 128;
+        uint8_t* prow = pbuf + sb * kTcPBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
@@ -836,10 +852,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       fence_proxy_async_shared();
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&p_full[j & 1]);
+      if (lane == 0) bar_arrive(&p_full[sb]);
     }
-    // ---- epilogue: O / l of this row (token tok, head r % 16)
-    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, tc_wait(o_done, (n_sel - 1) & 1, a.err));
+    // ---- epilogue: O / l of this row (token tok, head r % 16). O += P V of the last two
+    // blocks may both still be in flight (each is issued after the next block's S), so the
+    // waits go phase by phase: a parity wait is only unambiguous one phase ahead.
+    if (ok && n_sel > 1) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (n_sel - 2) & 1, a.err));
+    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (n_sel - 1) & 1, a.err));
     if (ok && n_sel > 0) {
       tc05::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -847,7 +866,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         float o[32];
-        tc05::ld32(t_o + lane_off + 32 * q4, o);
+        tc05::ld32(t_o + 32 * q4, o);
         tc05::wait_ld();
         if (tok < T) {
 #pragma unroll
@@ -891,7 +910,7 @@ void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUte
 void launch_prefill_attn_tc(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, int batch, cudaStream_t s) {
   cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-  prefill_attn_tc_kernel<<<dim3(a.nb_cap * kSlices, batch * a.G), kTcThreads, kTcSmem, s>>>(a, mq, mk, mv);
+  prefill_attn_tc_kernel<<<dim3(a.nb_cap * kTcSlices, batch * a.G), kTcThreads, kTcSmem, s>>>(a, mq, mk, mv);
 }
 
 }  // namespace sparda

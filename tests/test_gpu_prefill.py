@@ -154,3 +154,26 @@ def test_prefill_at_context_32768_sampled(sb):
                 ref = O.block_sparse_attention(to64(q[0, t, 16 * g:16 * g + 16]), K, V, sel, t + 1)
                 assert toks[-1] == t
                 check_attention(out[0, t, 16 * g:16 * g + 16].float().cpu().numpy(), ref)
+
+
+def test_prefill_attention_when_later_blocks_dominate(sb):
+    """Keys of the later blocks scaled up four-fold: every chunk's later blocks carry far larger
+    logits than block 0, so the running maximum of the online softmax must move (and the
+    partial output be rescaled) part-way through the blocks."""
+    T_list, k, max_ctx = [1100, 777], 6, 2048
+    shape, layer, q, f, seq = _prompt(sb, 57, T_list, k, max_ctx)
+    layer.k[:, :, 256:] *= 4
+    B = len(T_list)
+    idx, cnt = _select(sb, shape, "forecast", layer, f, seq, B)
+    out = torch.zeros((B, max_ctx, 32, 128), dtype=torch.bfloat16, device="cuda")
+    sb.sparda_prefill_attn(shape, layer, q, idx, cnt, seq, B, out)
+    torch.cuda.synchronize()
+    assert sb.sparda_device_error(clear=True) == 0
+    idx, cnt, o = idx.cpu().numpy(), cnt.cpu().numpy(), out.float().cpu().numpy()
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            sel = [[int(j) for j in idx[b, g, c, :cnt[b, g, c]]] for c in range(O.prefill_num_chunks(T))]
+            ref = O.prefill_block_sparse_attention(to64(q[b, :T, 16 * g:16 * g + 16]), to64(layer.k[b, g]),
+                                                   to64(layer.v[b, g]), sel, T)
+            for t in range(T):
+                check_attention(o[b, t, 16 * g:16 * g + 16], ref[t])
