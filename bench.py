@@ -707,12 +707,16 @@ def prefill_ab(device, seed, contexts=(32768, 65536, 131072)):
 
 
 # ---------------------------------------------------------------------- single-kernel cases
-def kernel_case(name, batch=16, ctx=CTX, reps=50, seed=0):
+def kernel_case(name, batch=16, ctx=CTX, reps=48, seed=0):
     """One kernel alone on a seeded case, for profilers and quick timing: 'attn' (the
     standalone block-sparse decode attention over a forecast selection), 'select' (the
     standalone Forecast selector), 'multihead' (the baseline selector) or 'prefill' (one layer's
-    prefill A/B, batch 1). Prints the mean device time of `reps` launches captured back to back
-    in a CUDA graph and of single launches after an L2 flush, with the algorithmic GB/s."""
+    prefill A/B, batch 1). Consecutive launches cycle through input sets whose bytes together
+    exceed twice the L2 (different selections for 'attn', different compressed-key buffers for
+    the selectors), so no launch finds its data in L2. Prints the mean device time of `reps`
+    launches captured back to back in a CUDA graph and the median of single launches after
+    an L2 flush (launch latency included), with the algorithmic GB/s."""
+    import math
     import torch
     import synth
     import block_sparse_attention_forecast_gb300.binding as sb
@@ -721,46 +725,52 @@ def kernel_case(name, batch=16, ctx=CTX, reps=50, seed=0):
         print(json.dumps(prefill_ab(device, seed, (ctx,))))
         return
     B = batch
+    l2 = 129 << 20
     shape = sb.Shape(n_groups=G, topk=TOPK, max_ctx=ctx, max_batch=B)
     layer = sb.LayerKV.empty(shape, device=device)
     layer.k.copy_(synth.normal_bf16_device(layer.k.shape, seed * 1000 + 11, device))
     layer.v.copy_(synth.normal_bf16_device(layer.v.shape, seed * 1000 + 12, device))
     seq = torch.full((B,), ctx, dtype=torch.int32, device=device)
     sb.sparda_compress_keys(shape, layer, seq - 1, B)
-    f = synth.normal_bf16_device((B, G, D), seed * 1000 + 13, device)
     q = synth.normal_bf16_device((B, G * H, D), seed * 1000 + 14, device)
-    idx = torch.zeros((B, G, TOPK + 2), dtype=torch.int32, device=device)
-    cnt = torch.zeros((B, G), dtype=torch.int32, device=device)
     ws = sb.workspace(shape, B, sb.WS_SELECT, device)
     wa = sb.workspace(shape, B, sb.WS_ATTN, device)
     wm = sb.workspace(shape, B, sb.WS_MULTIHEAD, device)
     out = torch.zeros((B, G * H, D), dtype=torch.bfloat16, device=device)
-    sb.sparda_forecast_select(shape, layer.ck, f, seq, B, idx, cnt, ws)
     from block_sparse_attention_forecast_gb300.binding import num_windows
     sel_b = B * G * (num_windows(ctx - 1) * D * 2 + D * 2)
-    calls = {
-        "attn": (lambda s: sb.sparda_sparse_decode_attn(shape, layer, q, idx, cnt, seq, B, out, wa, stream=s),
-                 attn_bytes(B)),
-        "select": (lambda s: sb.sparda_forecast_select(shape, layer.ck, f, seq, B, idx, cnt, ws, stream=s), sel_b),
-        "multihead": (lambda s: sb.sparda_multihead_select(shape, layer.ck, q, seq, B, idx, cnt, wm, stream=s),
-                      sel_b - B * G * D * 2 + B * G * H * D * 2),
-    }
-    fn, nbytes = calls[name]
-    t_chain = graph_time(lambda s: [fn(s) for _ in range(reps)]) / reps
+    nbytes = {"attn": attn_bytes(B), "select": sel_b, "multihead": sel_b - B * G * D * 2 + B * G * H * D * 2}[name]
+    n_sets = max(1, math.ceil(2 * l2 / nbytes))
+    fs = [synth.normal_bf16_device((B, G, D), seed * 1000 + 20 + i, device) for i in range(n_sets)]
+    idxs = [torch.zeros((B, G, TOPK + 2), dtype=torch.int32, device=device) for _ in range(n_sets)]
+    cnts = [torch.zeros((B, G), dtype=torch.int32, device=device) for _ in range(n_sets)]
+    cks = [layer.ck] + [layer.ck.clone() for _ in range(n_sets - 1)] if name != "attn" else [layer.ck]
+    for i in range(n_sets):
+        sb.sparda_forecast_select(shape, layer.ck, fs[i], seq, B, idxs[i], cnts[i], ws)
+
+    def call(i, s):
+        k = i % n_sets
+        if name == "attn":
+            sb.sparda_sparse_decode_attn(shape, layer, q, idxs[k], cnts[k], seq, B, out, wa, stream=s)
+        elif name == "select":
+            sb.sparda_forecast_select(shape, cks[k], fs[k], seq, B, idxs[k], cnts[k], ws, stream=s)
+        else:
+            sb.sparda_multihead_select(shape, cks[k], q, seq, B, idxs[k], cnts[k], wm, stream=s)
+    t_chain = graph_time(lambda s: [call(i, s) for i in range(reps)]) / reps
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     st = torch.cuda.current_stream()
     single = []
-    for _ in range(20):
+    for i in range(20):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
-        fn(st)
+        call(i, st)
         b.record(st)
         torch.cuda.synchronize()
         single.append(a.elapsed_time(b) * 1e-3)
     single.sort()
     t1 = single[len(single) // 2]
-    print(json.dumps({"case": name, "batch": B, "context": ctx, "alg_bytes": nbytes,
+    print(json.dumps({"case": name, "batch": B, "context": ctx, "alg_bytes": nbytes, "input_sets": n_sets,
                       "us_back_to_back": t_chain * 1e6, "gbs_back_to_back": nbytes / t_chain / 1e9,
                       "us_single_after_l2_flush": t1 * 1e6, "gbs_single": nbytes / t1 / 1e9,
                       "device_error_flags": sb.sparda_device_error(clear=True)}))

@@ -170,9 +170,8 @@ struct PrefillArgs {
 };
 void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s);
 void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mck, int batch, cudaStream_t s);
-void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, int batch,
-                         cudaStream_t s);
-// the same attention on tcgen05 tensor cores; mq: the queries as [rows, 128] in 64 x 16 boxes
+// the causal block-sparse prefill attention on tcgen05 tensor cores; mq: the queries as
+// [rows, 128] in 64 x 16 boxes, mk / mv: the layer's K and V as [rows, 128] in 64 x 64 boxes
 void launch_prefill_attn_tc(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, int batch, cudaStream_t s);
 int multihead_tiles(int w_cap);

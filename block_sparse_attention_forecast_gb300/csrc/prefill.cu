@@ -24,10 +24,10 @@
 //       (a warp = one token's 16 heads): the per-row log-sum-exp, then the column sums of the
 //       normalised probabilities, added in a fixed order into the chunk's window sums in
 //       shared memory; then max-pool and the top-k in the same CTA.
-//   prefill_attn_kernel            per (sequence-group, chunk, 8-token slice): the chunk's
-//       selected K/V blocks through a TMA ring; each consumer warp runs one token's 16 heads
-//       over every block (QK^T and PV on bf16 mma.sync, float32 online softmax), causal in
-//       the chunk's own block.
+//   prefill_attn_tc_kernel         per (sequence-group, chunk, 16-token slice): two 128-row
+//       query tiles on the fifth-generation tensor cores (tcgen05.mma, accumulators in tensor
+//       memory), the chunk's selected K/V blocks through a TMA ring, causal in the chunk's own
+//       block (described at the kernel).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
@@ -193,9 +193,7 @@ namespace {
 
 constexpr int kPaConsumerWarps = 8;
 constexpr int kPaThreads = (kPaConsumerWarps + 1) * 32;     // 8 consumer warps + producer
-constexpr int kPaStages = 4;
 constexpr int kPaSlotBytes = 2 * kBlockBytes;                // K + V of one block
-constexpr int kPaSmem = 1024 + 1024 + kPaStages * kPaSlotBytes;
 constexpr int kMhStages = 6;
 constexpr int kMhTileBytes = kBlockBytes;                    // 64 windows x 128 dims bf16
 // [align slack][barriers][ring][per-warp column sums, 2 buffers][top-k scratch][window sums]
@@ -203,7 +201,6 @@ constexpr int kMhFixedSmem = 1024 + 1024 + kMhStages * kMhTileBytes + 2 * kPaCon
                              ((int)sizeof(TopkShared) + 15) / 16 * 16;
 __host__ __device__ constexpr int mh_smem_bytes(int w_cap) { return kMhFixedSmem + 4 * w_cap; }
 static_assert(mh_smem_bytes(kMaxCtx / kWinStride) <= 227 * 1024, "the baseline prefill selector fits shared memory");
-constexpr int kSlices = 8;                                   // 8-token slices of a chunk
 
 // Shared address of 16-byte chunk `chunk` (0..15 over the 128 dims) of row r of a 64-row
 // tile staged by TMA as two 64-column halves with the 128-byte swizzle.
@@ -253,166 +250,6 @@ __device__ __forceinline__ void qk_tile(const uint32_t (&qf)[8][4], const uint8_
 }
 
 }  // namespace
-
-// ==================================================================== block-sparse attention
-__global__ void __launch_bounds__(kPaThreads, 1) prefill_attn_kernel(const PrefillArgs a,
-                                                                     const __grid_constant__ CUtensorMap mk,
-                                                                     const __grid_constant__ CUtensorMap mv) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kPaStages;
-  int* stage_j = reinterpret_cast<int*>(empty + kPaStages);
-  uint8_t* ring = smem + 1024;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
-  const int c = blockIdx.x / kSlices, sl = blockIdx.x % kSlices;
-  const int T = a.seq_len[b];
-  if (!valid_len(T, a.max_ctx)) {
-    if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
-    return;
-  }
-  const int tok0 = c * kBlock + sl * kPaConsumerWarps;
-  if (tok0 >= T) return;                                     // CTA-uniform
-  const int kslots = a.topk + 2;
-  const size_t row = (size_t)bg * a.nb_cap + c;
-  const int n_sel = min(max(a.cnt[row], 0), kslots);
-
-  if (tid == 0) {
-    for (int i = 0; i < kPaStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPaConsumerWarps);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == kPaConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    prefetch_tensormap(&mk);
-    prefetch_tensormap(&mv);
-    for (int s = 0; s < n_sel; ++s) {
-      int j = a.idx[row * kslots + s];
-      if (j < 0 || j > c) {                                   // only blocks up to the chunk's own
-        atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
-        j = 0;
-      }
-      const int stage = s % kPaStages;
-      if (s >= kPaStages && !mbar_wait(&empty[stage], ((s / kPaStages) & 1) ^ 1, a.err)) return;
-      uint8_t* dst = ring + stage * kPaSlotBytes;
-      stage_j[stage] = j;
-      const int rr = bg * a.max_ctx + j * kBlock;
-      mbar_arrive_expect_tx(&full[stage], kPaSlotBytes);
-      tma_load_2d(dst, &mk, 0, rr, &full[stage]);
-      tma_load_2d(dst + kBlockBytes / 2, &mk, 64, rr, &full[stage]);
-      tma_load_2d(dst + kBlockBytes, &mv, 0, rr, &full[stage]);
-      tma_load_2d(dst + kBlockBytes + kBlockBytes / 2, &mv, 64, rr, &full[stage]);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers: one token each
-  const int tok = tok0 + warp;
-  const bool active = tok < T;
-  const int g8 = lane >> 2, cq = lane & 3;
-  const float sl2 = 1.4426950408889634f * 0.08838834764831845f;     // log2(e) / sqrt(128)
-  const __nv_bfloat16* q16 = a.q + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim;
-  uint32_t qf[8][4];
-  if (active) load_q_frags(q16, lane, qf);
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  bool ok = true;
-  for (int s = 0; s < n_sel; ++s) {
-    const int stage = s % kPaStages;
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (s / kPaStages) & 1, a.err));
-    if (ok && active) {
-      const int j = stage_j[stage];
-      const uint8_t* Kt = ring + stage * kPaSlotBytes;
-      const uint8_t* Vt = Kt + kBlockBytes;
-      float sc[8][4];
-      qk_tile(qf, Kt, lane, sc);
-      // causal: keys after the token (only in the chunk's own block) are masked
-      const int kbase = j * kBlock + 2 * cq;
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pos = kbase + 8 * n + (e & 1);
-          sc[n][e] = pos <= tok ? sc[n][e] * sl2 : -INFINITY;
-          if (e < 2) mx0 = fmaxf(mx0, sc[n][e]);
-          else mx1 = fmaxf(mx1, sc[n][e]);
-        }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        sc[n][0] = exp2f(sc[n][0] - base0);
-        sc[n][1] = exp2f(sc[n][1] - base0);
-        sc[n][2] = exp2f(sc[n][2] - base1);
-        sc[n][3] = exp2f(sc[n][3] - base1);
-        ps0 += sc[n][0] + sc[n][1];
-        ps1 += sc[n][2] + sc[n][3];
-      }
-      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-      l0 = l0 * al0 + ps0;
-      l1 = l1 * al1 + ps1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= al0;
-        o[n][1] *= al0;
-        o[n][2] *= al1;
-        o[n][3] *= al1;
-      }
-      // O += P V, the keys of the block as 4 k-steps of 16
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t pa0 = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-        const uint32_t pa1 = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-        const uint32_t pa2 = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        const uint32_t pa3 = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-        const int r = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int hi = lane >> 4;
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(swz_addr(Vt, r, 2 * np + hi), b0, b1, b2, b3);
-          mma_16816(o[2 * np], pa0, pa1, pa2, pa3, b0, b1);
-          mma_16816(o[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) bar_arrive(&empty[stage]);
-  }
-  if (!active || !ok) return;
-  // out[tok, g*16 + h, :] = O / l (rows g8 and g8+8 of the accumulators)
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  __nv_bfloat16* o16 = a.out + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim;
-  uint32_t* r0p = reinterpret_cast<uint32_t*>(o16 + (size_t)g8 * kHeadDim);
-  uint32_t* r1p = reinterpret_cast<uint32_t*>(o16 + (size_t)(g8 + 8) * kHeadDim);
-#pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    r0p[4 * n + cq] = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-    r1p[4 * n + cq] = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
-  }
-}
 
 // ==================================================================== baseline multi-head
 __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const PrefillArgs a,
@@ -587,7 +424,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 }
 
 // ==================================================================== block-sparse attention, tcgen05
-// The same work as prefill_attn_kernel on the fifth-generation tensor cores. A CTA holds two
+// Causal block-sparse prefill attention on the fifth-generation tensor cores. A CTA holds two
 // query tiles of 128 rows (8 tokens x 16 heads each, row 16i + h), 16 tokens of one chunk,
 // which share every K/V block it loads:
 //   warp 0, one thread: TMA loads of the two Q tiles (once) and of the chunk's K/V blocks into
@@ -604,6 +441,18 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 //       grows by more than 2^8, P_t,j written to shared memory as bf16 in the 128-byte-swizzled
 //       K-major layout; at the end O / l to the output.
 namespace {
+// Non-blocking test of an mbarrier phase (the MMA issuer polls several barriers in turn).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 constexpr int kTcTiles = 2;
 constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
 constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
@@ -711,51 +560,73 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread keeps the tensor cores fed: it polls the barriers and issues, for each tile,
+    // S_t,j as soon as block j is in shared memory and the tile's softmax has read S_t,j-2
+    // (its buffer), and O_t += P_t,j V_j as soon as the softmax has written P_t,j, in block
+    // order per tile. A block's ring stage is released once both tiles' O += P V have read it.
     if (lane == 0) {
       constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
       const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring), p_addr = smem_addr(pbuf);
       ok = mbar_wait(q_full, 0, a.err);
-      auto issue_pv = [&](int jp) {
-        // O_t += P_t,jp V_jp for both tiles, each once its softmax has written P_t,jp
-        const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
-        for (int t = 0; t < kTcTiles && ok; ++t) {
-          ok = mbar_wait(&p_full[2 * t + (jp & 1)], (jp >> 1) & 1, a.err);
-          if (!ok) break;
-          tc05::fence_after();
-          const uint32_t pb = p_addr + (2 * t + (jp & 1)) * kTcPBytes;
+      int qk[kTcTiles] = {0}, pv[kTcTiles] = {0}, released = 0;
+      uint32_t idle = 0;
+      while (ok && released < n_sel) {
+        bool progress = false;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
-            const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
-            tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc05::commit(&o_done[t]);
-          tc05::commit(&p_free[2 * t + (jp & 1)]);
-        }
-        if (ok) tc05::commit(&kv_empty[jp % kTcStages]);
-      };
-      for (int j = 0; j < n_sel && ok; ++j) {
-        const int stage = j % kTcStages;
-        ok = mbar_wait(&kv_full[stage], (j / kTcStages) & 1, a.err);
-        const uint32_t kb = ring_addr + stage * kPaSlotBytes;
-        for (int t = 0; t < kTcTiles && ok; ++t) {
-          if (j >= 2) ok = mbar_wait(&s_free[2 * t + (j & 1)], ((j - 2) >> 1) & 1, a.err);
-          if (!ok) break;
-          tc05::fence_after();
-          const uint32_t qa = q_addr + t * kTcQBytes;
+        for (int t = 0; t < kTcTiles; ++t) {
+          const int jq = qk[t];
+          if (jq < n_sel && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
+              (jq < 2 || mbar_test(&s_free[2 * t + (jq & 1)], ((jq - 2) >> 1) & 1))) {
+            tc05::fence_after();
+            const uint32_t kb = ring_addr + (jq % kTcStages) * kPaSlotBytes;
+            const uint32_t qa = q_addr + t * kTcQBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
-            const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
-            const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
-            tc05::mma_bf16_ss(tmem + (2 * t + (j & 1)) * 64, da, db, id_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
+              const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
+              const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
+              tc05::mma_bf16_ss(tmem + (2 * t + (jq & 1)) * 64, da, db, id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc05::commit(&s_full[2 * t + (jq & 1)]);
+            qk[t] = jq + 1;
+            progress = true;
           }
-          tc05::commit(&s_full[2 * t + (j & 1)]);
+          const int jp = pv[t];
+          if (jp < qk[t] && mbar_test(&p_full[2 * t + (jp & 1)], (jp >> 1) & 1)) {
+            tc05::fence_after();
+            const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
+            const uint32_t pb = p_addr + (2 * t + (jp & 1)) * kTcPBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
+              const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
+              tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc05::commit(&o_done[t]);
+            tc05::commit(&p_free[2 * t + (jp & 1)]);
+            pv[t] = jp + 1;
+            progress = true;
+          }
         }
-        if (ok && j >= 1) issue_pv(j - 1);
+        // the ring stage of every block both tiles have finished with
+        int done_both = pv[0];
+#pragma unroll
+        for (int t = 1; t < kTcTiles; ++t) done_both = min(done_both, pv[t]);
+        while (released < done_both) {
+          tc05::commit(&kv_empty[released % kTcStages]);
+          ++released;
+        }
+        if (progress) {
+          idle = 0;
+        } else {
+          __nanosleep(32);
+          if (++idle > (kWaitPolls << 6)) {                  // ~0.5 s without progress
+            atomicOr(a.err, SPARDA_DEV_WAIT_TIMEOUT);
+            ok = false;
+          }
+        }
       }
-      if (ok && n_sel > 0) issue_pv(n_sel - 1);
     }
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
@@ -766,9 +637,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
+    // the chunk's block indices, lane i holding entries i and 32 + i (read before the loop: no
+    // global load on the per-block path)
+    int jreg0 = lane < n_sel ? a.idx[row * kslots + lane] : 0;
+    int jreg1 = lane + 32 < n_sel ? a.idx[row * kslots + lane + 32] : 0;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n_sel; ++j) {
       const int sb = 2 * t + (j & 1);
+      int jb = __shfl_sync(0xffffffffu, j < 32 ? jreg0 : jreg1, j & 31);   // the block of S_j
+      if (jb < 0 || jb > c) jb = 0;
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, a.err));
       float sv[64];
       if (ok) {
@@ -790,8 +667,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         if (lane == 0) bar_arrive(&p_full[sb]);
         continue;
       }
-      int jb = a.idx[row * kslots + j];                      // the block of S_j (as the producer read it)
-      if (jb < 0 || jb > c) jb = 0;
       // raw logits; the scale log2(e)/sqrt(d) > 0 is folded into the exponent below. Only the
       // chunk's own block has keys after some of the tile's tokens.
       if (jb == c) {
@@ -901,11 +776,6 @@ void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mc
   prefill_multihead_kernel<<<dim3(a.nb_cap, batch * a.G), kPaThreads, smem, s>>>(a, mck);
 }
 
-void launch_prefill_attn(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, int batch,
-                         cudaStream_t s) {
-  cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPaSmem);
-  prefill_attn_kernel<<<dim3(a.nb_cap * kSlices, batch * a.G), kPaThreads, kPaSmem, s>>>(a, mk, mv);
-}
 
 void launch_prefill_attn_tc(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, int batch, cudaStream_t s) {
