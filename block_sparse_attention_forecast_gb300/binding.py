@@ -34,7 +34,8 @@ __all__ = [
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libsparda.so")
+# SPARDA_LIB may name another build of the same library (the per-CTA timeline variant)
+LIB_PATH = os.environ.get("SPARDA_LIB") or os.path.join(_PKG, "_lib", "libsparda.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "sparda.h")
 
 OK = 0

@@ -19,6 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libsparda.so")
+# the per-CTA timeline variant (-DSPARDA_TIMELINE): a separate library, never the product one
+LIB_TIMELINE = os.path.join(OUT_DIR, "libsparda_timeline.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
@@ -42,15 +44,15 @@ def _deps():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src, extra):
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+def _compile(src, extra, tag=""):
+    obj = os.path.join(OUT_DIR, os.path.basename(src) + tag + ".o")
     cmd = [nvcc()] + ARCH + FLAGS + extra + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -58,28 +60,32 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(force=False, verbose=False, extra=None):
-    """Compile every CUDA source and link libsparda.so; returns the library path."""
+def build(force=False, verbose=False, extra=None, timeline=False):
+    """Compile every CUDA source and link libsparda.so; returns the library path. timeline=True
+    builds the per-CTA timeline variant (libsparda_timeline.so) instead."""
     extra = list(extra or [])
-    if not force and not extra and up_to_date():
-        return LIB
+    lib, tag = (LIB_TIMELINE, ".tl") if timeline else (LIB, "")
+    if timeline:
+        extra.append("-DSPARDA_TIMELINE")
+    if not force and (timeline or not extra) and up_to_date(lib):
+        return lib
     os.makedirs(OUT_DIR, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), sources()))
+        results = list(ex.map(lambda s: _compile(s, extra, tag), sources()))
     objs = [o for o, _ in results]
     if verbose:
         for _, err in results:
             if err.strip():
                 print(err, file=sys.stderr)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     for o in objs:
         os.remove(o)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

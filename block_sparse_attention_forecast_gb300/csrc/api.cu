@@ -19,6 +19,46 @@ void launch_select_topk(const SelectArgs& a, int bg_count, cudaStream_t s);     
 // The device error word (bits SPARDA_DEV_*). Kernels receive its device address.
 __device__ int g_sparda_dev_error;
 
+#include "timeline.cuh"
+#ifdef SPARDA_TIMELINE
+#include <atomic>
+static __device__ sparda::TimelineBuf g_sparda_timeline;
+namespace sparda {
+static std::atomic<uint32_t> g_tl_launch{0};
+uint32_t timeline_next_launch() { return g_tl_launch.fetch_add(1) + 1; }
+void* timeline_buffer() {
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, g_sparda_timeline) == cudaSuccess ? p : nullptr;
+}
+}  // namespace sparda
+// Timeline build only (not part of the product ABI): copy up to max_records records
+// (t_entry, t_release, t_exit as uint64 ns; launch, role << 24 | cta as uint32) to host memory,
+// the count to *n, and, if reset != 0, clear the count and restart the launch numbering.
+extern "C" int32_t sparda_timeline_read(void* host, int32_t max_records, int32_t* n, int32_t reset) {
+  unsigned int cnt = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPARDA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&cnt, g_sparda_timeline, sizeof(cnt)) != cudaSuccess) return SPARDA_ERR_CUDA;
+  if (cnt > (unsigned)sparda::kTimelineMax) cnt = sparda::kTimelineMax;
+  const unsigned int k = cnt < (unsigned)max_records ? cnt : (unsigned)max_records;
+  if (host && k &&
+      cudaMemcpyFromSymbol(host, g_sparda_timeline, k * sizeof(sparda::TimelineRec),
+                           offsetof(sparda::TimelineBuf, rec)) != cudaSuccess)
+    return SPARDA_ERR_CUDA;
+  if (n) *n = (int32_t)k;
+  if (reset) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_sparda_timeline, &zero, sizeof(zero)) != cudaSuccess) return SPARDA_ERR_CUDA;
+    sparda::g_tl_launch = 0;
+  }
+  return SPARDA_OK;
+}
+#else
+namespace sparda {
+uint32_t timeline_next_launch() { return 0; }
+void* timeline_buffer() { return nullptr; }
+}  // namespace sparda
+#endif
+
 namespace {
 
 constexpr int kMaxDevices = 64;

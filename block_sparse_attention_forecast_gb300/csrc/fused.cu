@@ -11,6 +11,7 @@
 // the attention CTAs, which need that top-k's blocks, take the SMs its CTAs release.
 #include "attn_body.cuh"
 #include "select_body.cuh"
+#include "timeline.cuh"
 
 namespace sparda {
 
@@ -26,14 +27,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
     const AttnArgs aa, const SelectArgs sa, int n_attn, const __grid_constant__ CUtensorMap mk,
     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap hk,
     const __grid_constant__ CUtensorMap hv) {
+  SPARDA_TL_ENTRY();
   grid_dep_launch();                   // the next prologue's projection may take freed SMs
   const int n_sel = (int)gridDim.x - n_attn;
-  if ((int)blockIdx.x >= n_sel)
+  const bool attn = (int)blockIdx.x >= n_sel;
+  if (attn)
     attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x - n_sel, n_attn);
   else if (sa.queue)
     sel_cta_dyn(sa, blockIdx.x, n_sel);
   else
     sel_cta(sa, blockIdx.x, n_sel);
+  SPARDA_TL_EXIT(aa.tl_buf, aa.tl_launch, attn ? kTlAttention : kTlSelection, 0ull);
 }
 
 int sm_count();
@@ -83,6 +87,8 @@ void launch_attend_and_select(const AttnArgs& a, const SelectArgs& s, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  aa.tl_launch = timeline_next_launch();
+  aa.tl_buf = timeline_buffer();
   cudaLaunchKernelEx(&cfg, attend_and_select_kernel, aa, sa, n_attn, mk, mv, hk, hv);
 }
 

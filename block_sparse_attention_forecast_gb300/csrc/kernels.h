@@ -84,6 +84,8 @@ struct AttnArgs {
   // (bg * stage_slots + stage_slot[u]) of the staging map; nullptr: row block u
   const int32_t* stage_slot = nullptr;
   int stage_slots = 0;
+  uint32_t tl_launch = 0;        // launch number for the timeline build's records
+  void* tl_buf = nullptr;        // the timeline build's record store
 };
 
 struct MultiheadArgs {
@@ -150,6 +152,8 @@ struct PrologueArgs {
   int32_t* cnt;                  // [B, G]
   int topk, nb_cap, bg_count;
   int n_proj, n_topk;            // CTAs of the projection and top-k roles
+  uint32_t tl_launch;            // launch number for the timeline build's records
+  void* tl_buf;                  // the timeline build's record store
 };
 void launch_decode_prologue(const PrologueArgs& a, cudaStream_t s);
 void launch_multihead_select(const MultiheadArgs& a, const CUtensorMap& mck, int bg_count, cudaStream_t s);

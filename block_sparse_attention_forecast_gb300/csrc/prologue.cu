@@ -25,6 +25,7 @@
 // so that it still completes after the previous launch.
 #include "append_body.cuh"
 #include "project_body.cuh"
+#include "timeline.cuh"
 #include "topk.cuh"
 
 namespace sparda {
@@ -40,22 +41,27 @@ union PrologueShared {
 
 __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const PrologueArgs a) {
   __shared__ PrologueShared sh;
+  SPARDA_TL_ENTRY();
+  unsigned long long t_rel = 0;
   int c = blockIdx.x;
   if (c < a.n_proj) {                  // reads only the layer's inputs and weights: no wait
     grid_dep_launch();
     const int n_tiles = a.pj.rows / 8;
     project_rows(a.pj, c % n_tiles, c / n_tiles, sh.pj, 1);
+    SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlProjection, t_rel);
     return;
   }
   c -= a.n_proj;
   if (c < a.n_topk) {                  // the scores are the previous launch's output
     grid_dep_wait();
+    SPARDA_TL_RELEASE(t_rel);
     grid_dep_launch();                 // only once the previous launch has completed
     if (c < a.bg_count) {
       const int T = a.ap.seq_len[c / a.ap.G];
       topk_select(a.block_scores + (size_t)c * a.nb_cap, a.idx + (size_t)c * (a.topk + 2), a.cnt + c,
                   a.topk, a.ap.max_ctx, T, sh.tk);
     }
+    SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlTopk, t_rel);
     return;
   }
   if (a.n_topk == 0) grid_dep_wait();
@@ -63,6 +69,7 @@ __global__ void __launch_bounds__(kPrologueThreads) decode_prologue_kernel(const
   c -= a.n_topk;
   const int bg = c * kAppendPerCta + (int)threadIdx.x / 64;
   if (bg < a.bg_count) append_token(a.ap, bg, threadIdx.x % 64);
+  SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlAppend, t_rel);
 }
 
 void launch_decode_prologue(const PrologueArgs& args, cudaStream_t s) {
@@ -80,6 +87,8 @@ void launch_decode_prologue(const PrologueArgs& args, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  a.tl_launch = timeline_next_launch();
+  a.tl_buf = timeline_buffer();
   cudaLaunchKernelEx(&cfg, decode_prologue_kernel, a);
 }
 
