@@ -67,10 +67,12 @@ def measured_peaks():
 
 # the sources each profiled kernel is built from (a change to any of them voids its counters)
 KERNEL_SOURCES = {
-    "attend_and_score": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
-    "attend_and_select": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
+    "attend_and_score": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h",
+                         "timeline.cuh"),
+    "attend_and_select": ("fused.cu", "attn_body.cuh", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h",
+                          "timeline.cuh"),
     "decode_prologue": ("prologue.cu", "append_body.cuh", "project_body.cuh", "topk.cuh", "common.cuh",
-                        "kernels.h"),
+                        "kernels.h", "timeline.cuh"),
     "sparse_decode_attn": ("attn.cu", "attn_body.cuh", "common.cuh", "kernels.h"),
     "forecast_select": ("select.cu", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
 }
@@ -1016,6 +1018,9 @@ def run_ours(args):
                      "traffic": ncu_traffic(dom), "alg_bytes_per_launch": dk["alg_bytes"],
                      "launch_us": dk["us"]},
         "kernels": kernels,
+        # the whole step against HBM: every layer's selection and attention bytes over the step
+        "select_attn_frac": {"bytes_per_step": n * (sel_b + att_b), "gbs": n * (sel_b + att_b) / (ms * 1e-3) / 1e9,
+                             "peak": hbm, "frac": n * (sel_b + att_b) / (ms * 1e-3) / 1e9 / hbm},
         "e2e": {"value": replica_throughput(world, BATCH, e2e_steps, e2e_elapsed), "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
