@@ -885,7 +885,10 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch": BATCH, "context": CTX, "layers": N_LAYERS, "topk": TOPK},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            # each "step" here is one sampled unit; ms_per_step is extrapolated to the 1024 units
+            # of a full step, so steps x ms_per_step is far longer than this run takes
+            "extrapolated": {"units_timed": units, "units_per_step": N_LAYERS * BATCH * G}}
     print(json.dumps(line), flush=True)
 
 

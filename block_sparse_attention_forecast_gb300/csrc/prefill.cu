@@ -441,6 +441,28 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 //       grows by more than 2^8, P_t,j written to shared memory as bf16 in the 128-byte-swizzled
 //       K-major layout; at the end O / l to the output.
 namespace {
+// The softmax warps' waits: the library's bounded wait, or (SPARDA_TC_SPIN) a bounded loop of
+// try_wait without the suspend-time hint.
+__device__ __forceinline__ bool sm_wait(uint64_t* bar, uint32_t parity, int* err) {
+#ifdef SPARDA_TC_SPIN
+  for (uint32_t i = 0; i < (kWaitPolls << 4); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  atomicOr(err, SPARDA_DEV_WAIT_TIMEOUT);
+  return false;
+#else
+  return mbar_wait(bar, parity, err);
+#endif
+}
+
 // Non-blocking test of an mbarrier phase (the MMA issuer polls several barriers in turn).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
@@ -456,11 +478,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 constexpr int kTcTiles = 2;
 constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
 constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
-constexpr int kTcStages = 3;
+#ifndef SPARDA_TC_STAGES
+#define SPARDA_TC_STAGES 4
+#endif
+#ifndef SPARDA_TC_PBUFS
+#define SPARDA_TC_PBUFS 1
+#endif
+constexpr int kTcStages = SPARDA_TC_STAGES;                 // K/V ring stages
+constexpr int kTcPBufs = SPARDA_TC_PBUFS;                   // P buffers per tile
 constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB per tile: 128 rows x 128 dims
 constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB per tile and buffer: 128 x 64 keys
 constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcTiles * kTcQBytes + kTcStages * kPaSlotBytes +
-                        kTcTiles * 2 * kTcPBytes;
+                        kTcTiles * kTcPBufs * kTcPBytes;
 static_assert(kTcSmem <= 227 * 1024, "the tcgen05 prefill attention fits shared memory");
 constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
 constexpr uint32_t kTcCols = 512;
@@ -478,13 +507,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   uint64_t* kv_empty = kv_full + kTcStages;                 // [stages]
   uint64_t* s_full = kv_empty + kTcStages;                  // [tile][2]
   uint64_t* s_free = s_full + 2 * kTcTiles;                 // [tile][2]
-  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile][2]
-  uint64_t* p_free = p_full + 2 * kTcTiles;                 // [tile][2]
-  uint64_t* o_done = p_free + 2 * kTcTiles;                 // [tile]
+  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile][P buffers]
+  uint64_t* p_free = p_full + kTcPBufs * kTcTiles;          // [tile][P buffers]
+  uint64_t* o_done = p_free + kTcPBufs * kTcTiles;          // [tile]
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(o_done + kTcTiles);
   uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
   uint8_t* ring = qs + kTcTiles * kTcQBytes;
-  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile][2] 16 KiB
+  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile][P buffers] 16 KiB
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
@@ -509,6 +538,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     for (int i = 0; i < 2 * kTcTiles; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
+    }
+    for (int i = 0; i < kTcPBufs * kTcTiles; ++i) {
       mbar_init(&p_full[i], 4);
       mbar_init(&p_free[i], 1);
     }
@@ -561,9 +592,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One thread keeps the tensor cores fed: it polls the barriers and issues, for each tile,
-    // S_t,j as soon as block j is in shared memory and the tile's softmax has read S_t,j-2
-    // (its buffer), and O_t += P_t,j V_j as soon as the softmax has written P_t,j, in block
-    // order per tile. A block's ring stage is released once both tiles' O += P V have read it.
+    // S_t,j as soon as block j is in shared memory, the tile's softmax has read S_t,j-2 (its
+    // buffer) and O_t += P_t,j-2 V_j-2 has been issued, and O_t += P_t,j V_j as soon as the
+    // softmax has written P_t,j, in block order per tile. A block's ring stage is released
+    // once both tiles' O += P V have read it.
     if (lane == 0) {
       constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
@@ -575,8 +607,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         bool progress = false;
 #pragma unroll
         for (int t = 0; t < kTcTiles; ++t) {
+          // S_t,j only after O_t += P_t,j-2 V_j-2 has been issued: then the completion of S_t,j
+          // implies that of every earlier O update of the tile, which keeps the softmax's
+          // parity waits on o_done and p_free at most one phase ahead
           const int jq = qk[t];
-          if (jq < n_sel && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
+          if (jq < n_sel && pv[t] >= jq - 1 && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
               (jq < 2 || mbar_test(&s_free[2 * t + (jq & 1)], ((jq - 2) >> 1) & 1))) {
             tc05::fence_after();
             const uint32_t kb = ring_addr + (jq % kTcStages) * kPaSlotBytes;
@@ -593,10 +628,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
             progress = true;
           }
           const int jp = pv[t];
-          if (jp < qk[t] && mbar_test(&p_full[2 * t + (jp & 1)], (jp >> 1) & 1)) {
+          const int pbi = kTcPBufs * t + jp % kTcPBufs;
+          if (jp < qk[t] && mbar_test(&p_full[pbi], (jp / kTcPBufs) & 1)) {
             tc05::fence_after();
             const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
-            const uint32_t pb = p_addr + (2 * t + (jp & 1)) * kTcPBytes;
+            const uint32_t pb = p_addr + pbi * kTcPBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
@@ -604,7 +640,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
               tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
             }
             tc05::commit(&o_done[t]);
-            tc05::commit(&p_free[2 * t + (jp & 1)]);
+            tc05::commit(&p_free[pbi]);
             pv[t] = jp + 1;
             progress = true;
           }
@@ -646,7 +682,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       const int sb = 2 * t + (j & 1);
       int jb = __shfl_sync(0xffffffffu, j < 32 ? jreg0 : jreg1, j & 31);   // the block of S_j
       if (jb < 0 || jb > c) jb = 0;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1, a.err));
+      if (ok) ok = __all_sync(0xffffffffu, sm_wait(&s_full[sb], (j >> 1) & 1, a.err));
       float sv[64];
       if (ok) {
         tc05::fence_after();
@@ -660,11 +696,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
           sv[32 + e] = x1[e];
         }
       }
+      const int pbi = kTcPBufs * t + j % kTcPBufs;            // this block's P buffer
       tc05::fence_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&s_free[sb]);
       if (!ok) {
-        if (lane == 0) bar_arrive(&p_full[sb]);
+        if (lane == 0) bar_arrive(&p_full[pbi]);
         continue;
       }
       // raw logits; the scale log2(e)/sqrt(d) > 0 is folded into the exponent below. Only the
@@ -674,10 +711,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[e] = (kbase + e <= tok) ? sv[e] : -INFINITY;
       }
-      float mb = -INFINITY;
+      // row max as a tree (six levels of independent fmax, not a 64-long chain)
+      float mx[32];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mb = fmaxf(mb, sv[e]);
-      mb *= sl2;
+      for (int e = 0; e < 32; ++e) mx[e] = fmaxf(sv[e], sv[e + 32]);
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+      const float mb = mx[0] * sl2;
       // move the running max only when it grows by more than 2^8 (or on the first block)
       const bool first = (m_used == -INFINITY);
       const bool grow = !first && mb > m_used + kRescaleLog2;
@@ -687,7 +729,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         // one phase ahead)
         const float mn = fmaxf(m_used, mb);
         const float alpha = exp2f(m_used - mn);
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1, a.err));
+        ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (j - 1) & 1, a.err));
         if (ok) {
           tc05::fence_after();
 #pragma unroll
@@ -706,19 +748,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       } else if (first) {
         m_used = mb;
       }
-      float ps = 0.f;
       uint32_t pk[32];
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent partial sums
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float p0 = exp2f(fmaf(sv[2 * e], sl2, -m_used)), p1 = exp2f(fmaf(sv[2 * e + 1], sl2, -m_used));
-        ps += p0 + p1;
+        ps[e & 7] += p0 + p1;
         pk[e] = pack_bf16(p0, p1);
       }
-      l += ps;
-      // P_t,j into its buffer once O_t += P_t,j-2 V_j-2 has read it
-      if (j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&p_free[sb], ((j - 2) >> 1) & 1, a.err));
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      // P_t,j into its buffer once the O update that last read it (block j - kTcPBufs) is done
+      if (j >= kTcPBufs)
+        ok = __all_sync(0xffffffffu, sm_wait(&p_free[pbi], ((j - kTcPBufs) / kTcPBufs) & 1, a.err));
       if (ok) {
-        uint8_t* prow = pbuf + sb * kTcPBytes + r * 128;
+        uint8_t* prow = pbuf + pbi * kTcPBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
@@ -727,13 +770,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       fence_proxy_async_shared();
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&p_full[sb]);
+      if (lane == 0) bar_arrive(&p_full[pbi]);
     }
     // ---- epilogue: O / l of this row (token tok, head r % 16). O += P V of the last two
     // blocks may both still be in flight (each is issued after the next block's S), so the
     // waits go phase by phase: a parity wait is only unambiguous one phase ahead.
-    if (ok && n_sel > 1) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (n_sel - 2) & 1, a.err));
-    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], (n_sel - 1) & 1, a.err));
+    if (ok && n_sel > 1) ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (n_sel - 2) & 1, a.err));
+    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (n_sel - 1) & 1, a.err));
     if (ok && n_sel > 0) {
       tc05::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
