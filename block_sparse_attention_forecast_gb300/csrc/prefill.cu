@@ -463,6 +463,20 @@ __device__ __forceinline__ bool sm_wait(uint64_t* bar, uint32_t parity, int* err
 #endif
 }
 
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (one MUFU operation; the PTX ISA bounds its
+// relative error by 2^-22). Results below 2^-126 flush to zero, which the softmax cannot
+// notice: the running maximum it subtracts is a logit it has already summed, so every row's
+// sum is at least 1.
+__device__ __forceinline__ float ex2_ftz(float x) {
+#ifdef SPARDA_TC_LIBM_EXP2
+  return exp2f(x);
+#else
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+#endif
+}
+
 // Non-blocking test of an mbarrier phase (the MMA issuer polls several barriers in turn).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
@@ -480,6 +494,9 @@ constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
 constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
 #ifndef SPARDA_TC_STAGES
 #define SPARDA_TC_STAGES 4
+#endif
+#ifndef SPARDA_TC_ISSUER_SLEEP
+#define SPARDA_TC_ISSUER_SLEEP 32                           // ns the MMA issuer sleeps when idle
 #endif
 #ifndef SPARDA_TC_PBUFS
 #define SPARDA_TC_PBUFS 1
@@ -656,7 +673,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         if (progress) {
           idle = 0;
         } else {
-          __nanosleep(32);
+#if SPARDA_TC_ISSUER_SLEEP > 0
+          __nanosleep(SPARDA_TC_ISSUER_SLEEP);
+#endif
           if (++idle > (kWaitPolls << 6)) {                  // ~0.5 s without progress
             atomicOr(a.err, SPARDA_DEV_WAIT_TIMEOUT);
             ok = false;
@@ -728,7 +747,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         // (O += P_{j-2} V_{j-2} was issued before S_j and is complete, so this parity wait is
         // one phase ahead)
         const float mn = fmaxf(m_used, mb);
-        const float alpha = exp2f(m_used - mn);
+        const float alpha = ex2_ftz(m_used - mn);
         ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (j - 1) & 1, a.err));
         if (ok) {
           tc05::fence_after();
@@ -752,7 +771,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent partial sums
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = exp2f(fmaf(sv[2 * e], sl2, -m_used)), p1 = exp2f(fmaf(sv[2 * e + 1], sl2, -m_used));
+        const float p0 = ex2_ftz(fmaf(sv[2 * e], sl2, -m_used)), p1 = ex2_ftz(fmaf(sv[2 * e + 1], sl2, -m_used));
         ps[e & 7] += p0 + p1;
         pk[e] = pack_bf16(p0, p1);
       }
