@@ -433,13 +433,19 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 //       columns and an O of 128 columns) and, from one thread, issues per block j and tile t
 //       S_t,j = Q_t K_j^T (M 128, N 64, 8 K steps of 16) and O_t += P_t,j V_j (M 128, N 128,
 //       4 K steps; V read M/N-major), each completion signalled by tcgen05.commit on an
-//       mbarrier; both tiles' S_j+1 are issued before their O += P_j V_j, so the tensor cores
-//       work on one tile while the other tile's softmax runs;
+//       mbarrier; a tile's S_j+1 is issued as soon as block j+1 is loaded and its S buffer has
+//       been read, ahead of O += P_j V_j, so the tensor cores work on one tile's S while the
+//       softmax of the other runs;
 //   warps 2-5 (tile 0) and 6-9 (tile 1), one thread per row (tensor-memory lane): load S_t,j,
 //       mask the keys after the token (the chunk's own block), an online softmax in the exp2
 //       domain whose running maximum is only moved (and O rescaled in tensor memory) when it
 //       grows by more than 2^8, P_t,j written to shared memory as bf16 in the 128-byte-swizzled
 //       K-major layout; at the end O / l to the output.
+// Every mbarrier phase a thread waits for can only be followed by the barrier's next phase
+// after that thread itself has arrived somewhere (a parity wait tells phase k from phase k+2
+// only if k+1 cannot have completed behind its back): the tile's one P buffer and its O are
+// both signalled by pv_done, whose phase j (O += P_j V_j complete) needs every softmax warp's
+// P_j, and each warp waits its phases in order, phase j-1 before it writes P_j.
 namespace {
 // The softmax warps' waits: the library's bounded wait, or (SPARDA_TC_SPIN) a bounded loop of
 // try_wait without the suspend-time hint.
@@ -498,15 +504,11 @@ constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
 #ifndef SPARDA_TC_ISSUER_SLEEP
 #define SPARDA_TC_ISSUER_SLEEP 32                           // ns the MMA issuer sleeps when idle
 #endif
-#ifndef SPARDA_TC_PBUFS
-#define SPARDA_TC_PBUFS 1
-#endif
 constexpr int kTcStages = SPARDA_TC_STAGES;                 // K/V ring stages
-constexpr int kTcPBufs = SPARDA_TC_PBUFS;                   // P buffers per tile
 constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB per tile: 128 rows x 128 dims
-constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB per tile and buffer: 128 x 64 keys
+constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB per tile: 128 x 64 keys
 constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcTiles * kTcQBytes + kTcStages * kPaSlotBytes +
-                        kTcTiles * kTcPBufs * kTcPBytes;
+                        kTcTiles * kTcPBytes;
 static_assert(kTcSmem <= 227 * 1024, "the tcgen05 prefill attention fits shared memory");
 constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
 constexpr uint32_t kTcCols = 512;
@@ -524,13 +526,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   uint64_t* kv_empty = kv_full + kTcStages;                 // [stages]
   uint64_t* s_full = kv_empty + kTcStages;                  // [tile][2]
   uint64_t* s_free = s_full + 2 * kTcTiles;                 // [tile][2]
-  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile][P buffers]
-  uint64_t* p_free = p_full + kTcPBufs * kTcTiles;          // [tile][P buffers]
-  uint64_t* o_done = p_free + kTcPBufs * kTcTiles;          // [tile]
-  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(o_done + kTcTiles);
+  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile]
+  uint64_t* pv_done = p_full + kTcTiles;                    // [tile]
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(pv_done + kTcTiles);
   uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
   uint8_t* ring = qs + kTcTiles * kTcQBytes;
-  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile][P buffers] 16 KiB
+  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile] 16 KiB
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
@@ -556,11 +557,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
     }
-    for (int i = 0; i < kTcPBufs * kTcTiles; ++i) {
-      mbar_init(&p_full[i], 4);
-      mbar_init(&p_free[i], 1);
+    for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(&p_full[t], 4);
+      mbar_init(&pv_done[t], 1);
     }
-    for (int t = 0; t < kTcTiles; ++t) mbar_init(&o_done[t], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -609,10 +609,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One thread keeps the tensor cores fed: it polls the barriers and issues, for each tile,
-    // S_t,j as soon as block j is in shared memory, the tile's softmax has read S_t,j-2 (its
-    // buffer) and O_t += P_t,j-2 V_j-2 has been issued, and O_t += P_t,j V_j as soon as the
-    // softmax has written P_t,j, in block order per tile. A block's ring stage is released
-    // once both tiles' O += P V have read it.
+    // S_t,j as soon as block j is in shared memory and the tile's softmax has read S_t,j-2 (its
+    // buffer), and O_t += P_t,j V_j as soon as the softmax has written P_t,j, in block order
+    // per tile. A block's ring stage is released once both tiles' O += P V have read it.
     if (lane == 0) {
       constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
@@ -624,11 +623,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         bool progress = false;
 #pragma unroll
         for (int t = 0; t < kTcTiles; ++t) {
-          // S_t,j only after O_t += P_t,j-2 V_j-2 has been issued: then the completion of S_t,j
-          // implies that of every earlier O update of the tile, which keeps the softmax's
-          // parity waits on o_done and p_free at most one phase ahead
           const int jq = qk[t];
-          if (jq < n_sel && pv[t] >= jq - 1 && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
+          if (jq < n_sel && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
               (jq < 2 || mbar_test(&s_free[2 * t + (jq & 1)], ((jq - 2) >> 1) & 1))) {
             tc05::fence_after();
             const uint32_t kb = ring_addr + (jq % kTcStages) * kPaSlotBytes;
@@ -645,19 +641,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
             progress = true;
           }
           const int jp = pv[t];
-          const int pbi = kTcPBufs * t + jp % kTcPBufs;
-          if (jp < qk[t] && mbar_test(&p_full[pbi], (jp / kTcPBufs) & 1)) {
+          if (jp < qk[t] && mbar_test(&p_full[t], jp & 1)) {
             tc05::fence_after();
             const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
-            const uint32_t pb = p_addr + pbi * kTcPBytes;
+            const uint32_t pb = p_addr + t * kTcPBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
               const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
               tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
             }
-            tc05::commit(&o_done[t]);
-            tc05::commit(&p_free[pbi]);
+            tc05::commit(&pv_done[t]);
             pv[t] = jp + 1;
             progress = true;
           }
@@ -697,6 +691,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     int jreg0 = lane < n_sel ? a.idx[row * kslots + lane] : 0;
     int jreg1 = lane + 32 < n_sel ? a.idx[row * kslots + lane + 32] : 0;
     float m_used = -INFINITY, l = 0.f;
+    int pv_seen = 0;                                         // phases of pv_done waited for
     for (int j = 0; j < n_sel; ++j) {
       const int sb = 2 * t + (j & 1);
       int jb = __shfl_sync(0xffffffffu, j < 32 ? jreg0 : jreg1, j & 31);   // the block of S_j
@@ -715,12 +710,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
           sv[32 + e] = x1[e];
         }
       }
-      const int pbi = kTcPBufs * t + j % kTcPBufs;            // this block's P buffer
       tc05::fence_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&s_free[sb]);
       if (!ok) {
-        if (lane == 0) bar_arrive(&p_full[pbi]);
+        if (lane == 0) bar_arrive(&p_full[t]);
         continue;
       }
       // raw logits; the scale log2(e)/sqrt(d) > 0 is folded into the exponent below. Only the
@@ -744,11 +738,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       const bool grow = !first && mb > m_used + kRescaleLog2;
       if (__any_sync(0xffffffffu, grow)) {
         // O in tensor memory holds P_0..P_{j-1} V: rescale it once O += P_{j-1} V_{j-1} is done
-        // (O += P_{j-2} V_{j-2} was issued before S_j and is complete, so this parity wait is
-        // one phase ahead)
+        // (j >= 1 here; phase j-2 was waited for at block j-1)
         const float mn = fmaxf(m_used, mb);
         const float alpha = ex2_ftz(m_used - mn);
-        ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (j - 1) & 1, a.err));
+        ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (j - 1) & 1, a.err));
+        pv_seen = j;
         if (ok) {
           tc05::fence_after();
 #pragma unroll
@@ -776,11 +770,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         pk[e] = pack_bf16(p0, p1);
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P_t,j into its buffer once the O update that last read it (block j - kTcPBufs) is done
-      if (j >= kTcPBufs)
-        ok = __all_sync(0xffffffffu, sm_wait(&p_free[pbi], ((j - kTcPBufs) / kTcPBufs) & 1, a.err));
+      // P_t,j into the tile's buffer once O += P_{j-1} V_{j-1}, which read it last, is done
+      if (pv_seen < j) {
+        ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (j - 1) & 1, a.err));
+        pv_seen = j;
+      }
       if (ok) {
-        uint8_t* prow = pbuf + pbi * kTcPBytes + r * 128;
+        uint8_t* prow = pbuf + t * kTcPBytes + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
@@ -789,13 +785,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       fence_proxy_async_shared();
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&p_full[pbi]);
+      if (lane == 0) bar_arrive(&p_full[t]);
     }
-    // ---- epilogue: O / l of this row (token tok, head r % 16). O += P V of the last two
-    // blocks may both still be in flight (each is issued after the next block's S), so the
-    // waits go phase by phase: a parity wait is only unambiguous one phase ahead.
-    if (ok && n_sel > 1) ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (n_sel - 2) & 1, a.err));
-    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, sm_wait(&o_done[t], (n_sel - 1) & 1, a.err));
+    // ---- epilogue: O / l of this row (token tok, head r % 16), once the last O += P V is done
+    // (its phase n_sel-1 is the barrier's last; n_sel-2 was waited for at the last block)
+    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (n_sel - 1) & 1, a.err));
     if (ok && n_sel > 0) {
       tc05::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -803,6 +797,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         float o[32];
+        __syncwarp();                                          // tcgen05.ld is warp-aligned
         tc05::ld32(t_o + 32 * q4, o);
         tc05::wait_ld();
         if (tok < T) {
