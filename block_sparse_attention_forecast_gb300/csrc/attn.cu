@@ -1,5 +1,7 @@
 // Launch of the standalone block-sparse decode attention kernel; its per-CTA work is
-// attn_cta (attn_body.cuh), which the fused attend-and-select kernel (fused.cu) shares.
+// attn_cta (attn_body.cuh), which the fused attend-and-select kernel (fused.cu) shares. When
+// every (sequence, group) gets the same number (2 to 8) of CTAs, that number is the cluster
+// size and a group's partial results meet in distributed shared memory, not in the workspace.
 #include "attn_body.cuh"
 
 namespace sparda {
@@ -9,7 +11,19 @@ int attn_blocks_per_cta() { return 1; }   // workspace holds up to topk+2 partia
 __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
     const AttnArgs a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
     const __grid_constant__ CUtensorMap hk, const __grid_constant__ CUtensorMap hv) {
-  attn_cta(a, &mk, &mv, &hk, &hv, blockIdx.x, gridDim.x);
+  SPARDA_TL_ENTRY();
+  unsigned long long tl_first = 0;
+  attn_cta(a, &mk, &mv, &hk, &hv, blockIdx.x, gridDim.x, &tl_first);
+  SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlAttention, tl_first);
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_cluster_kernel(
+    const AttnArgs a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+    const __grid_constant__ CUtensorMap hk, const __grid_constant__ CUtensorMap hv) {
+  SPARDA_TL_ENTRY();
+  unsigned long long tl_first = 0;
+  attn_cta<true>(a, &mk, &mv, &hk, &hv, blockIdx.x, gridDim.x, &tl_first);
+  SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlAttention, tl_first);
 }
 
 int sm_count() {
@@ -25,21 +39,34 @@ int sm_count() {
   return n[dev];
 }
 
+constexpr int kAttnMaxCluster = 8;
+
 void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& hk, const CUtensorMap& hv, int bg_count,
                         cudaStream_t s) {
-  cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   AttnArgs b = a;
   b.n_units = bg_count * a.kslots;
-  int grid = b.n_units < sm_count() ? b.n_units : sm_count();
+  const int sms = sm_count();
+  int grid = b.n_units < sms ? b.n_units : sms;
+  int cluster = 0;
   // a whole number of CTAs per (sequence, group) when the groups fit the SMs: no CTA spans
-  // two groups
-  if (bg_count <= sm_count()) {
-    int sg = sm_count() / bg_count;
-    if (sg > a.kslots) sg = a.kslots;
+  // two groups. Up to 8 of them form one cluster, when the clusters still cover three
+  // quarters of the SMs (otherwise more CTAs per group, merged through the workspace).
+  if (bg_count <= sms) {
+    int sg = sms / bg_count;
+    if (sg > a.kslots) sg = a.kslots;   // every CTA has a unit (the cluster form relies on it)
+    const int sg_cl = sg < kAttnMaxCluster ? sg : kAttnMaxCluster;
+    if (sg_cl >= 2 && 4 * sg_cl * bg_count >= 3 * sms) {
+      sg = sg_cl;
+      cluster = sg;
+    }
     b.seg_per_group = sg;
     grid = sg * bg_count;
   }
+  b.tl_launch = timeline_next_launch();
+  b.tl_buf = timeline_buffer();
+  auto kern = cluster ? sparse_attn_cluster_kernel : sparse_attn_kernel;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   // Programmatic serialization: barrier set-up and the unit metadata overlap the append
   // before it in the stream; the producer waits for it before the first TMA load.
   cudaLaunchConfig_t cfg = {};
@@ -47,12 +74,16 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = kAttnSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, sparse_attn_kernel, b, mk, mv, hk, hv);
+  cfg.numAttrs = cluster ? 2 : 1;
+  cudaLaunchKernelEx(&cfg, kern, b, mk, mv, hk, hv);
 }
 
 }  // namespace sparda

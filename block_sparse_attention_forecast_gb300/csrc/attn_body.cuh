@@ -18,14 +18,19 @@
 // with P re-packed from the S accumulators.
 //
 // At the end of a (sequence, group) in its range a CTA merges its eight warps' partial
-// results through shared memory (one write, one read of a padded buffer). A group covered by one CTA is written out directly;
-// otherwise each covering CTA stores (O, max, sum) to the workspace and the last one to
-// arrive (a counter in the workspace, which it resets) merges them with log-sum-exp weights.
-// Because ranges are contiguous, that merge overlaps the producer's loads for the next group.
+// results through shared memory (one write, one read of a padded buffer). A group covered by
+// one CTA is written out directly. Otherwise, in the cluster form (kClusterMerge: the standalone
+// launch with a whole number of CTAs per group, each group one thread-block cluster), the CTAs
+// exchange their (O, max, sum) through distributed shared memory and each combines a share of
+// the heads; in the general form each covering CTA stores (O, max, sum) to the workspace and
+// the last one to arrive (a counter in the workspace, which it resets) merges them with
+// log-sum-exp weights. Because ranges are contiguous, that merge overlaps the producer's loads
+// for the next group.
 #pragma once
 
 #include "common.cuh"
 #include "kernels.h"
+#include "timeline.cuh"
 
 namespace sparda {
 
@@ -81,9 +86,14 @@ __device__ __forceinline__ GroupInfo group_info(const AttnArgs& a, int bg) {
 }
 
 // The work of CTA c of `grid` CTAs that share the attention units. The tensor maps live in
-// the calling kernel's parameter space.
+// the calling kernel's parameter space. kClusterMerge: CTA c is rank c % seg_per_group of a
+// cluster of seg_per_group CTAs that covers group c / seg_per_group (seg_per_group >= 2), and
+// every thread of the CTA reaches the two cluster barriers of the merge. tl_first (timeline
+// build only): thread 0 stores there the time its first block arrived.
+template <bool kClusterMerge = false>
 __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
-                                         const CUtensorMap* hk, const CUtensorMap* hv, int c, int grid) {
+                                         const CUtensorMap* hk, const CUtensorMap* hv, int c, int grid,
+                                         unsigned long long* tl_first = nullptr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -182,9 +192,17 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
             tma_load_2d(dst + kBlockBytes + kBlockBytes / 2, tv, 64, rr, &full[stage]);
           }
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {  // a wait ran out: no further loads
+          if constexpr (!kClusterMerge) return;
+          base = u1;
+          break;
+        }
         ++it;
       }
+    }
+    if constexpr (kClusterMerge) {
+      cluster_sync();                           // the consumers' two merge barriers
+      cluster_sync();
     }
     return;
   }
@@ -231,6 +249,9 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         const int stage = it % kStages;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kStages) & 1, a.err));
         if (!ok) continue;
+#ifdef SPARDA_TIMELINE
+        if (tid == 0 && tl_first && *tl_first == 0) *tl_first = tl_now();
+#endif
         const int j = stage_j[stage];
         const uint8_t* Kt = ring + stage * kSlotBytes;
         const uint8_t* Vt = Kt + kBlockBytes;
@@ -355,6 +376,70 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         Oh[4 * e + 2] += wt * x.z;
         Oh[4 * e + 3] += wt * x.w;
       }
+    }
+    if constexpr (kClusterMerge) {
+      // this CTA's (O, max, sum) into its own shared memory, then each CTA of the cluster
+      // combines the heads h with h % sg == its rank from all sg partials
+      consumer_sync();                         // the local merge has read its buffer
+      float* cO = mO;                          // [16 heads][128 dims]
+      float* cM = mM;                          // [16]
+      float* cL = mL;                          // [16]
+      float4* mine = reinterpret_cast<float4*>(cO + h * kHeadDim + d0);
+      mine[0] = make_float4(Oh[0], Oh[1], Oh[2], Oh[3]);
+      mine[1] = make_float4(Oh[4], Oh[5], Oh[6], Oh[7]);
+      if ((t & 15) == 0) {
+        cM[h] = Mh;
+        cL[h] = Lh;
+      }
+      cluster_sync();                          // #1: every partial of the group is visible
+      if (h % sg == (int)cluster_rank()) {
+        // four partials at a time, every load of a round issued before any is combined (slots
+        // past sg repeat rank 0 with weight 0), the rounds joined by log-sum-exp rescaling
+        constexpr int kRound = 4;
+        float acc[8], L = 0.f, M = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int q0 = 0; q0 < sg; q0 += kRound) {
+          float pm[kRound], pl[kRound];
+          float4 px[kRound][2];
+#pragma unroll
+          for (int q = 0; q < kRound; ++q) {
+            const bool in = q0 + q < sg;
+            const uint32_t r = in ? (uint32_t)(q0 + q) : 0u;
+            const float m = ld_cluster_f(&cM[h], r);
+            pm[q] = in ? m : -INFINITY;
+            pl[q] = ld_cluster_f(&cL[h], r);
+            px[q][0] = ld_cluster_f4(mine, r);
+            px[q][1] = ld_cluster_f4(mine + 1, r);
+          }
+          float Mn = M;
+#pragma unroll
+          for (int q = 0; q < kRound; ++q) Mn = fmaxf(Mn, pm[q]);
+          const float base = (Mn == -INFINITY) ? 0.f : Mn;
+          const float sc = exp2f(M - base);
+          L *= sc;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] *= sc;
+#pragma unroll
+          for (int q = 0; q < kRound; ++q) {
+            const float wt = exp2f(pm[q] - base);
+            L += wt * pl[q];
+            acc[0] += wt * px[q][0].x; acc[1] += wt * px[q][0].y;
+            acc[2] += wt * px[q][0].z; acc[3] += wt * px[q][0].w;
+            acc[4] += wt * px[q][1].x; acc[5] += wt * px[q][1].y;
+            acc[6] += wt * px[q][1].z; acc[7] += wt * px[q][1].w;
+          }
+          M = Mn;
+        }
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          pk[e] = pack_bf16(L > 0.f ? acc[2 * e] / L : 0.f, L > 0.f ? acc[2 * e + 1] / L : 0.f);
+        *reinterpret_cast<uint4*>(a.out + ((size_t)bg * kHeads + h) * kHeadDim + d0) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      cluster_sync();                          // #2: no CTA leaves while its partial may be read
+      continue;
     }
     const long long first = (long long)bg * a.kslots, last = first + a.kslots - 1;
     const int c_first = sg > 0 ? (c / sg) * sg : cta_of_unit(first, grid, U);

@@ -31,13 +31,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attend_and_select_kernel(
   grid_dep_launch();                   // the next prologue's projection may take freed SMs
   const int n_sel = (int)gridDim.x - n_attn;
   const bool attn = (int)blockIdx.x >= n_sel;
+  unsigned long long tl_first = 0;         // an attention CTA's first block (timeline build)
   if (attn)
-    attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x - n_sel, n_attn);
+    attn_cta(aa, &mk, &mv, &hk, &hv, blockIdx.x - n_sel, n_attn, &tl_first);
   else if (sa.queue)
     sel_cta_dyn(sa, blockIdx.x, n_sel);
   else
     sel_cta(sa, blockIdx.x, n_sel);
-  SPARDA_TL_EXIT(aa.tl_buf, aa.tl_launch, attn ? kTlAttention : kTlSelection, 0ull);
+  SPARDA_TL_EXIT(aa.tl_buf, aa.tl_launch, attn ? kTlAttention : kTlSelection, tl_first);
 }
 
 int sm_count();

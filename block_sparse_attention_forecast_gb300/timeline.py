@@ -16,6 +16,13 @@ release of the layer's prologue top-k:
   next_release the next prologue's top-k CTAs are released (the launch has completed)
 
 The workload is the benchmark's, with fewer layers (seeded synthetic K/V, 16 planted blocks).
+
+    python -m block_sparse_attention_forecast_gb300.timeline --attn-chain [--layers 32]
+
+instead times the standalone block-sparse decode attention alone, launched once per layer back
+to back from a CUDA graph (the step's own selections), and prints per launch its CTAs' phases in
+microseconds from the launch's first CTA entry: first block in shared memory (median, max) and
+exit (median, max), and the gap to the next launch's first entry.
 """
 from __future__ import annotations
 
@@ -38,6 +45,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--layers", type=int, default=6)
     ap.add_argument("--batch", type=int, default=16)
+    ap.add_argument("--attn-chain", action="store_true",
+                    help="time the standalone attention launched back to back, one launch per layer")
     args = ap.parse_args()
     from block_sparse_attention_forecast_gb300 import build
     os.environ["SPARDA_LIB"] = build.build(timeline=True)
@@ -53,6 +62,9 @@ def main():
     if args.batch != bench.BATCH:
         bench.BATCH = args.batch
     shape, stack, T0 = bench.build_workload("cuda:0", 0, 4, args.layers, "pipelined")
+    if args.attn_chain:
+        attn_chain(stack, read, sb, bench, torch)
+        return
     stack.advance = False
     stack.capture()
     for _ in range(3):
@@ -111,6 +123,48 @@ def main():
         r0 = p["release"]
         print("%5d  %8.2f  %8.2f  %7.2f  %12.2f" % (i, (p["topk_end"] - r0) / 1e3, (p["attn_end"] - r0) / 1e3,
                                                  (p["sel_end"] - r0) / 1e3, (q["release"] - r0) / 1e3))
+
+
+
+def attn_chain(stack, read, sb, bench, torch):
+    """The standalone attention of every layer, back to back in one CUDA graph."""
+    stack.advance = False
+    stack.run()                                       # every layer's selection
+    torch.cuda.synchronize()
+    sh, B, n = stack.shape, stack.batch, stack.n_layers
+
+    def loop(s):
+        for L in range(n):
+            sb.sparda_sparse_decode_attn(sh, stack.layers[L], stack.q[L], stack.idx[L], stack.cnt[L],
+                                         stack.seq_len, B, stack.out[L], stack.ws_attn, stream=s)
+    t = bench.graph_time(loop, 1)                     # captures and replays once more
+    cnt = ctypes.c_int32(0)
+    read(None, 0, ctypes.byref(cnt), 1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        loop(torch.cuda.current_stream())
+    read(None, 0, ctypes.byref(cnt), 1)               # the capture's own launches record nothing
+    g.replay()
+    torch.cuda.synchronize()
+    cap = 1 << 16
+    buf = (Rec * cap)()
+    assert read(ctypes.addressof(buf), cap, ctypes.byref(cnt), 1) == 0
+    by_launch = {}
+    for r in buf[:cnt.value]:
+        by_launch.setdefault(r.launch, []).append(r)
+    launches = sorted(by_launch)
+    print("%d launches, %.2f us per launch (graph replay, CUDA events)" % (n, t / n * 1e6))
+    print("launch  CTAs  first_block med/max  exit med/max  gap_to_next (us from the launch's first entry)")
+    for i, lid in enumerate(launches):
+        rs = by_launch[lid]
+        t0 = min(r.t_entry for r in rs)
+        first = np.array([(r.t_release - t0) / 1e3 for r in rs if r.t_release])
+        ex = np.array([(r.t_exit - t0) / 1e3 for r in rs])
+        gap = ""
+        if i + 1 < len(launches):
+            gap = "%.2f" % ((min(r.t_entry for r in by_launch[launches[i + 1]]) - max(r.t_exit for r in rs)) / 1e3)
+        print("%5d  %4d  %6.2f %6.2f  %6.2f %6.2f  %s" % (lid, len(rs), np.median(first) if len(first) else -1,
+                                                        first.max() if len(first) else -1, np.median(ex), ex.max(), gap))
 
 
 if __name__ == "__main__":

@@ -216,6 +216,49 @@ def test_sparse_attention(sb, T_list, k, max_ctx):
     _no_device_error(sb)
 
 
+# Batches whose groups split evenly over 2 to 8 CTAs run the merge of a group's partial
+# results in one thread-block cluster (distributed shared memory); batch 5 splits its groups
+# over 15 CTAs and merges through the workspace in two rounds. Ragged lengths give groups with
+# fewer selected blocks than CTAs (empty partials), and k = 1 three slots per group.
+@pytest.mark.parametrize("B,k,max_ctx", [(8, 32, 2048), (12, 16, 2048), (16, 32, 4096), (24, 8, 1024),
+                                         (32, 1, 1024), (5, 32, 4096)])
+def test_sparse_attention_split_groups(sb, B, k, max_ctx):
+    rng = np.random.default_rng(1000 + B)
+    T_list = [int(x) for x in rng.integers(1, max_ctx + 1, size=B)]
+    T_list[0], T_list[-1] = max_ctx, 1
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 71, B, k)
+    V = synth.normal_bf16((B, 2, max_ctx, 128), 72, B, k)
+    q = synth.normal_bf16((B, 32, 128), 73, B, k)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    layer.v.copy_(V.cuda())
+    idx = torch.full((B, 2, k + 2), -1, dtype=torch.int32)
+    cnt = torch.zeros((B, 2), dtype=torch.int32)
+    sels = {}
+    for b, T in enumerate(T_list):
+        nb = (T - 1) // 64 + 1
+        for g in range(2):
+            n = min(k + 2, nb) - int(rng.integers(0, 2))      # sometimes one slot short
+            sel = sorted(int(x) for x in rng.choice(nb, size=max(n, 1), replace=False))
+            sels[b, g] = sel
+            idx[b, g, :len(sel)] = torch.tensor(sel, dtype=torch.int32)
+            cnt[b, g] = len(sel)
+    out = torch.full((B, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sb.workspace(shape, B, sb.WS_ATTN)
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    for rep in range(2):                      # the second call finds the workspace counters reset
+        sb.sparda_sparse_decode_attn(shape, layer, q.cuda(), idx.cuda(), cnt.cuda(), seq, B, out, ws)
+        torch.cuda.synchronize()
+        o = to64(out)
+        for b, T in enumerate(T_list):
+            for g in range(2):
+                ref = O.block_sparse_attention(to64(q[b, 16 * g:16 * g + 16]), to64(K[b, g]),
+                                               to64(V[b, g]), sels[b, g], T)
+                check_attention(o[b, 16 * g:16 * g + 16], ref)
+    _no_device_error(sb)
+
+
 def test_attention_all_blocks_equals_dense(sb):
     T, max_ctx = 1000, 1024
     shape = sb.Shape(max_ctx=max_ctx, max_batch=1, topk=62)
