@@ -193,7 +193,6 @@ namespace {
 
 constexpr int kPaConsumerWarps = 8;
 constexpr int kPaThreads = (kPaConsumerWarps + 1) * 32;     // 8 consumer warps + producer
-constexpr int kPaSlotBytes = 2 * kBlockBytes;                // K + V of one block
 constexpr int kMhStages = 6;
 constexpr int kMhTileBytes = kBlockBytes;                    // 64 windows x 128 dims bf16
 // [align slack][barriers][ring][per-warp column sums, 2 buffers][top-k scratch][window sums]
@@ -426,26 +425,32 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 // ==================================================================== block-sparse attention, tcgen05
 // Causal block-sparse prefill attention on the fifth-generation tensor cores. A CTA holds two
 // query tiles of 128 rows (8 tokens x 16 heads each, row 16i + h), 16 tokens of one chunk,
-// which share every K/V block it loads:
-//   warp 0, one thread: TMA loads of the two Q tiles (once) and of the chunk's K/V blocks into
-//       a ring of full / empty mbarriers;
-//   warp 1: allocates the 512 tensor-memory columns (per tile an S double buffer of 2 x 64
-//       columns and an O of 128 columns) and, from one thread, issues per block j and tile t
-//       S_t,j = Q_t K_j^T (M 128, N 64, 8 K steps of 16) and O_t += P_t,j V_j (M 128, N 128,
-//       4 K steps; V read M/N-major), each completion signalled by tcgen05.commit on an
-//       mbarrier; a tile's S_j+1 is issued as soon as block j+1 is loaded and its S buffer has
-//       been read, ahead of O += P_j V_j, so the tensor cores work on one tile's S while the
-//       softmax of the other runs;
-//   warps 2-5 (tile 0) and 6-9 (tile 1), one thread per row (tensor-memory lane): load S_t,j,
-//       mask the keys after the token (the chunk's own block), an online softmax in the exp2
-//       domain whose running maximum is only moved (and O rescaled in tensor memory) when it
-//       grows by more than 2^8, P_t,j written to shared memory as bf16 in the 128-byte-swizzled
-//       K-major layout; at the end O / l to the output.
+// which share every K/V block it loads, and takes the chunk's selected blocks two at a time
+// (a pair: 128 keys; an odd last block is paired with itself, its second copy masked):
+//   warp 0, one thread: TMA loads of the two Q tiles (once) and of each pair's K and V into a
+//       2-stage ring of full / empty mbarriers (a stage: K and V of both blocks, the second
+//       block's rows after the first's, so that each pair is one 128-key operand);
+//   warp 1: allocates the 512 tensor-memory columns (per tile 128 columns of S, which P
+//       overwrites, and 128 of O) and, from one thread, issues per pair p and tile t
+//       S_t,p = Q_t K_p^T (M 128, N 128, 8 K steps of 16) and O_t += P_t,p V_p (M 128, N 128,
+//       8 K steps; P read from tensor memory, V M/N-major from shared memory), each completion
+//       signalled by tcgen05.commit on an mbarrier; S_t,p+1 is issued right after
+//       O_t += P_t,p V_p, whose read of P it must follow (one thread's tcgen05.mma run in issue
+//       order), so the tensor cores work on one tile while the other tile's softmax runs;
+//   warps 2-5 (tile 0) and 6-9 (tile 1), one thread per row (tensor-memory lane): the row
+//       maximum of S_t,p over the keys the token may see (the chunk's own block is masked
+//       after the token), an online softmax in the exp2 domain whose running maximum is only
+//       moved (and O rescaled in tensor memory) when it grows by more than 2^8, then P_t,p as
+//       bf16 pairs into the first 64 of S's columns (a second pass over S, block by block: P
+//       never overwrites S that is still unread); at the end O / l. The two tiles take turns
+//       (tile 1's softmax of pair p follows tile 0's, tile 0's of pair p+1 follows tile 1's of
+//       pair p), so each runs alone on the exponential and FMA units while the tensor cores
+//       run the other tile's O += P V and next S: the tensor pipe stays busy.
 // Every mbarrier phase a thread waits for can only be followed by the barrier's next phase
 // after that thread itself has arrived somewhere (a parity wait tells phase k from phase k+2
-// only if k+1 cannot have completed behind its back): the tile's one P buffer and its O are
-// both signalled by pv_done, whose phase j (O += P_j V_j complete) needs every softmax warp's
-// P_j, and each warp waits its phases in order, phase j-1 before it writes P_j.
+// only if k+1 cannot have completed behind its back): s_full's next phase needs the issuer
+// to have seen this warp's P, pv_done's next phase this warp's next P, a tile's turn
+// barrier's next phase the other tile's turn, and each warp waits pv_done's phases in order.
 namespace {
 // The softmax warps' waits: the library's bounded wait, or (SPARDA_TC_SPIN) a bounded loop of
 // try_wait without the suspend-time hint.
@@ -498,17 +503,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 constexpr int kTcTiles = 2;
 constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
 constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
-#ifndef SPARDA_TC_STAGES
-#define SPARDA_TC_STAGES 4
-#endif
 #ifndef SPARDA_TC_ISSUER_SLEEP
 #define SPARDA_TC_ISSUER_SLEEP 32                           // ns the MMA issuer sleeps when idle
 #endif
-constexpr int kTcStages = SPARDA_TC_STAGES;                 // K/V ring stages
+constexpr int kTcStages = 2;                                // ring stages, one pair each
+constexpr int kTcHalf = kBlockBytes / 2;                    // 64 rows x 64 dims of one block: 8 KiB
+constexpr int kTcPart = 2 * kTcHalf;                        // the pair's 128 rows of one 64-dim half
+constexpr int kTcStageBytes = 4 * kTcPart;                  // K lo, K hi, V lo, V hi: 64 KiB
 constexpr int kTcQBytes = 128 * kRowBytes;                  // 32 KiB per tile: 128 rows x 128 dims
-constexpr int kTcPBytes = 128 * kBlock * 2;                 // 16 KiB per tile: 128 x 64 keys
-constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcTiles * kTcQBytes + kTcStages * kPaSlotBytes +
-                        kTcTiles * kTcPBytes;
+constexpr int kTcSmem = 1024 /*align*/ + 1024 /*barriers*/ + kTcTiles * kTcQBytes + kTcStages * kTcStageBytes;
 static_assert(kTcSmem <= 227 * 1024, "the tcgen05 prefill attention fits shared memory");
 constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;
 constexpr uint32_t kTcCols = 512;
@@ -524,14 +527,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   uint64_t* q_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* kv_full = q_full + 1;                           // [stages]
   uint64_t* kv_empty = kv_full + kTcStages;                 // [stages]
-  uint64_t* s_full = kv_empty + kTcStages;                  // [tile][2]
-  uint64_t* s_free = s_full + 2 * kTcTiles;                 // [tile][2]
-  uint64_t* p_full = s_free + 2 * kTcTiles;                 // [tile]
+  uint64_t* s_full = kv_empty + kTcStages;                  // [tile]
+  uint64_t* p_full = s_full + kTcTiles;                     // [tile]
   uint64_t* pv_done = p_full + kTcTiles;                    // [tile]
-  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(pv_done + kTcTiles);
+  uint64_t* turn = pv_done + kTcTiles;                      // [tile]: its softmax of a pair done
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(turn + kTcTiles);
   uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
-  uint8_t* ring = qs + kTcTiles * kTcQBytes;
-  uint8_t* pbuf = ring + kTcStages * kPaSlotBytes;          // [tile] 16 KiB
+  uint8_t* ring = qs + kTcTiles * kTcQBytes;                // [stage] 64 KiB
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
@@ -546,6 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   const int kslots = a.topk + 2;
   const size_t row = (size_t)bg * a.nb_cap + c;
   const int n_sel = min(max(a.cnt[row], 0), kslots);
+  const int n_pairs = (n_sel + 1) / 2;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -553,13 +556,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2 * kTcTiles; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-    }
     for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);
       mbar_init(&pv_done[t], 1);
+      mbar_init(&turn[t], 4);
     }
     fence_mbar_init();
   }
@@ -588,75 +589,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         tma_load_2d(qt, &mq, 0, qr, q_full);
         tma_load_2d(qt + kTcQBytes / 2, &mq, 64, qr, q_full);
       }
-      for (int s = 0; s < n_sel && ok; ++s) {
-        int j = a.idx[row * kslots + s];
-        if (j < 0 || j > c) {
-          atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
-          j = 0;
-        }
-        const int stage = s % kTcStages;
-        if (s >= kTcStages) ok = mbar_wait(&kv_empty[stage], ((s / kTcStages) & 1) ^ 1, a.err);
+      for (int p = 0; p < n_pairs && ok; ++p) {
+        const int stage = p % kTcStages;
+        if (p >= kTcStages) ok = mbar_wait(&kv_empty[stage], ((p / kTcStages) & 1) ^ 1, a.err);
         if (!ok) break;
-        uint8_t* dst = ring + stage * kPaSlotBytes;
-        const int rr = bg * a.max_ctx + j * kBlock;
-        mbar_arrive_expect_tx(&kv_full[stage], kPaSlotBytes);
-        tma_load_2d(dst, &mk, 0, rr, &kv_full[stage]);
-        tma_load_2d(dst + kBlockBytes / 2, &mk, 64, rr, &kv_full[stage]);
-        tma_load_2d(dst + kBlockBytes, &mv, 0, rr, &kv_full[stage]);
-        tma_load_2d(dst + kBlockBytes + kBlockBytes / 2, &mv, 64, rr, &kv_full[stage]);
+        uint8_t* dst = ring + stage * kTcStageBytes;
+        mbar_arrive_expect_tx(&kv_full[stage], kTcStageBytes);
+        for (int h = 0; h < 2; ++h) {
+          const int s = min(2 * p + h, n_sel - 1);         // an odd last block is loaded twice
+          int j = a.idx[row * kslots + s];
+          if (j < 0 || j > c) {
+            atomicOr(a.err, SPARDA_DEV_BAD_INDEX);
+            j = 0;
+          }
+          const int rr = bg * a.max_ctx + j * kBlock;
+          tma_load_2d(dst + h * kTcHalf, &mk, 0, rr, &kv_full[stage]);
+          tma_load_2d(dst + kTcPart + h * kTcHalf, &mk, 64, rr, &kv_full[stage]);
+          tma_load_2d(dst + 2 * kTcPart + h * kTcHalf, &mv, 0, rr, &kv_full[stage]);
+          tma_load_2d(dst + 3 * kTcPart + h * kTcHalf, &mv, 64, rr, &kv_full[stage]);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread keeps the tensor cores fed: it polls the barriers and issues, for each tile,
-    // S_t,j as soon as block j is in shared memory and the tile's softmax has read S_t,j-2 (its
-    // buffer), and O_t += P_t,j V_j as soon as the softmax has written P_t,j, in block order
-    // per tile. A block's ring stage is released once both tiles' O += P V have read it.
+    // One thread keeps the tensor cores fed: it polls the barriers and issues, per tile,
+    // S_t,p as soon as pair p is in shared memory and O_t += P_t,p-1 V_p-1 has been issued,
+    // and O_t += P_t,p V_p as soon as the softmax has written P_t,p. A pair's ring stage is
+    // released once both tiles' O += P V have read it.
     if (lane == 0) {
-      constexpr uint32_t id_qk = tc05::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t id_qk = tc05::idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
-      const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring), p_addr = smem_addr(pbuf);
+      const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring);
       ok = mbar_wait(q_full, 0, a.err);
       int qk[kTcTiles] = {0}, pv[kTcTiles] = {0}, released = 0;
       uint32_t idle = 0;
-      while (ok && released < n_sel) {
+      while (ok && released < n_pairs) {
         bool progress = false;
 #pragma unroll
         for (int t = 0; t < kTcTiles; ++t) {
-          const int jq = qk[t];
-          if (jq < n_sel && mbar_test(&kv_full[jq % kTcStages], (jq / kTcStages) & 1) &&
-              (jq < 2 || mbar_test(&s_free[2 * t + (jq & 1)], ((jq - 2) >> 1) & 1))) {
+          const int pq = qk[t];
+          if (pq < n_pairs && pv[t] >= pq && mbar_test(&kv_full[pq % kTcStages], (pq / kTcStages) & 1)) {
             tc05::fence_after();
-            const uint32_t kb = ring_addr + (jq % kTcStages) * kPaSlotBytes;
+            const uint32_t kb = ring_addr + (pq % kTcStages) * kTcStageBytes;
             const uint32_t qa = q_addr + t * kTcQBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
               const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
-              const uint64_t db = tc05::smem_desc(kb + half * (kBlockBytes / 2) + off, 16, 1024);
-              tc05::mma_bf16_ss(tmem + (2 * t + (jq & 1)) * 64, da, db, id_qk, kk > 0 ? 1u : 0u);
+              const uint64_t db = tc05::smem_desc(kb + half * kTcPart + off, 16, 1024);
+              tc05::mma_bf16_ss(tmem + 256 * t, da, db, id_qk, kk > 0 ? 1u : 0u);
             }
-            tc05::commit(&s_full[2 * t + (jq & 1)]);
-            qk[t] = jq + 1;
+            tc05::commit(&s_full[t]);
+            qk[t] = pq + 1;
             progress = true;
           }
-          const int jp = pv[t];
-          if (jp < qk[t] && mbar_test(&p_full[t], jp & 1)) {
+          const int pp = pv[t];
+          if (pp < qk[t] && mbar_test(&p_full[t], pp & 1)) {
             tc05::fence_after();
-            const uint32_t vb = ring_addr + (jp % kTcStages) * kPaSlotBytes + kBlockBytes;
-            const uint32_t pb = p_addr + t * kTcPBytes;
+            const uint32_t vb = ring_addr + (pp % kTcStages) * kTcStageBytes + 2 * kTcPart;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t da = tc05::smem_desc(pb + kk * 32, 16, 1024);
-              const uint64_t db = tc05::smem_desc(vb + kk * 2048, kBlockBytes / 2, 1024);
-              tc05::mma_bf16_ss(tmem + 256 + 128 * t, da, db, id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t db = tc05::smem_desc(vb + kk * 2048, kTcPart, 1024);
+              tc05::mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk, db, id_pv,
+                                (pp > 0 || kk > 0) ? 1u : 0u);
             }
             tc05::commit(&pv_done[t]);
-            pv[t] = jp + 1;
+            pv[t] = pp + 1;
             progress = true;
           }
         }
-        // the ring stage of every block both tiles have finished with
+        // the ring stage of every pair both tiles have finished with
         int done_both = pv[0];
 #pragma unroll
         for (int t = 1; t < kTcTiles; ++t) done_both = min(done_both, pv[t]);
@@ -685,112 +687,128 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     const int tok = tok0 + 8 * t + (r >> 4);
     const float sl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
+    const uint32_t t_s = tmem + 256 * t + lane_off;          // S, then P
+    const uint32_t t_o = t_s + 128;
     // the chunk's block indices, lane i holding entries i and 32 + i (read before the loop: no
-    // global load on the per-block path)
+    // global load on the per-pair path)
     int jreg0 = lane < n_sel ? a.idx[row * kslots + lane] : 0;
     int jreg1 = lane + 32 < n_sel ? a.idx[row * kslots + lane + 32] : 0;
     float m_used = -INFINITY, l = 0.f;
-    int pv_seen = 0;                                         // phases of pv_done waited for
-    for (int j = 0; j < n_sel; ++j) {
-      const int sb = 2 * t + (j & 1);
-      int jb = __shfl_sync(0xffffffffu, j < 32 ? jreg0 : jreg1, j & 31);   // the block of S_j
-      if (jb < 0 || jb > c) jb = 0;
-      if (ok) ok = __all_sync(0xffffffffu, sm_wait(&s_full[sb], (j >> 1) & 1, a.err));
-      float sv[64];
-      if (ok) {
-        tc05::fence_after();
-        float x0[32], x1[32];
-        tc05::ld32(tmem + sb * 64 + lane_off, x0);
-        tc05::ld32(tmem + sb * 64 + lane_off + 32, x1);
-        tc05::wait_ld();
+    for (int p = 0; p < n_pairs; ++p) {
+      // the pair's two blocks; -1: the second copy of an odd last block (every key masked)
+      int jb[2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = x0[e];
-          sv[32 + e] = x1[e];
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int s = 2 * p + h;
+        const int j = __shfl_sync(0xffffffffu, s < 32 ? jreg0 : jreg1, s & 31);
+        jb[h] = s >= n_sel ? -1 : ((j < 0 || j > c) ? 0 : j);
       }
-      tc05::fence_before();
-      __syncwarp();
-      if (lane == 0) bar_arrive(&s_free[sb]);
+      if (ok) ok = __all_sync(0xffffffffu, sm_wait(&s_full[t], p & 1, a.err));
+      // the two tiles take turns: tile 1 runs its softmax of pair p after tile 0's, tile 0 its
+      // softmax of pair p after tile 1's of pair p-1, so that each runs alone on the SM's
+      // exponential and FMA units while the tensor cores work on the other tile
+      if (ok && (t == 1 || p > 0))
+        ok = __all_sync(0xffffffffu, sm_wait(&turn[1 - t], (t == 1 ? p : p - 1) & 1, a.err));
       if (!ok) {
-        if (lane == 0) bar_arrive(&p_full[t]);
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          bar_arrive(&p_full[t]);
+          bar_arrive(&turn[t]);
+        }
         continue;
       }
-      // raw logits; the scale log2(e)/sqrt(d) > 0 is folded into the exponent below. Only the
-      // chunk's own block has keys after some of the tile's tokens.
-      if (jb == c) {
-        const int kbase = jb * kBlock;
+      tc05::fence_after();
+      // pass 1: the row maximum over the keys this token may see, one block (64 columns) at a
+      // time. Only the chunk's own block has keys after some of the tile's tokens.
+      float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = (kbase + e <= tok) ? sv[e] : -INFINITY;
+      for (int h = 0; h < 2; ++h) {
+        const int j = jb[h];
+        if (j < 0) continue;                                   // warp-uniform
+        float x[64];
+        tc05::ld32(t_s + 64 * h, *reinterpret_cast<float(*)[32]>(x));
+        tc05::ld32(t_s + 64 * h + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        tc05::wait_ld();
+        if (j == c) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) x[e] = (j * kBlock + e <= tok) ? x[e] : -INFINITY;
+        }
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+        for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
+        mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
       }
-      // row max as a tree (six levels of independent fmax, not a 64-long chain)
-      float mx[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) mx[e] = fmaxf(sv[e], sv[e + 32]);
-#pragma unroll
-      for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-      const float mb = mx[0] * sl2;
-      // move the running max only when it grows by more than 2^8 (or on the first block)
+      const float mb = mx * sl2;
+      // every pair after the first: O += P_{p-1} V_{p-1} is complete (S_p was issued after it),
+      // and this warp takes pv_done's phase p-1 in turn
+      if (p > 0) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (p - 1) & 1, a.err));
+      // move the running max only when it grows by more than 2^8 (or on the first pair)
       const bool first = (m_used == -INFINITY);
       const bool grow = !first && mb > m_used + kRescaleLog2;
-      if (__any_sync(0xffffffffu, grow)) {
-        // O in tensor memory holds P_0..P_{j-1} V: rescale it once O += P_{j-1} V_{j-1} is done
-        // (j >= 1 here; phase j-2 was waited for at block j-1)
+      if (ok && __any_sync(0xffffffffu, grow)) {
         const float mn = fmaxf(m_used, mb);
         const float alpha = ex2_ftz(m_used - mn);
-        ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (j - 1) & 1, a.err));
-        pv_seen = j;
-        if (ok) {
-          tc05::fence_after();
+        tc05::fence_after();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            float o[32];
-            tc05::ld32(t_o + 32 * q4, o);
-            tc05::wait_ld();
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float o[32];
+          tc05::ld32(t_o + 32 * q4, o);
+          tc05::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tc05::st32(t_o + 32 * q4, o);
-          }
-          tc05::wait_st();
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc05::st32(t_o + 32 * q4, o);
         }
+        tc05::wait_st();
         l *= alpha;
         m_used = mn;
       } else if (first) {
         m_used = mb;
       }
-      uint32_t pk[32];
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent partial sums
+      // pass 2: P = 2^(s * log2(e)/sqrt(d) - m) as bf16 pairs into columns 32h .. 32h+31, after
+      // the S columns 64h .. 64h+63 they come from (and every S column below) have been read
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2_ftz(fmaf(sv[2 * e], sl2, -m_used)), p1 = ex2_ftz(fmaf(sv[2 * e + 1], sl2, -m_used));
-        ps[e & 7] += p0 + p1;
-        pk[e] = pack_bf16(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+        const int j = jb[h];
+        uint32_t pk[32];
+        if (j < 0) {                                           // warp-uniform
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = 0u;
+        } else {
+          float x[64];
+          tc05::ld32(t_s + 64 * h, *reinterpret_cast<float(*)[32]>(x));
+          tc05::ld32(t_s + 64 * h + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+          tc05::wait_ld();
+          if (j == c) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = (j * kBlock + e <= tok) ? x[e] : -INFINITY;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2_ftz(fmaf(x[2 * e], sl2, -m_used)), p1 = ex2_ftz(fmaf(x[2 * e + 1], sl2, -m_used));
+            ps[e & 7] += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+        }
+        tc05::st32(t_s + 32 * h, *reinterpret_cast<const float(*)[32]>(pk));
       }
+      tc05::wait_st();
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P_t,j into the tile's buffer once O += P_{j-1} V_{j-1}, which read it last, is done
-      if (pv_seen < j) {
-        ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (j - 1) & 1, a.err));
-        pv_seen = j;
-      }
-      if (ok) {
-        uint8_t* prow = pbuf + t * kTcPBytes + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_proxy_async_shared();
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&p_full[t]);
+      if (lane == 0) {
+        bar_arrive(&p_full[t]);
+        bar_arrive(&turn[t]);
+      }
     }
     // ---- epilogue: O / l of this row (token tok, head r % 16), once the last O += P V is done
-    // (its phase n_sel-1 is the barrier's last; n_sel-2 was waited for at the last block)
-    if (ok && n_sel > 0) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (n_sel - 1) & 1, a.err));
-    if (ok && n_sel > 0) {
+    // (its phase n_pairs-1 is the barrier's last; n_pairs-2 was waited for at the last pair)
+    if (ok && n_pairs > 0) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (n_pairs - 1) & 1, a.err));
+    if (ok && n_pairs > 0) {
       tc05::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(a.out + ((((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads + (r & 15)) * kHeadDim);
