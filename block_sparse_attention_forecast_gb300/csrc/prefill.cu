@@ -488,24 +488,9 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 #endif
 }
 
-// Non-blocking test of an mbarrier phase (the MMA issuer polls several barriers in turn).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
 constexpr int kTcTiles = 2;
 constexpr int kTcTokens = 8 * kTcTiles;                     // tokens per CTA
 constexpr int kTcSlices = kBlock / kTcTokens;               // CTAs per chunk
-#ifndef SPARDA_TC_ISSUER_SLEEP
-#define SPARDA_TC_ISSUER_SLEEP 32                           // ns the MMA issuer sleeps when idle
-#endif
 constexpr int kTcStages = 2;                                // ring stages, one pair each
 constexpr int kTcHalf = kBlockBytes / 2;                    // 64 rows x 64 dims of one block: 8 KiB
 constexpr int kTcPart = 2 * kTcHalf;                        // the pair's 128 rows of one 64-dim half
@@ -612,71 +597,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread keeps the tensor cores fed: it polls the barriers and issues, per tile,
-    // S_t,p as soon as pair p is in shared memory and O_t += P_t,p-1 V_p-1 has been issued,
-    // and O_t += P_t,p V_p as soon as the softmax has written P_t,p. A pair's ring stage is
-    // released once both tiles' O += P V have read it.
+    // One thread issues every MMA in the one order the softmax's turns fix: S_0,0 and S_1,0,
+    // then per pair p and tile t (0, then 1) O_t += P_t,p V_p once the softmax has written
+    // P_t,p, followed by S_t,p+1 once pair p+1 is in shared memory (after the O update that
+    // read P_t,p from the same columns: one thread's MMAs run in issue order). Each wait
+    // blocks on exactly the barrier it needs. A pair's ring stage is released once both
+    // tiles' O += P V have read it.
     if (lane == 0) {
       constexpr uint32_t id_qk = tc05::idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t id_pv = tc05::idesc_bf16(128, 128, 0, 1);
       const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring);
+      auto issue_qk = [&](int t, int pq) {
+        const uint32_t kb = ring_addr + (pq % kTcStages) * kTcStageBytes;
+        const uint32_t qa = q_addr + t * kTcQBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
+          const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
+          const uint64_t db = tc05::smem_desc(kb + half * kTcPart + off, 16, 1024);
+          tc05::mma_bf16_ss(tmem + 256 * t, da, db, id_qk, kk > 0 ? 1u : 0u);
+        }
+        tc05::commit(&s_full[t]);
+      };
       ok = mbar_wait(q_full, 0, a.err);
-      int qk[kTcTiles] = {0}, pv[kTcTiles] = {0}, released = 0;
-      uint32_t idle = 0;
-      while (ok && released < n_pairs) {
-        bool progress = false;
+      if (ok && n_pairs > 0) ok = mbar_wait(&kv_full[0], 0, a.err);
+      if (ok && n_pairs > 0) {
+        tc05::fence_after();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+      }
+      for (int pp = 0; ok && pp < n_pairs; ++pp) {
 #pragma unroll
         for (int t = 0; t < kTcTiles; ++t) {
-          const int pq = qk[t];
-          if (pq < n_pairs && pv[t] >= pq && mbar_test(&kv_full[pq % kTcStages], (pq / kTcStages) & 1)) {
+          ok = mbar_wait(&p_full[t], pp & 1, a.err);
+          if (!ok) break;
+          tc05::fence_after();
+          const uint32_t vb = ring_addr + (pp % kTcStages) * kTcStageBytes + 2 * kTcPart;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t db = tc05::smem_desc(vb + kk * 2048, kTcPart, 1024);
+            tc05::mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk, db, id_pv,
+                              (pp > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc05::commit(&pv_done[t]);
+          if (pp + 1 < n_pairs) {
+            const int pq = pp + 1;
+            ok = mbar_wait(&kv_full[pq % kTcStages], (pq / kTcStages) & 1, a.err);
+            if (!ok) break;
             tc05::fence_after();
-            const uint32_t kb = ring_addr + (pq % kTcStages) * kTcStageBytes;
-            const uint32_t qa = q_addr + t * kTcQBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
-              const uint64_t da = tc05::smem_desc(qa + half * (kTcQBytes / 2) + off, 16, 1024);
-              const uint64_t db = tc05::smem_desc(kb + half * kTcPart + off, 16, 1024);
-              tc05::mma_bf16_ss(tmem + 256 * t, da, db, id_qk, kk > 0 ? 1u : 0u);
-            }
-            tc05::commit(&s_full[t]);
-            qk[t] = pq + 1;
-            progress = true;
-          }
-          const int pp = pv[t];
-          if (pp < qk[t] && mbar_test(&p_full[t], pp & 1)) {
-            tc05::fence_after();
-            const uint32_t vb = ring_addr + (pp % kTcStages) * kTcStageBytes + 2 * kTcPart;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t db = tc05::smem_desc(vb + kk * 2048, kTcPart, 1024);
-              tc05::mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk, db, id_pv,
-                                (pp > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc05::commit(&pv_done[t]);
-            pv[t] = pp + 1;
-            progress = true;
+            issue_qk(t, pq);
           }
         }
-        // the ring stage of every pair both tiles have finished with
-        int done_both = pv[0];
-#pragma unroll
-        for (int t = 1; t < kTcTiles; ++t) done_both = min(done_both, pv[t]);
-        while (released < done_both) {
-          tc05::commit(&kv_empty[released % kTcStages]);
-          ++released;
-        }
-        if (progress) {
-          idle = 0;
-        } else {
-#if SPARDA_TC_ISSUER_SLEEP > 0
-          __nanosleep(SPARDA_TC_ISSUER_SLEEP);
-#endif
-          if (++idle > (kWaitPolls << 6)) {                  // ~0.5 s without progress
-            atomicOr(a.err, SPARDA_DEV_WAIT_TIMEOUT);
-            ok = false;
-          }
-        }
+        if (ok) tc05::commit(&kv_empty[pp % kTcStages]);   // both tiles' O += P V of pair pp
       }
     }
   } else {
@@ -719,57 +691,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         continue;
       }
       tc05::fence_after();
-      // pass 1: the row maximum over the keys this token may see, one block (64 columns) at a
-      // time. Only the chunk's own block has keys after some of the tile's tokens.
-      float mx = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = jb[h];
-        if (j < 0) continue;                                   // warp-uniform
-        float x[64];
-        tc05::ld32(t_s + 64 * h, *reinterpret_cast<float(*)[32]>(x));
-        tc05::ld32(t_s + 64 * h + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-        tc05::wait_ld();
-        if (j == c) {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) x[e] = (j * kBlock + e <= tok) ? x[e] : -INFINITY;
-        }
-        float m8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m8[e] = x[e];
-#pragma unroll
-        for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
-        mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
-      }
-      const float mb = mx * sl2;
-      // every pair after the first: O += P_{p-1} V_{p-1} is complete (S_p was issued after it),
-      // and this warp takes pv_done's phase p-1 in turn
-      if (p > 0) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (p - 1) & 1, a.err));
-      // move the running max only when it grows by more than 2^8 (or on the first pair)
-      const bool first = (m_used == -INFINITY);
-      const bool grow = !first && mb > m_used + kRescaleLog2;
-      if (ok && __any_sync(0xffffffffu, grow)) {
-        const float mn = fmaxf(m_used, mb);
-        const float alpha = ex2_ftz(m_used - mn);
-        tc05::fence_after();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float o[32];
-          tc05::ld32(t_o + 32 * q4, o);
-          tc05::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tc05::st32(t_o + 32 * q4, o);
-        }
-        tc05::wait_st();
-        l *= alpha;
-        m_used = mn;
-      } else if (first) {
-        m_used = mb;
-      }
-      // pass 2: P = 2^(s * log2(e)/sqrt(d) - m) as bf16 pairs into columns 32h .. 32h+31, after
-      // the S columns 64h .. 64h+63 they come from (and every S column below) have been read
+      // One pass over S, block by block: the block's row maximum over the keys this token may
+      // see (only the chunk's own block has keys after some of the tile's tokens), then its P
+      // into columns 32h .. 32h+31, after the S columns 64h .. 64h+63 it comes from (and every
+      // S column below) have been read. The running maximum moves only on the first block or
+      // when it grows by more than 2^8; then O (which holds P_{p-1} V_{p-1} once pv_done's
+      // phase p-1 is in) and, on the pair's second block, the first block's P are rescaled.
+      bool pv_waited = (p == 0);
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -787,6 +715,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
 #pragma unroll
             for (int e = 0; e < 64; ++e) x[e] = (j * kBlock + e <= tok) ? x[e] : -INFINITY;
           }
+          float m8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+          for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
+          const float mb = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;
+          const bool first = (m_used == -INFINITY);
+          const bool grow = first || mb > m_used + kRescaleLog2;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float mn = grow ? (first ? mb : fmaxf(m_used, mb)) : m_used;
+            const float alpha = first ? 0.f : ex2_ftz(m_used - mn);
+            if (!pv_waited) {
+              // O += P_{p-1} V_{p-1} is complete (S_p was issued after it): take the phase
+              ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (p - 1) & 1, a.err)) && ok;
+              pv_waited = true;
+              tc05::fence_after();
+            }
+            if (p > 0) {                                       // O holds earlier pairs
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                float o[32];
+                tc05::ld32(t_o + 32 * q4, o);
+                tc05::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                tc05::st32(t_o + 32 * q4, o);
+              }
+            }
+            if (h == 1 && jb[0] >= 0) {                        // the first block's P, written
+              float pa[32];
+              tc05::wait_st();                                 // (its store is complete)
+              tc05::ld32(t_s, pa);
+              tc05::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const uint32_t u = __float_as_uint(pa[e]);
+                pa[e] = __uint_as_float(pack_bf16(__uint_as_float(u << 16) * alpha,
+                                                  __uint_as_float(u & 0xffff0000u) * alpha));
+              }
+              tc05::st32(t_s, pa);
+            }
+            tc05::wait_st();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ps[e] *= alpha;
+            l *= alpha;
+            m_used = mn;
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float p0 = ex2_ftz(fmaf(x[2 * e], sl2, -m_used)), p1 = ex2_ftz(fmaf(x[2 * e + 1], sl2, -m_used));
@@ -798,6 +774,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       }
       tc05::wait_st();
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      // pv_done's phase p-1 in turn (long complete) before this warp's P_p can complete phase p
+      if (!pv_waited) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (p - 1) & 1, a.err)) && ok;
       tc05::fence_before();
       __syncwarp();
       if (lane == 0) {
