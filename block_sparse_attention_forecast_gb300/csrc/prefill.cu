@@ -442,15 +442,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const 
 //       after the token), an online softmax in the exp2 domain whose running maximum is only
 //       moved (and O rescaled in tensor memory) when it grows by more than 2^8, then P_t,p as
 //       bf16 pairs into the first 64 of S's columns (a second pass over S, block by block: P
-//       never overwrites S that is still unread); at the end O / l. The two tiles take turns
-//       (tile 1's softmax of pair p follows tile 0's, tile 0's of pair p+1 follows tile 1's of
-//       pair p), so each runs alone on the exponential and FMA units while the tensor cores
-//       run the other tile's O += P V and next S: the tensor pipe stays busy.
+//       never overwrites S that is still unread); at the end O / l.
 // Every mbarrier phase a thread waits for can only be followed by the barrier's next phase
 // after that thread itself has arrived somewhere (a parity wait tells phase k from phase k+2
 // only if k+1 cannot have completed behind its back): s_full's next phase needs the issuer
-// to have seen this warp's P, pv_done's next phase this warp's next P, a tile's turn
-// barrier's next phase the other tile's turn, and each warp waits pv_done's phases in order.
+// to have seen this warp's P, pv_done's next phase this warp's next P, and each warp waits
+// pv_done's phases in order.
 namespace {
 // The softmax warps' waits: the library's bounded wait, or (SPARDA_TC_SPIN) a bounded loop of
 // try_wait without the suspend-time hint.
@@ -515,8 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   uint64_t* s_full = kv_empty + kTcStages;                  // [tile]
   uint64_t* p_full = s_full + kTcTiles;                     // [tile]
   uint64_t* pv_done = p_full + kTcTiles;                    // [tile]
-  uint64_t* turn = pv_done + kTcTiles;                      // [tile]: its softmax of a pair done
-  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(turn + kTcTiles);
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(pv_done + kTcTiles);
   uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
   uint8_t* ring = qs + kTcTiles * kTcQBytes;                // [stage] 64 KiB
 
@@ -545,7 +541,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);
       mbar_init(&pv_done[t], 1);
-      mbar_init(&turn[t], 4);
     }
     fence_mbar_init();
   }
@@ -597,8 +592,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues every MMA in the one order the softmax's turns fix: S_0,0 and S_1,0,
-    // then per pair p and tile t (0, then 1) O_t += P_t,p V_p once the softmax has written
+    // One thread issues every MMA in one fixed order: S_0,0 and S_1,0, then per pair p and
+    // tile t (0, then 1) O_t += P_t,p V_p once the softmax has written
     // P_t,p, followed by S_t,p+1 once pair p+1 is in shared memory (after the O update that
     // read P_t,p from the same columns: one thread's MMAs run in issue order). Each wait
     // blocks on exactly the barrier it needs. A pair's ring stage is released once both
@@ -676,18 +671,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
         jb[h] = s >= n_sel ? -1 : ((j < 0 || j > c) ? 0 : j);
       }
       if (ok) ok = __all_sync(0xffffffffu, sm_wait(&s_full[t], p & 1, a.err));
-      // the two tiles take turns: tile 1 runs its softmax of pair p after tile 0's, tile 0 its
-      // softmax of pair p after tile 1's of pair p-1, so that each runs alone on the SM's
-      // exponential and FMA units while the tensor cores work on the other tile
-      if (ok && (t == 1 || p > 0))
-        ok = __all_sync(0xffffffffu, sm_wait(&turn[1 - t], (t == 1 ? p : p - 1) & 1, a.err));
       if (!ok) {
         tc05::fence_before();
         __syncwarp();
-        if (lane == 0) {
-          bar_arrive(&p_full[t]);
-          bar_arrive(&turn[t]);
-        }
+        if (lane == 0) bar_arrive(&p_full[t]);
         continue;
       }
       tc05::fence_after();
@@ -778,10 +765,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
       if (!pv_waited) ok = __all_sync(0xffffffffu, sm_wait(&pv_done[t], (p - 1) & 1, a.err)) && ok;
       tc05::fence_before();
       __syncwarp();
-      if (lane == 0) {
-        bar_arrive(&p_full[t]);
-        bar_arrive(&turn[t]);
-      }
+      if (lane == 0) bar_arrive(&p_full[t]);
     }
     // ---- epilogue: O / l of this row (token tok, head r % 16), once the last O += P V is done
     // (its phase n_pairs-1 is the barrier's last; n_pairs-2 was waited for at the last pair)
