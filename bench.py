@@ -73,7 +73,7 @@ KERNEL_SOURCES = {
                           "timeline.cuh"),
     "decode_prologue": ("prologue.cu", "append_body.cuh", "project_body.cuh", "topk.cuh", "common.cuh",
                         "kernels.h", "timeline.cuh"),
-    "sparse_decode_attn": ("attn.cu", "attn_body.cuh", "common.cuh", "kernels.h"),
+    "sparse_decode_attn": ("attn.cu", "attn_body.cuh", "common.cuh", "kernels.h", "timeline.cuh"),
     "forecast_select": ("select.cu", "select_body.cuh", "topk.cuh", "common.cuh", "kernels.h"),
 }
 
