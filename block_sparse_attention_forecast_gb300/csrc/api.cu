@@ -609,9 +609,13 @@ int32_t sparda_prefill_multihead_select(const sparda_shape* s, const void* ck, c
   PrefillArgs a;
   SPARDA_TRY(prepare_prefill(s, ck, q, seq_len, batch, idx, cnt, ws, ws_bytes, &a));
   a.q = static_cast<const __nv_bfloat16*>(q);
-  CUtensorMap mck;
+  const uint64_t rows = (uint64_t)s->max_batch * s->n_groups * s->max_ctx;
+  // every query row must fit a signed 32-bit TMA coordinate
+  if (rows * kHeads >= ((uint64_t)1 << 31)) return SPARDA_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap mck, mq;
   SPARDA_TRY(make_kv_map(&mck, ck, (uint64_t)s->max_batch * s->n_groups * w_cap(s)));
-  launch_prefill_multihead_select(a, mck, batch, static_cast<cudaStream_t>(stream));
+  SPARDA_TRY(make_kv_map(&mq, q, rows * kHeads, 16));
+  launch_prefill_multihead_select(a, mq, mck, batch, static_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 

@@ -173,7 +173,9 @@ struct PrefillArgs {
   int G, W_cap, max_ctx, nb_cap, topk;
 };
 void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s);
-void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mck, int batch, cudaStream_t s);
+// mq: the queries [B*max_ctx*G*16 rows, 128] in boxes of 16 rows; mck: the compressed keys.
+void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mck, int batch,
+                                     cudaStream_t s);
 // the causal block-sparse prefill attention on tcgen05 tensor cores; mq: the queries as
 // [rows, 128] in 64 x 16 boxes, mk / mv: the layer's K and V as [rows, 128] in 64 x 64 boxes
 void launch_prefill_attn_tc(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,

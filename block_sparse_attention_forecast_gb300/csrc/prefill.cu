@@ -188,240 +188,6 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const Prefil
               c * kBlock + 1, sh);
 }
 
-// ==================================================================== tensor-core helpers
-namespace {
-
-constexpr int kPaConsumerWarps = 8;
-constexpr int kPaThreads = (kPaConsumerWarps + 1) * 32;     // 8 consumer warps + producer
-constexpr int kMhStages = 6;
-constexpr int kMhTileBytes = kBlockBytes;                    // 64 windows x 128 dims bf16
-// [align slack][barriers][ring][per-warp column sums, 2 buffers][top-k scratch][window sums]
-constexpr int kMhFixedSmem = 1024 + 1024 + kMhStages * kMhTileBytes + 2 * kPaConsumerWarps * 64 * 4 +
-                             ((int)sizeof(TopkShared) + 15) / 16 * 16;
-__host__ __device__ constexpr int mh_smem_bytes(int w_cap) { return kMhFixedSmem + 4 * w_cap; }
-static_assert(mh_smem_bytes(kMaxCtx / kWinStride) <= 227 * 1024, "the baseline prefill selector fits shared memory");
-
-// Shared address of 16-byte chunk `chunk` (0..15 over the 128 dims) of row r of a 64-row
-// tile staged by TMA as two 64-column halves with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t swz_addr(const uint8_t* tile, int r, int chunk) {
-  return smem_addr(tile + (chunk >> 3) * (kBlockBytes / 2) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kPaConsumerWarps * 32) : "memory");
-}
-
-// The A fragments of one token's 16 query heads (rows = heads, k = dims), from global memory.
-__device__ __forceinline__ void load_q_frags(const __nv_bfloat16* q16, int lane, uint32_t (&qf)[8][4]) {
-  const int g = lane >> 2, cq = lane & 3;
-  const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q16 + (size_t)g * kHeadDim);
-  const uint32_t* q1 = q0 + 8 * (kHeadDim / 2);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    qf[ks][0] = q0[8 * ks + cq];
-    qf[ks][1] = q1[8 * ks + cq];
-    qf[ks][2] = q0[8 * ks + 4 + cq];
-    qf[ks][3] = q1[8 * ks + 4 + cq];
-  }
-}
-
-// S[16 heads x 64 rows of the tile] = Q . tile^T; sc[n] is n-tile n (rows 8n .. 8n+7 of the
-// tile) in the m16n8 accumulator layout.
-__device__ __forceinline__ void qk_tile(const uint32_t (&qf)[8][4], const uint8_t* tile, int lane, float (&sc)[8][4]) {
-#pragma unroll
-  for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-  const int hi = (lane >> 3) & 1;
-#pragma unroll
-  for (int wq = 0; wq < 4; ++wq) {
-    const int r = 16 * wq + (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(swz_addr(tile, r, 2 * ks + hi), b0, b1, b2, b3);
-      mma_16816(sc[2 * wq], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-      mma_16816(sc[2 * wq + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-    }
-  }
-}
-
-}  // namespace
-
-// ==================================================================== baseline multi-head
-__global__ void __launch_bounds__(kPaThreads, 1) prefill_multihead_kernel(const PrefillArgs a,
-                                                                          const __grid_constant__ CUtensorMap mck) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMhStages;
-  uint8_t* ring = smem + 1024;
-  float* part = reinterpret_cast<float*>(ring + kMhStages * kMhTileBytes);    // [2][8 warps][64]
-  TopkShared& sh = *reinterpret_cast<TopkShared*>(part + 2 * kPaConsumerWarps * 64);
-  float* win_sum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sh) +
-                                            ((int)sizeof(TopkShared) + 15) / 16 * 16);   // [W_cap]
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
-  const int c = a.nb_cap - 1 - (int)blockIdx.x;                // the longest chunks first
-  const int T = a.seq_len[b];
-  const int kslots = a.topk + 2;
-  const size_t row = (size_t)bg * a.nb_cap + c;
-  if (!valid_len(T, a.max_ctx) || c * kBlock >= T) {
-    if (!valid_len(T, a.max_ctx) && tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
-    for (int s = tid; s < kslots; s += blockDim.x) a.idx[row * kslots + s] = -1;
-    if (tid == 0) a.cnt[row] = 0;
-    return;
-  }
-  const int Wc = num_windows(c * kBlock);
-  const int n_wt = (Wc + 63) / 64;
-  const int n_tok = min(kBlock, T - c * kBlock);
-  const int n_sl = (n_tok + kPaConsumerWarps - 1) / kPaConsumerWarps;
-  const int n_loads = n_sl * 2 * n_wt;                           // slices x passes x tiles
-
-  if (tid == 0) {
-    for (int i = 0; i < kMhStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPaConsumerWarps);
-    }
-    fence_mbar_init();
-  }
-  for (int i = tid; i < Wc; i += blockDim.x) win_sum[i] = 0.f;
-  __syncthreads();
-
-  if (warp == kPaConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&mck);
-      for (int it = 0; it < n_loads; ++it) {
-        const int m = it % n_wt;
-        const int stage = it % kMhStages;
-        if (it >= kMhStages && !mbar_wait(&empty[stage], ((it / kMhStages) & 1) ^ 1, a.err)) break;
-        uint8_t* dst = ring + stage * kMhTileBytes;
-        const int rr = bg * a.W_cap + m * 64;
-        mbar_arrive_expect_tx(&full[stage], kMhTileBytes);
-        tma_load_2d(dst, &mck, 0, rr, &full[stage]);
-        tma_load_2d(dst + kBlockBytes / 2, &mck, 64, rr, &full[stage]);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int cq = lane & 3;
-    const float zl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-    bool ok = true;
-    int it = 0, tile_no = 0;
-    for (int s = 0; s < n_sl; ++s) {
-      const int tok = c * kBlock + s * kPaConsumerWarps + warp;
-      const bool active = tok < T;
-      uint32_t qf[8][4];
-      if (active) {
-        load_q_frags(a.q + (((size_t)b * a.max_ctx + tok) * a.G + g) * kHeads * kHeadDim, lane, qf);
-      }
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      for (int pass = 0; pass < 2; ++pass) {
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-        for (int m = 0; m < n_wt; ++m, ++it) {
-          const int stage = it % kMhStages;
-          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (it / kMhStages) & 1, a.err));
-          float sc[8][4];
-          if (ok && active) {
-            qk_tile(qf, ring + stage * kMhTileBytes, lane, sc);
-            const int ibase = m * 64 + 2 * cq;
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                sc[n][e] = (ibase + 8 * n + (e & 1)) < Wc ? sc[n][e] * zl2 : -INFINITY;
-          }
-          __syncwarp();
-          if (lane == 0) bar_arrive(&empty[stage]);
-          if (pass == 0) {
-            if (ok && active) {
-              float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-              for (int n = 0; n < 8; ++n) {
-                mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-                mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-              }
-              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-              const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-              const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-              const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-              float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-              for (int n = 0; n < 8; ++n) {
-                ps0 += exp2f(sc[n][0] - base0) + exp2f(sc[n][1] - base0);
-                ps1 += exp2f(sc[n][2] - base1) + exp2f(sc[n][3] - base1);
-              }
-              ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-              ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-              ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-              ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-              l0 = l0 * exp2f(m0 - base0) + ps0;
-              l1 = l1 * exp2f(m1 - base1) + ps1;
-              m0 = mn0;
-              m1 = mn1;
-            }
-          } else {
-            // normalised probabilities summed over this token's 16 heads, per window
-            float cs[8][2];
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-              cs[n][0] = cs[n][1] = 0.f;
-              if (ok && active) {
-                const float b0 = (m0 == -INFINITY) ? 0.f : m0, b1 = (m1 == -INFINITY) ? 0.f : m1;
-                cs[n][0] = exp2f(sc[n][0] - b0) * inv0 + exp2f(sc[n][2] - b1) * inv1;
-                cs[n][1] = exp2f(sc[n][1] - b0) * inv0 + exp2f(sc[n][3] - b1) * inv1;
-              }
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 4);
-                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 8);
-                cs[n][e] += __shfl_xor_sync(0xffffffffu, cs[n][e], 16);
-              }
-            }
-            float* pw = part + ((tile_no & 1) * kPaConsumerWarps + warp) * 64;
-            if (lane < 4) {
-#pragma unroll
-              for (int n = 0; n < 8; ++n) {
-                pw[8 * n + 2 * lane] = cs[n][0];
-                pw[8 * n + 2 * lane + 1] = cs[n][1];
-              }
-            }
-            consumers_sync();
-            // the eight tokens' sums, added in warp order into the chunk's window sums
-            if (tid < 64) {
-              const float* pb = part + (tile_no & 1) * kPaConsumerWarps * 64;
-              float acc = 0.f;
-#pragma unroll
-              for (int w = 0; w < kPaConsumerWarps; ++w) acc += pb[w * 64 + tid];
-              const int i = m * 64 + tid;
-              if (i < Wc) win_sum[i] += acc;
-            }
-            ++tile_no;
-          }
-        }
-      }
-    }
-    consumers_sync();
-    // max-pool onto blocks j <= c (windows 4j-1 .. 4j+3 below Wc), then the top-k
-    float* S = a.block_scores + row * a.nb_cap;
-    for (int j = tid; j <= c; j += kPaConsumerWarps * 32) {
-      float v = -INFINITY;
-      for (int i = max(0, 4 * j - 1); i <= min(Wc - 1, 4 * j + 3); ++i) v = fmaxf(v, win_sum[i]);
-      S[j] = v;
-    }
-    __threadfence_block();
-    consumers_sync();
-    topk_select(S, a.idx + row * kslots, a.cnt + row, a.topk, a.max_ctx, c * kBlock + 1, sh);
-  }
-}
-
 // ==================================================================== block-sparse attention, tcgen05
 // Causal block-sparse prefill attention on the fifth-generation tensor cores. A CTA holds two
 // query tiles of 128 rows (8 tokens x 16 heads each, row 16i + h), 16 tokens of one chunk,
@@ -469,6 +235,10 @@ __device__ __forceinline__ bool sm_wait(uint64_t* bar, uint32_t parity, int* err
 #else
   return mbar_wait(bar, parity, err);
 #endif
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // 2^x by the PTX instruction ex2.approx.ftz.f32 (one MUFU operation; the PTX ISA bounds its
@@ -800,6 +570,315 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const Pr
   }
 }
 
+// ==================================================================== baseline multi-head, tcgen05
+// The baseline chunk selector on the fifth-generation tensor cores. One CTA per (sequence-
+// group, chunk), the longest chunks first. The chunk's 1024 query rows (64 tokens x 16 heads)
+// are taken two 128-row tiles at a time (a tile: 8 tokens, row 16i + h; an odd last tile is
+// paired with a tile of rows past the prompt, which count for nothing). For each pair, two
+// passes over the chunk's windows, 128 at a time:
+//   warp 0, one thread: TMA loads of the pair's Q tiles (once per pair, after the pair before
+//       has been read) and of each 128-window tile of compressed keys into a ring;
+//   warp 1: allocates 512 tensor-memory columns (per tile an S double buffer of 2 x 128) and,
+//       from one thread, issues per window tile and query tile S = Q CK^T (M 128, N 128, 8 K
+//       steps), each completion signalled by tcgen05.commit;
+//   warps 2-9, one thread per row: pass 1 keeps the row's running maximum and sum of
+//       2^(s - max) over the windows (logits scaled by log2(e)/sqrt(d)); pass 2 forms
+//       p = 2^(s - max) / sum and sums it over the rows: within a warp by a butterfly that
+//       leaves lane l the sums of windows 2l, 2l+1 of each 64, then over the eight warps in a
+//       fixed order into the chunk's window sums in shared memory.
+// Then the max-pool onto blocks and the exact top-k, as in the Forecast selector. Every wait
+// is bounded; each parity wait can only be followed by the barrier's next phase after the
+// waiting thread has itself arrived somewhere.
+namespace {
+constexpr int kMtTiles = 2;
+constexpr int kMtWin = 128;                                 // windows per S tile
+constexpr int kMtCkBytes = kMtWin * kRowBytes;              // 32 KiB
+constexpr int kMtQBytes = 128 * kRowBytes;                  // 32 KiB per query tile
+constexpr int kMtThreads = (2 + 4 * kMtTiles) * 32;         // 320
+constexpr int kMtPartFloats = 2 * 4 * kMtTiles * kMtWin;    // [2 buffers][8 warps][128 windows]
+constexpr uint32_t kMtCols = 512;
+static_assert((int)sizeof(TopkShared) <= kMtTiles * kMtQBytes, "the top-k scratch fits over the query tiles");
+// [align slack][barriers][Q tiles][ring][column sums][window sums]
+__host__ __device__ constexpr int mt_smem_bytes(int w_cap, int stages) {
+  return 1024 + 1024 + kMtTiles * kMtQBytes + stages * kMtCkBytes + kMtPartFloats * 4 + (4 * w_cap + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int mt_stages(int w_cap) { return mt_smem_bytes(w_cap, 3) <= 227 * 1024 ? 3 : 2; }
+static_assert(mt_smem_bytes(kMaxCtx / kWinStride, 2) <= 227 * 1024, "the baseline prefill selector fits shared memory");
+
+// Sum of v over the 32 lanes, per index: lane l gets the sums of entries 2l and 2l+1 (a
+// transposing butterfly: each step a lane keeps one half of its entries, adds the partner's
+// copy of that half, and hands the other half over).
+__device__ __forceinline__ void lane_colsum64(float (&v)[64], int lane, float& s0, float& s1) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool up = lane & 16;
+    const float give = up ? v[i] : v[i + 32];
+    const float keep = up ? v[i + 32] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool up = lane & 8;
+    const float give = up ? v[i] : v[i + 16];
+    const float keep = up ? v[i + 16] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool up = lane & 4;
+    const float give = up ? v[i] : v[i + 8];
+    const float keep = up ? v[i + 8] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 2;
+    const float give = up ? v[i] : v[i + 4];
+    const float keep = up ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 2);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 1;
+    const float give = up ? v[i] : v[i + 2];
+    const float keep = up ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 1);
+  }
+  s0 = v[0];
+  s1 = v[1];
+}
+
+__device__ __forceinline__ void mt_softmax_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(4 * kMtTiles * 32) : "memory");
+}
+}  // namespace
+
+__global__ void __launch_bounds__(kMtThreads, 1) prefill_multihead_tc_kernel(const PrefillArgs a, int n_st,
+                                                                            const __grid_constant__ CUtensorMap mq,
+                                                                            const __grid_constant__ CUtensorMap mck) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* q_free = q_full + 1;
+  uint64_t* kv_full = q_free + 1;                           // [stages]
+  uint64_t* kv_empty = kv_full + 3;                         // [stages]
+  uint64_t* s_full = kv_empty + 3;                          // [tile][2]
+  uint64_t* s_free = s_full + 2 * kMtTiles;                 // [tile][2]
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(s_free + 2 * kMtTiles);
+  uint8_t* qs = smem + 1024;                                // [tile] 32 KiB
+  uint8_t* ring = qs + kMtTiles * kMtQBytes;                // [stage] 32 KiB
+  float* part = reinterpret_cast<float*>(ring + n_st * kMtCkBytes);   // [2][8 warps][128]
+  float* win_sum = part + kMtPartFloats;                    // [W_cap]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bg = blockIdx.y, b = bg / a.G, g = bg % a.G;
+  const int c = a.nb_cap - 1 - (int)blockIdx.x;               // the longest chunks first
+  const int T = a.seq_len[b];
+  const int kslots = a.topk + 2;
+  const size_t row = (size_t)bg * a.nb_cap + c;
+  if (!valid_len(T, a.max_ctx) || c * kBlock >= T) {
+    if (!valid_len(T, a.max_ctx) && tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
+    for (int s = tid; s < kslots; s += blockDim.x) a.idx[row * kslots + s] = -1;
+    if (tid == 0) a.cnt[row] = 0;
+    return;
+  }
+  const int Wc = num_windows(c * kBlock);
+  const int n_wt = (Wc + kMtWin - 1) / kMtWin;
+  const int n_tok = min(kBlock, T - c * kBlock);
+  const int n_rp = (n_tok + 8 * kMtTiles - 1) / (8 * kMtTiles);  // pairs of 8-token tiles
+  const int n_steps = 2 * n_wt;                                   // per pair: two passes
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
+    for (int i = 0; i < n_st; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2 * kMtTiles; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid; i < Wc; i += blockDim.x) win_sum[i] = 0.f;
+  if (warp == 1) {
+    tc05::alloc(tmem_base_sh, kMtCols);
+    tc05::relinquish();
+  }
+  tc05::fence_before();
+  __syncthreads();
+  tc05::fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+  bool ok = true;
+
+  if (n_wt > 0 && warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mck);
+      int gs = 0;
+      for (int rp = 0; rp < n_rp && ok; ++rp) {
+        if (rp > 0) ok = mbar_wait(q_free, (rp - 1) & 1, a.err);    // the pair before has been read
+        if (!ok) break;
+        mbar_arrive_expect_tx(q_full, kMtTiles * kMtQBytes);
+        for (int i = 0; i < 8 * kMtTiles; ++i) {
+          const int tok = c * kBlock + 8 * kMtTiles * rp + i;          // < max_ctx: a row past T counts for nothing
+          const int qr = (((b * a.max_ctx) + tok) * a.G + g) * kHeads;
+          uint8_t* qt = qs + (i >> 3) * kMtQBytes + (i & 7) * 16 * 128;
+          tma_load_2d(qt, &mq, 0, qr, q_full);
+          tma_load_2d(qt + kMtQBytes / 2, &mq, 64, qr, q_full);
+        }
+        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
+          const int stage = gs % n_st;
+          if (gs >= n_st) ok = mbar_wait(&kv_empty[stage], ((gs / n_st) & 1) ^ 1, a.err);
+          if (!ok) break;
+          const int rr = bg * a.W_cap + (s % n_wt) * kMtWin;
+          uint8_t* dst = ring + stage * kMtCkBytes;
+          mbar_arrive_expect_tx(&kv_full[stage], kMtCkBytes);
+          tma_load_2d(dst, &mck, 0, rr, &kv_full[stage]);
+          tma_load_2d(dst + kMtCkBytes / 4, &mck, 0, rr + 64, &kv_full[stage]);
+          tma_load_2d(dst + kMtCkBytes / 2, &mck, 64, rr, &kv_full[stage]);
+          tma_load_2d(dst + 3 * kMtCkBytes / 4, &mck, 64, rr + 64, &kv_full[stage]);
+        }
+      }
+    }
+  } else if (n_wt > 0 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc05::idesc_bf16(128, kMtWin, 0, 0);
+      const uint32_t q_addr = smem_addr(qs), ring_addr = smem_addr(ring);
+      int gs = 0;
+      for (int rp = 0; rp < n_rp && ok; ++rp) {
+        ok = mbar_wait(q_full, rp & 1, a.err);
+        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
+          const int stage = gs % n_st;
+          ok = mbar_wait(&kv_full[stage], (gs / n_st) & 1, a.err);
+          for (int t = 0; t < kMtTiles && ok; ++t) {
+            const int sb = 2 * t + (gs & 1);
+            if (gs >= 2) ok = mbar_wait(&s_free[sb], ((gs >> 1) - 1) & 1, a.err);   // read two steps ago
+            if (!ok) break;
+            tc05::fence_after();
+            const uint32_t kb = ring_addr + stage * kMtCkBytes;
+            const uint32_t qa = q_addr + t * kMtQBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t half = (uint32_t)(kk >> 2), off = (uint32_t)(kk & 3) * 32;
+              const uint64_t da = tc05::smem_desc(qa + half * (kMtQBytes / 2) + off, 16, 1024);
+              const uint64_t db = tc05::smem_desc(kb + half * (kMtCkBytes / 2) + off, 16, 1024);
+              tc05::mma_bf16_ss(tmem + 256 * t + 128 * (gs & 1), da, db, id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc05::commit(&s_full[sb]);
+          }
+          if (ok) tc05::commit(&kv_empty[stage]);                  // both tiles' S read the stage
+        }
+        if (ok) tc05::commit(q_free);                              // every S of the pair read Q
+      }
+    }
+  } else if (n_wt > 0 && warp >= 2) {
+    // ------------------------------------------------------------ softmax, one row per thread
+    const int t = (warp - 2) >> 2;                           // query tile
+    const int quarter = warp & 3;                            // tensor-memory lanes 32q .. 32q+31
+    const int r = quarter * 32 + lane;                       // row: token r/16 of the tile, head r%16
+    const int wi = warp - 2;                                 // this warp's slot in the column sums
+    const float zl2 = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int st = tid - 64;                                 // 0 .. 255 over the softmax warps
+    int gs = 0;
+    for (int rp = 0; rp < n_rp; ++rp) {
+      const int tok = c * kBlock + 8 * kMtTiles * rp + 8 * t + (r >> 4);
+      const bool live = tok < T;
+      float M = -INFINITY, L = 0.f, invL = 0.f;
+      for (int s = 0; s < n_steps; ++s, ++gs) {
+        const bool pass2 = s >= n_wt;
+        const int m = s - (pass2 ? n_wt : 0);
+        const int nvalid = min(kMtWin, Wc - m * kMtWin);     // windows of this tile below Wc
+        const int sb = 2 * t + (gs & 1);
+        if (ok) ok = __all_sync(0xffffffffu, sm_wait(&s_full[sb], (gs >> 1) & 1, a.err));
+        if (ok) tc05::fence_after();
+        float* pw = part + ((gs & 1) * 4 * kMtTiles + wi) * kMtWin;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float x[64];
+          if (ok) {
+            const uint32_t ta = tmem + 256 * t + 128 * (gs & 1) + 64 * h + lane_off;
+            tc05::ld32(ta, *reinterpret_cast<float(*)[32]>(x));
+            tc05::ld32(ta + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+            tc05::wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = 0.f;
+          }
+          if (64 * (h + 1) > nvalid) {                       // warp-uniform: windows past Wc
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = (64 * h + e < nvalid) ? x[e] : -INFINITY;
+          }
+          if (!pass2) {
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+            for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * zl2;
+            const float mn = fmaxf(M, mx);
+            if (mn != -INFINITY) {
+              float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int e = 0; e < 64; ++e) ps[e & 7] += ex2_ftz(fmaf(x[e], zl2, -mn));
+              L = L * ex2_ftz(M - mn) + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+              M = mn;
+            }
+          } else {
+            // p = 2^(s - max) / sum, 0 for rows past the prompt and windows past Wc
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = live ? ex2_ftz(fmaf(x[e], zl2, -M)) * invL : 0.f;
+            float s0, s1;
+            lane_colsum64(x, lane, s0, s1);
+            *reinterpret_cast<float2*>(pw + 64 * h + 2 * lane) = make_float2(s0, s1);
+          }
+        }
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(&s_free[sb]);
+        if (s == n_wt - 1) invL = L > 0.f ? 1.f / L : 0.f;
+        if (pass2) {
+          // the eight warps' sums of this window tile, added in warp order
+          mt_softmax_sync();
+          if (st < kMtWin) {
+            const float* pb = part + (gs & 1) * 4 * kMtTiles * kMtWin;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4 * kMtTiles; ++w) acc += pb[w * kMtWin + st];
+            if (st < nvalid) win_sum[m * kMtWin + st] += acc;
+          }
+        }
+      }
+    }
+  }
+  // ---- every thread: the window sums are complete once every role has left its loop
+  tc05::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc05::fence_after();
+    tc05::dealloc(tmem, kMtCols);
+  }
+  if (warp < 8) {
+    // max-pool onto blocks j <= c (windows 4j-1 .. 4j+3 below Wc), then the top-k (threads
+    // 0 .. 255; its scratch over the query tiles, free now)
+    float* S = a.block_scores + row * a.nb_cap;
+    for (int j = tid; j <= c; j += 256) {
+      float v = -INFINITY;
+      for (int i = max(0, 4 * j - 1); i <= min(Wc - 1, 4 * j + 3); ++i) v = fmaxf(v, win_sum[i]);
+      S[j] = v;
+    }
+    __threadfence_block();
+    topk_sync();
+    TopkShared& sh = *reinterpret_cast<TopkShared*>(qs);
+    topk_select(S, a.idx + row * kslots, a.cnt + row, a.topk, a.max_ctx, c * kBlock + 1, sh);
+  }
+}
+
 // ==================================================================== launches
 void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_t s) {
   const int n_ct = (a.nb_cap + kPfChunks - 1) / kPfChunks;
@@ -807,10 +886,12 @@ void launch_prefill_forecast_select(const PrefillArgs& a, int batch, cudaStream_
   prefill_topk_kernel<<<dim3(a.nb_cap, batch * a.G), kTopkThreads, 0, s>>>(a);
 }
 
-void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mck, int batch, cudaStream_t s) {
-  const int smem = mh_smem_bytes(a.W_cap);
-  cudaFuncSetAttribute(prefill_multihead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  prefill_multihead_kernel<<<dim3(a.nb_cap, batch * a.G), kPaThreads, smem, s>>>(a, mck);
+void launch_prefill_multihead_select(const PrefillArgs& a, const CUtensorMap& mq, const CUtensorMap& mck, int batch,
+                                     cudaStream_t s) {
+  const int n_st = mt_stages(a.W_cap);
+  const int smem = mt_smem_bytes(a.W_cap, n_st);
+  cudaFuncSetAttribute(prefill_multihead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  prefill_multihead_tc_kernel<<<dim3(a.nb_cap, batch * a.G), kMtThreads, smem, s>>>(a, n_st, mq, mck);
 }
 
 
