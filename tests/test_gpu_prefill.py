@@ -177,3 +177,29 @@ def test_prefill_attention_when_later_blocks_dominate(sb):
                                                    to64(layer.v[b, g]), sel, T)
             for t in range(T):
                 check_attention(o[b, t, 16 * g:16 * g + 16], ref[t])
+
+
+def test_prefill_selection_at_the_largest_context_shape(sb):
+    """max_ctx 262144: the baseline selector's window sums take the room of a ring stage (two
+    stages instead of three); a 5000-token prompt, every chunk checked, both selectors."""
+    max_ctx, T, k = 262144, 5000, 8
+    shape = sb.Shape(n_groups=2, topk=k, max_ctx=max_ctx, max_batch=1)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(synth.normal_bf16_device(layer.k.shape, 81, "cuda"))
+    layer.v.copy_(synth.normal_bf16_device(layer.v.shape, 82, "cuda"))
+    q = synth.normal_bf16_device((1, max_ctx, 32, 128), 83, "cuda")
+    f = synth.normal_bf16_device((1, max_ctx, 2, 128), 84, "cuda")
+    seq = torch.full((1,), T, dtype=torch.int32, device="cuda")
+    sb.sparda_compress_keys(shape, layer, seq, 1)
+    nc = O.prefill_num_chunks(T)
+    for which in ("forecast", "multihead"):
+        idx, cnt = _select(sb, shape, which, layer, f if which == "forecast" else q, seq, 1)
+        idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+        assert (cnt[0, :, nc:] == 0).all()
+        for g in range(2):
+            ck = O.compress_keys(to64(layer.k[0, g, :T]), O.num_windows(T))
+            if which == "forecast":
+                queries = lambda c: to64(f[0, 64 * c:min(64 * c + 64, T), g])
+            else:
+                queries = lambda c: to64(q[0, 64 * c:min(64 * c + 64, T), 16 * g:16 * g + 16])
+            _check_chunks(idx, cnt, 0, g, T, k, ck, range(nc), queries, which)
