@@ -259,7 +259,11 @@ int32_t sparda_forecast_score(const sparda_shape* shape, const void* ck, const v
  * layer: staging_k / staging_v (device bf16 [max_batch, G, topk+2, 64, d], filled by
  * sparda_prefetch_blocks for the same idx) supply every selected block except block 0 and
  * the tail block, which come from the layer's hot buffers. QK^T and PV run on tensor cores
- * (bf16 operands, float32 accumulation); the softmax is float32. workspace: SPARDA_WS_ATTN.
+ * (bf16 operands, float32 accumulation); the softmax is float32. workspace: SPARDA_WS_ATTN
+ * (partial results of (sequence, group)s split over several CTAs, and a counter per group,
+ * zero between calls and left zero; when every group gets the same 2 to 8 CTAs, they form
+ * one thread-block cluster and merge in distributed shared memory, and the workspace is
+ * not touched).
  */
 int32_t sparda_sparse_decode_attn(const sparda_shape* shape, const sparda_layer_kv* layer,
                                   const void* staging_k, const void* staging_v, const void* q,
@@ -529,8 +533,10 @@ int32_t sparda_prefill_forecast_select(const sparda_shape* shape, const void* ck
  * every (token, head) query of the chunk gets its own softmax over the windows before the
  * chunk (logits scaled by 1/sqrt(d)), and the probabilities are summed over the chunk's
  * tokens and the group's heads; then the same max-pool and top-k. q: device bf16
- * [max_batch, max_ctx, G*H, d]. The logits run on tensor cores (bf16 operands, float32
- * accumulation); the softmax and the sums are float32.
+ * [max_batch, max_ctx, G*H, d]. The logits run on tensor cores (tcgen05: bf16 operands,
+ * float32 accumulation); the softmax and the sums are float32, the sums over rows in a
+ * fixed order (the result does not vary from call to call). SPARDA_ERR_UNSUPPORTED_SHAPE
+ * when max_batch * G * max_ctx * H reaches 2^31 (a query row's TMA coordinate).
  */
 int32_t sparda_prefill_multihead_select(const sparda_shape* shape, const void* ck, const void* q,
                                         const int32_t* seq_len, int32_t batch, int32_t* idx, int32_t* cnt,
