@@ -2,6 +2,13 @@
 // attn_cta (attn_body.cuh), which the fused attend-and-select kernel (fused.cu) shares. When
 // every (sequence, group) gets the same number (2 to 8) of CTAs, that number is the cluster
 // size and a group's partial results meet in distributed shared memory, not in the workspace.
+//
+// Every CTA lets the next launch in the stream begin as soon as it starts (programmatic
+// dependent launch): that launch's CTAs take the SMs this one leaves free and set up there
+// (barriers, tensor-map prefetch), and each of the library's kernels that may begin early
+// waits for this one to complete before it reads or writes anything this one touches (the
+// output, the workspace, the error word). Back to back, one launch's start-up then overlaps
+// the previous one's merge.
 #include "attn_body.cuh"
 
 namespace sparda {
@@ -12,6 +19,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_kernel(
     const AttnArgs a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
     const __grid_constant__ CUtensorMap hk, const __grid_constant__ CUtensorMap hv) {
   SPARDA_TL_ENTRY();
+  grid_dep_launch();
   unsigned long long tl_first = 0;
   attn_cta(a, &mk, &mv, &hk, &hv, blockIdx.x, gridDim.x, &tl_first);
   SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlAttention, tl_first);
@@ -21,6 +29,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_cluster_kernel(
     const AttnArgs a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
     const __grid_constant__ CUtensorMap hk, const __grid_constant__ CUtensorMap hv) {
   SPARDA_TL_ENTRY();
+  grid_dep_launch();
   unsigned long long tl_first = 0;
   attn_cta<true>(a, &mk, &mv, &hk, &hv, blockIdx.x, gridDim.x, &tl_first);
   SPARDA_TL_EXIT(a.tl_buf, a.tl_launch, kTlAttention, tl_first);
@@ -67,8 +76,9 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   b.tl_buf = timeline_buffer();
   auto kern = cluster ? sparse_attn_cluster_kernel : sparse_attn_kernel;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-  // Programmatic serialization: barrier set-up and the unit metadata overlap the append
-  // before it in the stream; the producer waits for it before the first TMA load.
+  // Programmatic serialization: the barrier set-up overlaps the kernel before it in the
+  // stream; the producer waits for it before it reads the unit metadata, the consumers before
+  // they write anything.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kAttnThreads);

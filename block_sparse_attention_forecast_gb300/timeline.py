@@ -21,8 +21,9 @@ The workload is the benchmark's, with fewer layers (seeded synthetic K/V, 16 pla
 
 instead times the standalone block-sparse decode attention alone, launched once per layer back
 to back from a CUDA graph (the step's own selections), and prints per launch its CTAs' phases in
-microseconds from the launch's first CTA entry: first block in shared memory (median, max) and
-exit (median, max), and the gap to the next launch's first entry.
+microseconds from the previous launch's last CTA exit (each launch lets the next begin at once,
+so CTAs of the next may enter early and wait): entry (first, median), first block in shared
+memory (median, max), exit (median, max), and the period (this launch's last exit).
 """
 from __future__ import annotations
 
@@ -154,18 +155,22 @@ def attn_chain(stack, read, sb, bench, torch):
         by_launch.setdefault(r.launch, []).append(r)
     launches = sorted(by_launch)
     print("%d launches, %.2f us per launch (graph replay, CUDA events)" % (n, t / n * 1e6))
-    print("launch  CTAs  first_block med/max  exit med/max  gap_to_next (us from the launch's first entry)")
-    for i, lid in enumerate(launches):
+    # Each launch lets the next begin at once, so the next one's CTAs may enter (and wait) long
+    # before this one ends: phases are measured from the previous launch's last CTA exit (the
+    # first launch: from its own first entry).
+    print("launch  CTAs  entry first/med  first_block med/max  exit med/max  period"
+          "  (us from the previous launch's last exit)")
+    prev_end = None
+    for lid in launches:
         rs = by_launch[lid]
-        t0 = min(r.t_entry for r in rs)
+        t0 = prev_end if prev_end is not None else min(r.t_entry for r in rs)
+        ent = np.array([(r.t_entry - t0) / 1e3 for r in rs])
         first = np.array([(r.t_release - t0) / 1e3 for r in rs if r.t_release])
         ex = np.array([(r.t_exit - t0) / 1e3 for r in rs])
-        gap = ""
-        if i + 1 < len(launches):
-            gap = "%.2f" % ((min(r.t_entry for r in by_launch[launches[i + 1]]) - max(r.t_exit for r in rs)) / 1e3)
-        print("%5d  %4d  %6.2f %6.2f  %6.2f %6.2f  %s" % (lid, len(rs), np.median(first) if len(first) else -1,
-                                                        first.max() if len(first) else -1, np.median(ex), ex.max(), gap))
-
+        print("%5d  %4d  %6.2f %6.2f  %6.2f %6.2f  %6.2f %6.2f  %6.2f" % (
+            lid, len(rs), ent.min(), np.median(ent), np.median(first) if len(first) else -1,
+            first.max() if len(first) else -1, np.median(ex), ex.max(), ex.max()))
+        prev_end = max(r.t_exit for r in rs)
 
 if __name__ == "__main__":
     main()

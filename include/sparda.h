@@ -264,6 +264,12 @@ int32_t sparda_forecast_score(const sparda_shape* shape, const void* ck, const v
  * zero between calls and left zero; when every group gets the same 2 to 8 CTAs, they form
  * one thread-block cluster and merge in distributed shared memory, and the workspace is
  * not touched).
+ * Ordering: the call begins while the kernel before it in the stream still runs
+ * (programmatic dependent launch) and reads nothing before that kernel has completed. It
+ * lets the next launch in the stream begin as soon as it starts; every call of this library
+ * that can begin that early waits for it to complete before touching its output, workspace
+ * or error word. Such a following call may then also run beside the launch before this one:
+ * between two sparda_attend_and_score calls, this call does not separate them (see there).
  */
 int32_t sparda_sparse_decode_attn(const sparda_shape* shape, const sparda_layer_kv* layer,
                                   const void* staging_k, const void* staging_v, const void* q,
@@ -323,8 +329,10 @@ int32_t sparda_attend_and_select(const sparda_shape* shape, const sparda_layer_k
  * A run of these calls (or of sparda_attend_and_select) directly after one another in a
  * stream therefore overlaps: as many as fit on the GPU may run at once, so give each call of
  * such a run its own ws_scores (the selection's work queue lives there; ws_attn may be
- * shared). With a sparda_decode_prologue between two calls, as in the decode step, the
- * second begins only after the first has completed, and two workspaces alternating suffice.
+ * shared); a sparda_sparse_decode_attn between two calls, which also lets the next launch
+ * begin at once, counts as no separation. With a sparda_decode_prologue between two calls,
+ * as in the decode step, the second begins only after the first has completed, and two
+ * workspaces alternating suffice.
  */
 int32_t sparda_attend_and_score(const sparda_shape* shape, const sparda_layer_kv* layer,
                                 const void* staging_k, const void* staging_v, const void* q,
