@@ -259,6 +259,72 @@ def test_sparse_attention_split_groups(sb, B, k, max_ctx):
     _no_device_error(sb)
 
 
+# Calls issued back to back without a host synchronisation. Each attention launch lets the next
+# launch begin at its start, so this checks the ordering the library keeps without a host wait:
+# a second attention sharing the first one's workspace, a forecast selection (which may also
+# begin early) rewriting the block indices the first attention read, and a third attention
+# reading the new indices and writing the first one's output buffer. Batch 16 merges each
+# group in a thread-block cluster, batch 5 through the workspace.
+@pytest.mark.parametrize("B", [16, 5])
+def test_attention_calls_back_to_back(sb, B):
+    k, max_ctx = 16, 4096
+    rng = np.random.default_rng(3000 + B)
+    T_list = [int(x) for x in rng.integers(200, max_ctx + 1, size=B)]
+    T_list[0] = max_ctx
+    shape = sb.Shape(max_ctx=max_ctx, max_batch=B, topk=k)
+    K = synth.normal_bf16((B, 2, max_ctx, 128), 81, B)
+    V = synth.normal_bf16((B, 2, max_ctx, 128), 82, B)
+    qs = [synth.normal_bf16((B, 32, 128), 83 + i, B) for i in range(3)]
+    f = synth.normal_bf16((B, 2, 128), 86, B)
+    layer = sb.LayerKV.empty(shape)
+    layer.k.copy_(K.cuda())
+    layer.v.copy_(V.cuda())
+    seq = torch.tensor(T_list, dtype=torch.int32, device="cuda")
+    sb.sparda_compress_keys(shape, layer, seq - 1, B)
+    # two fixed selections (random block sets) for the first two calls
+    sels = []
+    idx_d, cnt_d = [], []
+    for i in range(2):
+        idx = torch.full((B, 2, k + 2), -1, dtype=torch.int32)
+        cnt = torch.zeros((B, 2), dtype=torch.int32)
+        sel_i = {}
+        for b, T in enumerate(T_list):
+            nb = (T - 1) // 64 + 1
+            for g in range(2):
+                sel = sorted(int(x) for x in rng.choice(nb, size=min(k + 2, nb), replace=False))
+                sel_i[b, g] = sel
+                idx[b, g, :len(sel)] = torch.tensor(sel, dtype=torch.int32)
+                cnt[b, g] = len(sel)
+        sels.append(sel_i)
+        idx_d.append(idx.cuda())
+        cnt_d.append(cnt.cuda())
+    wa = sb.workspace(shape, B, sb.WS_ATTN)
+    ws = sb.workspace(shape, B, sb.WS_SELECT)
+    out1 = torch.full((B, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.full((B, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q_d = [q.cuda() for q in qs]
+    torch.cuda.synchronize()
+    sb.sparda_sparse_decode_attn(shape, layer, q_d[0], idx_d[0], cnt_d[0], seq, B, out1, wa)
+    sb.sparda_sparse_decode_attn(shape, layer, q_d[1], idx_d[1], cnt_d[1], seq, B, out2, wa)
+    sb.sparda_forecast_select(shape, layer.ck, f.cuda(), seq, B, idx_d[0], cnt_d[0], ws)
+    sb.sparda_sparse_decode_attn(shape, layer, q_d[2], idx_d[0], cnt_d[0], seq, B, out1, wa)
+    torch.cuda.synchronize()
+    idx3, cnt3 = idx_d[0].cpu(), cnt_d[0].cpu()
+    o1, o2 = to64(out1), to64(out2)
+    for b, T in enumerate(T_list):
+        for g in range(2):
+            _, S = O.forecast_select_one(to64(K[b, g]), to64(f[b, g]), T, k, return_scores=True)
+            check_selection(idx3[b, g], cnt3[b, g], S, T, k)
+            sel3 = [int(x) for x in idx3[b, g, :int(cnt3[b, g])]]
+            ref3 = O.block_sparse_attention(to64(qs[2][b, 16 * g:16 * g + 16]), to64(K[b, g]),
+                                            to64(V[b, g]), sel3, T)
+            check_attention(o1[b, 16 * g:16 * g + 16], ref3)
+            ref2 = O.block_sparse_attention(to64(qs[1][b, 16 * g:16 * g + 16]), to64(K[b, g]),
+                                            to64(V[b, g]), sels[1][b, g], T)
+            check_attention(o2[b, 16 * g:16 * g + 16], ref2)
+    _no_device_error(sb)
+
+
 def test_attention_all_blocks_equals_dense(sb):
     T, max_ctx = 1000, 1024
     shape = sb.Shape(max_ctx=max_ctx, max_batch=1, topk=62)
