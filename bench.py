@@ -523,6 +523,25 @@ def run_offload(device, seed, steps, warmup):
         gc.collect()
         torch.cuda.empty_cache()
     del h_bank
+    # between the two: hidden states that drift from step to step, h <- sqrt(1 - eps^2) h + eps z
+    # with fresh noise z, from the stack's own starting states (so the planted blocks stay
+    # relevant), which keeps part of consecutive steps' selections
+    for eps in (0.05, 0.2):
+        st_bc = make(layers, True, block_cache=TOPK + 2)
+        walk, h = [], st_bc.h.float()
+        for i in range(warmup + steps):
+            z = synth.normal_bf16_device(st_bc.h.shape, seed * 1000 + 840 + i, device).float()
+            h = (1.0 - eps * eps) ** 0.5 * h + eps * z
+            walk.append(h.to(torch.bfloat16))
+        t_bc = time_stack(st_bc, walk)
+        hits, misses = st_bc.cache_stats.cpu().tolist()
+        cache_res["hidden_drift_%g" % eps] = {"tok_s": B / t_bc, "ms_per_step": t_bc * 1e3,
+                                              "hit_rate": hits / max(1, hits + misses),
+                                              "blocks_gathered_per_step": misses / steps,
+                                              "offload_vs_resident_time": t_bc / t_res}
+        del st_bc, walk, h
+        gc.collect()
+        torch.cuda.empty_cache()
     cache_res["slots_per_group"] = TOPK + 2
     # without the cache, at new hidden states every step (the comparison for the worst case)
     h_bank = [synth.normal_bf16_device((N_LAYERS, B, HIDDEN), seed * 1000 + 830 + i, device) for i in range(4)]
