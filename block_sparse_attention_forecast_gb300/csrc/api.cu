@@ -666,7 +666,7 @@ int32_t sparda_prefetch_blocks_cached(const sparda_shape* s, const sparda_layer_
   CacheArgs a{static_cast<const __nv_bfloat16*>(L->k), static_cast<const __nv_bfloat16*>(L->v), idx, cnt, seq_len,
               cache_blocks, slot, fetch, stats, static_cast<__nv_bfloat16*>(cache_k),
               static_cast<__nv_bfloat16*>(cache_v), err, batch, s->n_groups, s->max_ctx, kslots(s), n_cache};
-  launch_cache_gather(a, n_ctas ? n_ctas : sparda_prefetch_default_ctas(batch), static_cast<cudaStream_t>(stream));
+  launch_cache_gather(a, static_cast<cudaStream_t>(stream));   // one CTA per (b, g): n_ctas is not used
   return cuda_status(cudaGetLastError());
 }
 

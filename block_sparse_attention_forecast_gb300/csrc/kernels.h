@@ -128,7 +128,7 @@ struct CacheArgs {
   int* err;
   int B, G, max_ctx, kslots, n_cache;
 };
-void launch_cache_gather(const CacheArgs& a, int n_ctas, cudaStream_t s);
+void launch_cache_gather(const CacheArgs& a, cudaStream_t s);   // one CTA per (sequence, group)
 
 void launch_append_kv(const AppendArgs& a, int bg_count, cudaStream_t s);
 void launch_compress_keys(const CompressArgs& a, int bg_count, cudaStream_t s);

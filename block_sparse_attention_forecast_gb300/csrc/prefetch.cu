@@ -90,19 +90,23 @@ void launch_prefetch(const PrefetchArgs& a, int n_ctas, cudaStream_t s) {
 // it gathered at earlier steps in n_cache slots of HBM, and only blocks that are not there
 // yet cross the host link. cache_blocks[bg][c] names the block held in slot c (-1: none).
 //
-// cache_assign_kernel: one warp per (sequence, group). A selected block (not block 0 or the
-// tail block, which the hot ring supplies) already held in a slot keeps it (a hit). Every
-// other selected block (a miss) takes, in order of its position in idx, the lowest slot whose
-// block is not selected at this step; fetch[bg][c] = the block slot c must receive (-1:
-// none), slot[bg][s] = the cache slot of idx entry s (-1 for block 0, the tail block and
-// padding). cache_fetch_kernel then copies the fetched blocks on the copy CTAs.
-constexpr int kCacheMaxSlots = 128;                 // 4 words of 32 lanes
-constexpr int kAssignWarps = 4;
+// cache_gather_kernel: one CTA per (sequence, group). Its first warp assigns the slots: a
+// selected block (not block 0 or the tail block, which the hot ring supplies) already held in
+// a slot keeps it (a hit); every other selected block (a miss) takes, in order of its position
+// in idx, the lowest slot whose block is not selected at this step; fetch[bg][c] = the block
+// slot c must receive (-1: none), slot[bg][s] = the cache slot of idx entry s (-1 for block 0,
+// the tail block and padding). After a CTA barrier the CTA copies the group's misses on
+// kCacheStreams copy streams of 128 threads. Only this CTA reads or writes the group's slot
+// table, so the assignment and the copies need no ordering across CTAs, and the gather is one
+// launch: a separate assignment launch ahead of the copies stalled every layer's gather stream
+// (the offloaded step with every block a miss took 25 ms instead of 20).
+constexpr int kCacheMaxSlots = 128;                 // 4 words of 32 lanes (n_cache at most)
+static_assert(kCacheMaxSlots == 4 * 32, "the assignment keeps each lane's slots in four words");
+constexpr int kCacheStreams = 4;
+constexpr int kCacheThreads = kCacheStreams * kGatherThreads;   // 512
 
-__global__ void __launch_bounds__(kAssignWarps * 32) cache_assign_kernel(const CacheArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int bg = blockIdx.x * kAssignWarps + (threadIdx.x >> 5);
-  if (bg >= a.B * a.G) return;
+// The slot assignment of (sequence, group) bg by one warp.
+__device__ __forceinline__ void assign_group(const CacheArgs& a, int bg, int lane) {
   const int T = a.seq_len[bg / a.G];
   const bool valid = T >= 1 && T <= a.max_ctx;
   if (!valid && lane == 0) atomicOr(a.err, SPARDA_DEV_BAD_SEQ_LEN);
@@ -204,22 +208,22 @@ __global__ void __launch_bounds__(kAssignWarps * 32) cache_assign_kernel(const C
   }
 }
 
-__global__ void __launch_bounds__(kGatherThreads) cache_fetch_kernel(const CacheArgs a) {
-  const int n_items = a.B * a.G * a.n_cache;
-  const int t = threadIdx.x;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+__global__ void __launch_bounds__(kCacheThreads) cache_gather_kernel(const CacheArgs a) {
+  const int bg = blockIdx.x;
+  if (threadIdx.x < 32) assign_group(a, bg, threadIdx.x);
+  __syncthreads();                                 // the fetch list is written
+  const int stream = threadIdx.x / kGatherThreads, t = threadIdx.x % kGatherThreads;
+  for (int c = stream; c < a.n_cache; c += kCacheStreams) {
+    const size_t item = (size_t)bg * a.n_cache + c;
     const int j = a.fetch[item];
     if (j < 0) continue;
-    const int bg = item / a.n_cache;
     copy_block(a.hk, a.hv, ((size_t)bg * a.max_ctx + (size_t)j * kBlock) * kHeadDim, a.ck_cache, a.cv_cache,
-               (size_t)item * kBlock * kHeadDim, t);
+               item * kBlock * kHeadDim, t);
   }
 }
 
-void launch_cache_gather(const CacheArgs& a, int n_ctas, cudaStream_t s) {
-  const int bgc = a.B * a.G;
-  cache_assign_kernel<<<(bgc + kAssignWarps - 1) / kAssignWarps, kAssignWarps * 32, 0, s>>>(a);
-  cache_fetch_kernel<<<n_ctas, kGatherThreads, 0, s>>>(a);
+void launch_cache_gather(const CacheArgs& a, cudaStream_t s) {
+  cache_gather_kernel<<<a.B * a.G, kCacheThreads, 0, s>>>(a);
 }
 
 }  // namespace sparda

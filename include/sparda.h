@@ -474,10 +474,13 @@ int32_t sparda_prefetch_blocks_copy_engine(const sparda_shape* shape, const spar
  * sparda_prefetch_blocks_cached -- sparda_prefetch_blocks with the block cache. For every
  * (b, g), a selected block (other than block 0 and the tail block, which the hot buffers
  * hold) already held in a slot keeps it; each other selected block, in idx order, takes the
- * lowest slot whose block is not selected now, and is copied there from the host cache by the
- * copy CTAs. slot[b, g, s] receives the cache slot of idx entry s (-1 for block 0, the tail
- * block and padding). stats (optional, NULL for none; device uint64 [2], 8-byte aligned)
- * accumulates the hits and the misses (blocks copied). n_ctas as sparda_prefetch_blocks.
+ * lowest slot whose block is not selected now, and is copied there from the host cache.
+ * slot[b, g, s] receives the cache slot of idx entry s (-1 for block 0, the tail block and
+ * padding). stats (optional, NULL for none; device uint64 [2], 8-byte aligned) accumulates
+ * the hits and the misses (blocks copied). One launch of one CTA per (b, g): the CTA assigns
+ * its group's slots and copies its group's misses itself (four copy streams of 128 threads),
+ * so the number of copy CTAs follows the batch; n_ctas is checked as for
+ * sparda_prefetch_blocks (0 .. 4096) but not used.
  * Errors: as sparda_prefetch_blocks; SPARDA_ERR_UNSUPPORTED_SHAPE for n_cache out of range.
  */
 int32_t sparda_prefetch_blocks_cached(const sparda_shape* shape, const sparda_layer_kv* host_layer,
