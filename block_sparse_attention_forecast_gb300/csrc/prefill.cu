@@ -215,26 +215,10 @@ __global__ void __launch_bounds__(kTopkThreads) prefill_topk_kernel(const Prefil
 // to have seen this warp's P, pv_done's next phase this warp's next P, and each warp waits
 // pv_done's phases in order.
 namespace {
-// The softmax warps' waits: the library's bounded wait, or (SPARDA_TC_SPIN) a bounded loop of
-// try_wait without the suspend-time hint.
+// The softmax warps' waits: the library's bounded wait (try_wait with a suspend-time hint; a
+// polling loop of test_wait measured slower, its thread taking issue slots from the softmax).
 __device__ __forceinline__ bool sm_wait(uint64_t* bar, uint32_t parity, int* err) {
-#ifdef SPARDA_TC_SPIN
-  for (uint32_t i = 0; i < (kWaitPolls << 4); ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  atomicOr(err, SPARDA_DEV_WAIT_TIMEOUT);
-  return false;
-#else
   return mbar_wait(bar, parity, err);
-#endif
 }
 
 __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
@@ -246,13 +230,9 @@ __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
 // notice: the running maximum it subtracts is a logit it has already summed, so every row's
 // sum is at least 1.
 __device__ __forceinline__ float ex2_ftz(float x) {
-#ifdef SPARDA_TC_LIBM_EXP2
-  return exp2f(x);
-#else
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-#endif
 }
 
 constexpr int kTcTiles = 2;
