@@ -31,9 +31,12 @@ def _offloaded_layer(sb, shape, K, V, n_cached):
     return layer
 
 
-@pytest.mark.parametrize("n_cache", [10, 16])
-def test_cache_slots_hits_and_contents(sb, n_cache):
-    T_list, k, max_ctx = [3000, 2100, 4096], 8, 4096
+# The largest case keeps 62 blocks per step in 128 slots: hits pin slots and misses then take
+# slots past 31, so the assignment runs over all four words of lane slots.
+@pytest.mark.parametrize("k,n_cache,max_ctx,T_list", [(8, 10, 4096, [3000, 2100, 4096]),
+                                                      (8, 16, 4096, [3000, 2100, 4096]),
+                                                      (62, 128, 8192, [8192, 6000, 4500])])
+def test_cache_slots_hits_and_contents(sb, k, n_cache, max_ctx, T_list):
     B = len(T_list)
     shape = sb.Shape(n_groups=2, topk=k, max_ctx=max_ctx, max_batch=B)
     K = synth.normal_bf16((B, 2, max_ctx, 128), 71, 1)
@@ -83,8 +86,10 @@ def test_cache_slots_hits_and_contents(sb, n_cache):
                 assert len(set(slots)) == len(slots)
         got = (stats - before).cpu().tolist()
         assert got == [hits, misses], (step, got, hits, misses)
-        if step == 2:
-            assert hits > 0                                     # the cache kept step 0's blocks?
+        if step == 2 and n_cache <= 16:
+            # the cache kept some of step 0's blocks (with 128 slots the lowest-free rule may
+            # have given all of them to step 1's misses)
+            assert hits > 0
         # attention from the cache equals attention from the per-step staging, bit for bit
         out_c = torch.zeros((B, 32, 128), dtype=torch.bfloat16, device="cuda")
         out_s = torch.zeros_like(out_c)
