@@ -48,7 +48,6 @@ int sm_count() {
   return n[dev];
 }
 
-constexpr int kAttnMaxCluster = 8;
 
 void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& hk, const CUtensorMap& hv, int bg_count,
@@ -64,7 +63,7 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   if (bg_count <= sms) {
     int sg = sms / bg_count;
     if (sg > a.kslots) sg = a.kslots;   // every CTA has a unit (the cluster form relies on it)
-    const int sg_cl = sg < kAttnMaxCluster ? sg : kAttnMaxCluster;
+    const int sg_cl = sg < kMaxClusterCtas ? sg : kMaxClusterCtas;
     if (sg_cl >= 2 && 4 * sg_cl * bg_count >= 3 * sms) {
       sg = sg_cl;
       cluster = sg;
@@ -75,14 +74,15 @@ void launch_sparse_attn(const AttnArgs& a, const CUtensorMap& mk, const CUtensor
   b.tl_launch = timeline_next_launch();
   b.tl_buf = timeline_buffer();
   auto kern = cluster ? sparse_attn_cluster_kernel : sparse_attn_kernel;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  const int smem = cluster ? kAttnClusterSmem : kAttnSmem;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   // Programmatic serialization: the barrier set-up overlaps the kernel before it in the
   // stream; the producer waits for it before it reads the unit metadata, the consumers before
   // they write anything.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

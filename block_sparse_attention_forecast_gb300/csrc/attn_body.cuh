@@ -50,6 +50,13 @@ constexpr int kMergeFloats = kConsumerWarps * (kHeads * kMStride + 2 * kHeads);
 constexpr int kMaxInlineSeg = 8;           // partials the last arriver keeps in registers
 constexpr int kAttnSmem = 1024 /*align slack*/ + 1024 /*header*/ + kStages * kSlotBytes +
                           kMergeFloats * 4;
+// The cluster form's receive area, after the merge buffer: for each head h, the sg partials
+// (O, max, sum) that the cluster's CTAs push to the CTA owning h (rank h % sg), at entry
+// (h / sg) * sg + source rank: below ceil(16 / sg) * sg <= 16 + sg - 1 entries.
+constexpr int kMaxClusterCtas = 8;
+constexpr int kRecvEntries = kHeads + kMaxClusterCtas - 1;
+constexpr int kRecvFloats = kRecvEntries * kHeadDim + 2 * kRecvEntries;
+constexpr int kAttnClusterSmem = kAttnSmem + kRecvFloats * 4;
 
 // Shared-memory address of 16-byte chunk `chunk` (0..15 over the 128 dims) of row `r` of a
 // K or V block staged as two 64-row x 128-byte halves with the 128-byte TMA swizzle.
@@ -200,10 +207,7 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         ++it;
       }
     }
-    if constexpr (kClusterMerge) {
-      cluster_sync();                           // the consumers' two merge barriers
-      cluster_sync();
-    }
+    if constexpr (kClusterMerge) cluster_sync();   // the consumers' merge barrier
     return;
   }
 
@@ -378,58 +382,37 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
       }
     }
     if constexpr (kClusterMerge) {
-      // this CTA's (O, max, sum) into its own shared memory, then each CTA of the cluster
-      // combines the heads h with h % sg == its rank from all sg partials
-      consumer_sync();                         // the local merge has read its buffer
-      float* cO = mO;                          // [16 heads][128 dims]
-      float* cM = mM;                          // [16]
-      float* cL = mL;                          // [16]
-      float4* mine = reinterpret_cast<float4*>(cO + h * kHeadDim + d0);
-      mine[0] = make_float4(Oh[0], Oh[1], Oh[2], Oh[3]);
-      mine[1] = make_float4(Oh[4], Oh[5], Oh[6], Oh[7]);
+      // this CTA's (O, max, sum) of head h pushed into the receive area of the CTA that owns
+      // h (rank h % sg); after one cluster barrier each CTA combines its heads' sg partials
+      // from its own shared memory, and no CTA reads another's, so none has to stay resident
+      float* rO = mL + kConsumerWarps * kHeads;            // [kRecvEntries][128 dims]
+      float* rM = rO + kRecvEntries * kHeadDim;            // [kRecvEntries]
+      float* rL = rM + kRecvEntries;                       // [kRecvEntries]
+      const uint32_t rank = cluster_rank();
+      const int entry = (h / sg) * sg + (int)rank;
+      const uint32_t owner = (uint32_t)(h % sg);
+      st_cluster_f4(rO + entry * kHeadDim + d0, owner, make_float4(Oh[0], Oh[1], Oh[2], Oh[3]));
+      st_cluster_f4(rO + entry * kHeadDim + d0 + 4, owner, make_float4(Oh[4], Oh[5], Oh[6], Oh[7]));
       if ((t & 15) == 0) {
-        cM[h] = Mh;
-        cL[h] = Lh;
+        st_cluster_f(rM + entry, owner, Mh);
+        st_cluster_f(rL + entry, owner, Lh);
       }
-      cluster_sync();                          // #1: every partial of the group is visible
-      if (h % sg == (int)cluster_rank()) {
-        // four partials at a time, every load of a round issued before any is combined (slots
-        // past sg repeat rank 0 with weight 0), the rounds joined by log-sum-exp rescaling
-        constexpr int kRound = 4;
-        float acc[8], L = 0.f, M = -INFINITY;
+      cluster_sync();                          // every partial of the cluster's heads is in place
+      if (h % sg == (int)rank) {
+        const int e0 = (h / sg) * sg;
+        float Mx = -INFINITY;
+        for (int q = 0; q < sg; ++q) Mx = fmaxf(Mx, rM[e0 + q]);
+        const float base = (Mx == -INFINITY) ? 0.f : Mx;
+        float acc[8], L = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int q0 = 0; q0 < sg; q0 += kRound) {
-          float pm[kRound], pl[kRound];
-          float4 px[kRound][2];
-#pragma unroll
-          for (int q = 0; q < kRound; ++q) {
-            const bool in = q0 + q < sg;
-            const uint32_t r = in ? (uint32_t)(q0 + q) : 0u;
-            const float m = ld_cluster_f(&cM[h], r);
-            pm[q] = in ? m : -INFINITY;
-            pl[q] = ld_cluster_f(&cL[h], r);
-            px[q][0] = ld_cluster_f4(mine, r);
-            px[q][1] = ld_cluster_f4(mine + 1, r);
-          }
-          float Mn = M;
-#pragma unroll
-          for (int q = 0; q < kRound; ++q) Mn = fmaxf(Mn, pm[q]);
-          const float base = (Mn == -INFINITY) ? 0.f : Mn;
-          const float sc = exp2f(M - base);
-          L *= sc;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] *= sc;
-#pragma unroll
-          for (int q = 0; q < kRound; ++q) {
-            const float wt = exp2f(pm[q] - base);
-            L += wt * pl[q];
-            acc[0] += wt * px[q][0].x; acc[1] += wt * px[q][0].y;
-            acc[2] += wt * px[q][0].z; acc[3] += wt * px[q][0].w;
-            acc[4] += wt * px[q][1].x; acc[5] += wt * px[q][1].y;
-            acc[6] += wt * px[q][1].z; acc[7] += wt * px[q][1].w;
-          }
-          M = Mn;
+        for (int q = 0; q < sg; ++q) {
+          const float wt = exp2f(rM[e0 + q] - base);
+          L += wt * rL[e0 + q];
+          const float4* src = reinterpret_cast<const float4*>(rO + (e0 + q) * kHeadDim + d0);
+          const float4 x0 = src[0], x1 = src[1];
+          acc[0] += wt * x0.x; acc[1] += wt * x0.y; acc[2] += wt * x0.z; acc[3] += wt * x0.w;
+          acc[4] += wt * x1.x; acc[5] += wt * x1.y; acc[6] += wt * x1.z; acc[7] += wt * x1.w;
         }
         uint32_t pk[4];
 #pragma unroll
@@ -438,7 +421,6 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* m
         *reinterpret_cast<uint4*>(a.out + ((size_t)bg * kHeads + h) * kHeadDim + d0) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      cluster_sync();                          // #2: no CTA leaves while its partial may be read
       continue;
     }
     const long long first = (long long)bg * a.kslots, last = first + a.kslots - 1;

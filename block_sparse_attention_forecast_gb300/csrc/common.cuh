@@ -111,6 +111,14 @@ __device__ __forceinline__ float2 ld_cluster_f2(const void* p, uint32_t rank) {
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(cluster_addr(p, rank)) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_cluster_f(void* p, uint32_t rank, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(p, rank)), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f4(void* p, uint32_t rank, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr(p, rank)), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ float4 ld_cluster_f4(const void* p, uint32_t rank) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
