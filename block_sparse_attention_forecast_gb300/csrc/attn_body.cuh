@@ -20,9 +20,9 @@
 // At the end of a (sequence, group) in its range a CTA merges its eight warps' partial
 // results through shared memory (one write, one read of a padded buffer). A group covered by
 // one CTA is written out directly. Otherwise, in the cluster form (kClusterMerge: the standalone
-// launch with a whole number of CTAs per group, each group one thread-block cluster), the CTAs
-// exchange their (O, max, sum) through distributed shared memory and each combines a share of
-// the heads; in the general form each covering CTA stores (O, max, sum) to the workspace and
+// launch with a whole number of CTAs per group, each group one thread-block cluster), each CTA
+// pushes its (O, max, sum) of every head into the shared memory of the CTA that owns the head,
+// and after one cluster barrier each combines its share of the heads; in the general form each covering CTA stores (O, max, sum) to the workspace and
 // the last one to arrive (a counter in the workspace, which it resets) merges them with
 // log-sum-exp weights. Because ranges are contiguous, that merge overlaps the producer's loads
 // for the next group.
@@ -95,7 +95,7 @@ __device__ __forceinline__ GroupInfo group_info(const AttnArgs& a, int bg) {
 // The work of CTA c of `grid` CTAs that share the attention units. The tensor maps live in
 // the calling kernel's parameter space. kClusterMerge: CTA c is rank c % seg_per_group of a
 // cluster of seg_per_group CTAs that covers group c / seg_per_group (seg_per_group >= 2), and
-// every thread of the CTA reaches the two cluster barriers of the merge. tl_first (timeline
+// every thread of the CTA reaches the merge's one cluster barrier. tl_first (timeline
 // build only): thread 0 stores there the time its first block arrived.
 template <bool kClusterMerge = false>
 __device__ __forceinline__ void attn_cta(const AttnArgs& a, const CUtensorMap* mk, const CUtensorMap* mv,
